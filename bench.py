@@ -1,0 +1,388 @@
+"""Throughput of the FP4 routed-MoE layer on GB300.
+
+One step = one pass of the whole layer (routing, expert sort, W13 + SwiGLU,
+W2, combine) over one batch of synthetic inputs resident in HBM.  The
+default workload is the decode-shaped layer (T=32, d=4096, I=2048, E=256,
+k=8); the prefill-shaped layer (T=4608) is measured the same way and
+reported in the "prefill" object of the same line.  Every expert weight
+set touched per step (~2.2 GB decode, 3.4 GB prefill) is far larger than
+L2 (129 MB), so no L2 flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs under torchrun: every rank runs its own replica of the same
+workload (the layer has no data-path exchange here), timed between
+barriers; the max over ranks is taken and rank 0 prints one JSON line.
+``--impl reference`` times the CPU oracle on a bounded sample of the same
+workload on the host cores (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from moe_inputs import CONFIGS, make_config  # noqa: E402
+
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+STAGES = ["route", "gather", "w13_swiglu", "w2", "combine"]
+
+
+def peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def expert_bytes(d, I):
+    """packed codes + E8M0 scales of one expert: W13 [2I, d] and W2 [d, I]"""
+    w13 = 2 * I * d // 2 + 2 * I * d // 32
+    w2 = d * I // 2 + d * I // 32
+    return w13, w2
+
+
+# ----------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append((time.time(), ln.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = []
+        for ts, ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[5:]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        window = inside if inside else [r for r in rows if t0 - 0.3 <= r[0] <= t1 + 0.3]
+        if not window:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in window:
+            for name, v in zip(names, r[3][1:]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median([r[1] for r in window])), "sm_max_mhz": max(r[2] for r in window),
+                "reasons": sorted(reasons), "samples": len(inside)}
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+def dist_setup(n_gpus):
+    import torch
+    if n_gpus <= 1:
+        return 0, 1, 0, None
+    import torch.distributed as dist
+    rank = int(os.environ["RANK"])
+    world = int(os.environ["WORLD_SIZE"])
+    local = int(os.environ.get("LOCAL_RANK", rank))
+    torch.cuda.set_device(local)
+    dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return rank, world, local, dist
+
+
+def barrier(dist):
+    import torch
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+        torch.cuda.synchronize()
+
+
+def max_over_ranks(dist, v):
+    import torch
+    if dist is None:
+        return v
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def measure_workload(name, steps, warmup, dist, local, sampler=None):
+    """Time `steps` forward passes of one workload; returns a dict of results."""
+    import torch
+
+    import fp4_mixture_experts_gb300 as moe
+
+    L = make_config(name)
+    dev = torch.device("cuda", local)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    x = t(L.x_bf16.view(np.int16)).view(torch.bfloat16)
+    logits, w13, w13s, w2, w2s = t(L.router_logits), t(L.w13), t(L.w13_scale), t(L.w2), t(L.w2_scale)
+    ws = torch.empty(moe.workspace_bytes(L.T, L.d, L.I, L.E, L.k), dtype=torch.uint8, device=dev)
+    out = torch.empty(L.T, L.d, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    # per-step stage events; record each once so the handles exist
+    n_ev = 6
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ev)] for _ in range(steps)]
+    for row in evs:
+        for ev in row:
+            ev.record(stream)
+    r = moe.forward(x, logits, w13, w13s, w2, w2s, L.k, out=out, workspace=ws, return_routing=True)
+    torch.cuda.synchronize()
+    ids = r["topk_ids"].cpu().numpy()
+    touched = int(np.unique(ids).size)
+    for _ in range(warmup):
+        moe.forward(x, logits, w13, w13s, w2, w2s, L.k, out=out, workspace=ws)
+    barrier(dist)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    start.record(stream)
+    for s in range(steps):
+        moe.forward(x, logits, w13, w13s, w2, w2s, L.k, out=out, workspace=ws, stage_events=evs[s])
+    end.record(stream)
+    barrier(dist)
+    t_wall1 = time.time()
+    ms_total = start.elapsed_time(end)
+    stage_ms = {name_: float(np.mean([evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(steps)]))
+                for i, name_ in enumerate(STAGES)}
+    res = dict(L=L, touched=touched, ms_total=max_over_ranks(dist, ms_total), stage_ms=stage_ms,
+               t_wall=(t_wall0, t_wall1), tensors=(x, logits, w13, w13s, w2, w2s, ws))
+    return res
+
+
+def measure_e2e(res, steps, warmup, dist, local):
+    """Same metric through the host-buffer entry point: H2D of x and logits,
+    the layer, D2H of out, every step (pinned host memory)."""
+    import torch
+
+    import fp4_mixture_experts_gb300 as moe
+    L = res["L"]
+    _, _, w13, w13s, w2, w2s, _ = res["tensors"]
+    xh = torch.from_numpy(L.x_bf16.view(np.int16).copy()).view(torch.bfloat16).pin_memory()
+    lh = torch.from_numpy(L.router_logits.copy()).pin_memory()
+    oh = torch.empty(L.T, L.d, dtype=torch.float32).pin_memory()
+    dev = torch.device("cuda", local)
+    wsh = torch.empty(moe.host_workspace_bytes(L.T, L.d, L.I, L.E, L.k), dtype=torch.uint8, device=dev)
+    for _ in range(warmup):
+        moe.forward_host(xh, lh, w13, w13s, w2, w2s, L.k, out_host=oh, workspace=wsh)
+    barrier(dist)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        moe.forward_host(xh, lh, w13, w13s, w2, w2s, L.k, out_host=oh, workspace=wsh)
+    barrier(dist)
+    dt = max_over_ranks(dist, time.perf_counter() - t0)
+    h2d = L.x_bf16.nbytes + L.router_logits.nbytes
+    d2h = L.T * L.d * 4
+    return dt, h2d, d2h
+
+
+def roofline_decode(res, pk, src):
+    """Dominant kernel of the streaming path: W13 + SwiGLU (2/3 of the weight bytes)."""
+    L = res["L"]
+    w13b, w2b = expert_bytes(L.d, L.I)
+    st = res["stage_ms"]
+    w13_bytes = res["touched"] * w13b + L.T * L.d * 2
+    w2_bytes = res["touched"] * w2b
+    ach = w13_bytes / (st["w13_swiglu"] * 1e-3) / 1e9
+    step_bytes = w13_bytes + w2_bytes
+    return {"bound": "hbm", "kernel": "w13_swiglu", "achieved": round(ach, 1), "peak": pk["hbm_gbs"],
+            "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4), "traffic": None,
+            "peak_source": f"{src} hbm_gbs (copy, burst)",
+            "bytes_per_launch": w13_bytes,
+            "step_bytes": step_bytes,
+            "step_frac": round(step_bytes / (res["ms_total"] / res["steps"] * 1e-3) / 1e9 / pk["hbm_gbs"], 4)}
+
+
+def roofline_prefill(res, pk, src):
+    L = res["L"]
+    st = res["stage_ms"]
+    flops_w13 = 4.0 * L.T * L.k * L.d * L.I
+    ach = flops_w13 / (st["w13_swiglu"] * 1e-3) / 1e12
+    peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+    step_flops = 6.0 * L.T * L.k * L.d * L.I
+    return {"bound": "tensor", "kernel": "w13_swiglu", "achieved": round(ach, 1), "peak": peak,
+            "unit": "TFLOP/s", "frac": round(ach / peak, 4), "traffic": None,
+            "peak_source": f"{src} bf16_tflops_sustained (cuBLAS bf16 loop)",
+            "flops_per_launch": flops_w13,
+            "step_frac": round(step_flops / (res["ms_total"] / res["steps"] * 1e-3) / 1e12 / peak, 4)}
+
+
+def cpu_baseline_sample(name, seconds_target=15.0):
+    """The oracle, as it stands, on a bounded sample of the workload: whole
+    tokens through oracle.forward_tokens until ~seconds_target elapse."""
+    import oracle
+    L = make_config(name)
+    toks = 0
+    t0 = time.perf_counter()
+    for t in range(L.T):
+        oracle.forward_tokens(L.x_bf16, L.router_logits, L.w13, L.w13_scale, L.w2, L.w2_scale, L.k, [t])
+        toks += 1
+        if time.perf_counter() - t0 >= seconds_target:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(toks / dt, 4), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{toks} of {L.T} tokens of the {name} layer, one token per oracle call "
+                      f"(numpy fp64, BLAS threads = host cores), {dt:.1f} s"}
+
+
+def run_ours(args):
+    import torch
+    rank, world, local, dist = dist_setup(args.gpus)
+    pk, src = peaks()
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    dec = measure_workload("decode", args.steps, args.warmup, dist, local)
+    dec["steps"] = args.steps
+    t0, t1 = dec["t_wall"]
+    clocks = sampler.summary(t0, t1) if sampler else None
+    e2e_dt, h2d, d2h = measure_e2e(dec, args.steps, args.warmup, dist, local)
+    pre = None
+    if not args.no_prefill:
+        pre_steps = max(3, min(args.steps, 50))
+        pre = measure_workload("prefill", pre_steps, max(3, min(args.warmup, 5)), dist, local)
+        pre["steps"] = pre_steps
+    if sampler:
+        sampler.stop()
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    L = dec["L"]
+    ms_step = dec["ms_total"] / args.steps
+    value = world * L.T * args.steps / (dec["ms_total"] * 1e-3)
+    launches_per_step = 6  # route_hist, sort_scan, scatter, w13_swiglu, w2, combine
+    line = {
+        "metric": "routed-MoE tokens/s (decode T=32, prefill T=4608); % of HBM/tensor roofline",
+        "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp4(e2m1)xbf16->f32", "data": "synthetic",
+        "config": {"workload": "decode-shaped MoE layer T=32 d=4096 I=2048 E=256 k=8 (seed 0)",
+                   "global_batch": world * L.T, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (touched weights %.2f GB)" % (
+                       dec["touched"] * sum(expert_bytes(L.d, L.I)) / 1e9),
+                   "touched_experts": dec["touched"]},
+        "stage_ms": {k: round(v, 5) for k, v in dec["stage_ms"].items()},
+        "roofline": roofline_decode(dec, pk, src),
+        "gpu_launches": launches_per_step * args.steps,
+        "e2e": {"value": round(world * L.T * args.steps / e2e_dt, 1), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "clocks": clocks,
+    }
+    if pre is not None:
+        P = pre["L"]
+        ms_pre = pre["ms_total"] / pre["steps"]
+        line["prefill"] = {
+            "workload": "prefill-shaped MoE layer T=4608 d=4096 I=2048 E=256 k=8 (seed 0)",
+            "value": round(world * P.T / (ms_pre * 1e-3), 1), "unit": "tokens/s", "steps": pre["steps"],
+            "ms_per_step": round(ms_pre, 4), "stage_ms": {k: round(v, 4) for k, v in pre["stage_ms"].items()},
+            "roofline": roofline_prefill(pre, pk, src)}
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_sample("decode", args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------
+# reference arm: the CPU oracle on the host cores
+# ----------------------------------------------------------------------------
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import oracle
+    L = make_config("decode")
+    # one step = one token of the decode layer through the oracle
+    for s in range(args.warmup):
+        oracle.forward_tokens(L.x_bf16, L.router_logits, L.w13, L.w13_scale, L.w2, L.w2_scale, L.k, [s % L.T])
+    per_step_cap = max(0.05, 150.0 / max(1, args.steps))
+    t0 = time.perf_counter()
+    units = 0.0
+    for s in range(args.steps):
+        ts = time.perf_counter()
+        t = s % L.T
+        ids, _ = oracle.route(L.router_logits[t:t + 1], L.k)
+        # experts of this token, one oracle expert evaluation at a time, until the per-step cap
+        done = 0
+        x = oracle.bf16_bits_to_f64(L.x_bf16[t:t + 1])
+        for e in ids[0]:
+            oracle.expert_ffn(x, L.w13[e], L.w13_scale[e], L.w2[e], L.w2_scale[e])
+            done += 1
+            if time.perf_counter() - ts > per_step_cap:
+                break
+        units += done / L.k
+    dt = time.perf_counter() - t0
+    value = units / dt
+    line = {"impl": "reference", "metric": "routed-MoE tokens/s (decode T=32, prefill T=4608); % of HBM/tensor roofline",
+            "value": round(value, 4), "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "decode-shaped MoE layer T=32 d=4096 I=2048 E=256 k=8 (seed 0)"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": f"{units:.3f} tokens (one token, or part of its {L.k} experts, per step)"},
+            "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

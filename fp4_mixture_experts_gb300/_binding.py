@@ -1,0 +1,218 @@
+"""ctypes binding of libmoe_fp4.so: argument marshalling only.
+
+Each function mirrors one C entry point of include/moe_fp4.h and takes torch
+tensors (device tensors unless stated), passing their data pointers and the
+current CUDA stream.  A nonzero status becomes a MoeFp4Error.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_NAME = "libmoe_fp4.so"
+
+FLAG_FORCE_GEMV = 0x1
+FLAG_FORCE_TC = 0x2
+
+EXPORTED_SYMBOLS = (
+    "moe_fp4_workspace_bytes",
+    "moe_fp4_host_workspace_bytes",
+    "moe_fp4_route",
+    "moe_fp4_forward",
+    "moe_fp4_forward_profiled",
+    "moe_fp4_forward_host",
+    "moe_fp4_check",
+    "moe_fp4_status_string",
+)
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("d", ctypes.c_int32), ("I", ctypes.c_int32),
+                ("E", ctypes.c_int32), ("k", ctypes.c_int32)]
+
+
+class MoeFp4Error(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+
+
+_lib = None
+
+
+def lib_path() -> str:
+    return os.environ.get("MOE_FP4_LIB", os.path.join(PKG, _LIB_NAME))
+
+
+def load_library():
+    """Load the in-tree library (built by fp4_mixture_experts_gb300.build); raises if missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = lib_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with `python -m fp4_mixture_experts_gb300.build` "
+                           "(there is no fallback implementation)")
+    lib = ctypes.CDLL(path)
+    P = ctypes.c_void_p
+    pd = ctypes.POINTER(Dims)
+    lib.moe_fp4_workspace_bytes.argtypes = [pd]
+    lib.moe_fp4_workspace_bytes.restype = ctypes.c_size_t
+    lib.moe_fp4_host_workspace_bytes.argtypes = [pd]
+    lib.moe_fp4_host_workspace_bytes.restype = ctypes.c_size_t
+    lib.moe_fp4_route.argtypes = [pd, P, P, P, P, P, P, ctypes.c_size_t, P]
+    lib.moe_fp4_route.restype = ctypes.c_int
+    lib.moe_fp4_forward.argtypes = [pd, P, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_uint, P, ctypes.c_size_t, P]
+    lib.moe_fp4_forward.restype = ctypes.c_int
+    lib.moe_fp4_forward_profiled.argtypes = lib.moe_fp4_forward.argtypes + [ctypes.POINTER(ctypes.c_void_p)]
+    lib.moe_fp4_forward_profiled.restype = ctypes.c_int
+    lib.moe_fp4_forward_host.argtypes = [pd, P, P, P, P, P, P, P, ctypes.c_uint, P, ctypes.c_size_t, P]
+    lib.moe_fp4_forward_host.restype = ctypes.c_int
+    lib.moe_fp4_check.argtypes = [P, P]
+    lib.moe_fp4_check.restype = ctypes.c_int
+    lib.moe_fp4_status_string.argtypes = [ctypes.c_int]
+    lib.moe_fp4_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load_library().moe_fp4_status_string(int(status)).decode()
+
+
+def _dims(T, d, I, E, k) -> Dims:
+    return Dims(int(T), int(d), int(I), int(E), int(k))
+
+
+def workspace_bytes(T, d, I, E, k) -> int:
+    return int(load_library().moe_fp4_workspace_bytes(ctypes.byref(_dims(T, d, I, E, k))))
+
+
+def host_workspace_bytes(T, d, I, E, k) -> int:
+    return int(load_library().moe_fp4_host_workspace_bytes(ctypes.byref(_dims(T, d, I, E, k))))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _workspace(nbytes, device, workspace):
+    import torch
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device)
+    if workspace.numel() < nbytes:
+        raise ValueError(f"workspace has {workspace.numel()} bytes, needs {nbytes}")
+    return workspace
+
+
+def route(router_logits, k: int, d: int = 128, I: int = 128, workspace=None, stream=None):
+    """Top-k routing and the expert sort.  router_logits: fp32 [T, E] on the GPU.
+
+    Returns (topk_ids int32 [T, k], topk_weights fp32 [T, k], expert_offsets int32 [E+1],
+    sorted_slot int32 [T*k]).  d and I only size the workspace (the routing part does not use them).
+    """
+    import torch
+    T, E = router_logits.shape
+    dims = _dims(T, d, I, E, k)
+    lib = load_library()
+    nbytes = lib.moe_fp4_workspace_bytes(ctypes.byref(dims))
+    if nbytes == 0:
+        raise MoeFp4Error(-2, "moe_fp4_route")
+    dev = router_logits.device
+    ws = _workspace(nbytes, dev, workspace)
+    ids = torch.empty(T, k, dtype=torch.int32, device=dev)
+    w = torch.empty(T, k, dtype=torch.float32, device=dev)
+    off = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    ss = torch.empty(T * k, dtype=torch.int32, device=dev)
+    rc = lib.moe_fp4_route(ctypes.byref(dims), _ptr(router_logits), _ptr(ids), _ptr(w), _ptr(off), _ptr(ss),
+                           _ptr(ws), ws.numel(), _stream(stream))
+    if rc != 0:
+        raise MoeFp4Error(rc, "moe_fp4_route")
+    return ids, w, off, ss
+
+
+def forward(x_bf16, router_logits, w13, w13_scale, w2, w2_scale, k: int, out=None, flags: int = 0,
+            workspace=None, return_routing: bool = False, return_h: bool = False, stream=None,
+            stage_events=None):
+    """The whole layer on device tensors.
+
+    x_bf16: bf16 [T, d]; router_logits: fp32 [T, E]; w13: uint8 [E, 2I, d/2];
+    w13_scale: uint8 [E, 2I, d/32]; w2: uint8 [E, d, I/2]; w2_scale: uint8 [E, d, I/32].
+    Returns out fp32 [T, d], or a dict with out and the requested extras.
+    """
+    import torch
+    T, d = x_bf16.shape
+    E, twoI, _ = w13.shape
+    I = twoI // 2
+    dims = _dims(T, d, I, E, k)
+    lib = load_library()
+    nbytes = lib.moe_fp4_workspace_bytes(ctypes.byref(dims))
+    if nbytes == 0:
+        raise MoeFp4Error(-2, "moe_fp4_forward")
+    dev = x_bf16.device
+    ws = _workspace(nbytes, dev, workspace)
+    if out is None:
+        out = torch.empty(T, d, dtype=torch.float32, device=dev)
+    extras = {}
+    if return_routing:
+        extras = dict(topk_ids=torch.empty(T, k, dtype=torch.int32, device=dev),
+                      topk_weights=torch.empty(T, k, dtype=torch.float32, device=dev),
+                      expert_offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+                      sorted_slot=torch.empty(T * k, dtype=torch.int32, device=dev))
+    if return_h:
+        extras["h"] = torch.empty(T * k, I, dtype=torch.bfloat16, device=dev)
+    args = [ctypes.byref(dims), _ptr(x_bf16), _ptr(router_logits), _ptr(w13), _ptr(w13_scale),
+            _ptr(w2), _ptr(w2_scale), _ptr(out), _ptr(extras.get("topk_ids")),
+            _ptr(extras.get("topk_weights")), _ptr(extras.get("expert_offsets")),
+            _ptr(extras.get("sorted_slot")), _ptr(extras.get("h")), int(flags), _ptr(ws),
+            ws.numel(), _stream(stream)]
+    if stage_events is not None:
+        # torch.cuda.Event handles; each must have been recorded once so that it exists
+        arr = (ctypes.c_void_p * len(stage_events))(*[ctypes.c_void_p(ev.cuda_event) for ev in stage_events])
+        rc = lib.moe_fp4_forward_profiled(*args, arr)
+    else:
+        rc = lib.moe_fp4_forward(*args)
+    if rc != 0:
+        raise MoeFp4Error(rc, "moe_fp4_forward")
+    if extras:
+        extras["out"] = out
+        return extras
+    return out
+
+
+def forward_host(x_bf16_host, router_logits_host, w13, w13_scale, w2, w2_scale, k: int, out_host=None,
+                 flags: int = 0, workspace=None, stream=None):
+    """The whole layer with HOST x (bf16 [T, d]), router_logits (fp32 [T, E]) and out (fp32 [T, d]);
+    the weights are device tensors.  Synchronises before returning."""
+    import torch
+    T, d = x_bf16_host.shape
+    E, twoI, _ = w13.shape
+    I = twoI // 2
+    dims = _dims(T, d, I, E, k)
+    lib = load_library()
+    nbytes = lib.moe_fp4_host_workspace_bytes(ctypes.byref(dims))
+    if nbytes == 0:
+        raise MoeFp4Error(-2, "moe_fp4_forward_host")
+    ws = _workspace(nbytes, w13.device, workspace)
+    if out_host is None:
+        out_host = torch.empty(T, d, dtype=torch.float32, pin_memory=x_bf16_host.is_pinned())
+    rc = lib.moe_fp4_forward_host(ctypes.byref(dims), _ptr(x_bf16_host), _ptr(router_logits_host), _ptr(w13),
+                                  _ptr(w13_scale), _ptr(w2), _ptr(w2_scale), _ptr(out_host), int(flags), _ptr(ws),
+                                  ws.numel(), _stream(stream))
+    if rc != 0:
+        raise MoeFp4Error(rc, "moe_fp4_forward_host")
+    return out_host
+
+
+def check(workspace, stream=None) -> None:
+    """Synchronise and raise if a kernel reported an out-of-range index."""
+    rc = load_library().moe_fp4_check(_ptr(workspace), _stream(stream))
+    if rc != 0:
+        raise MoeFp4Error(rc, "moe_fp4_check")

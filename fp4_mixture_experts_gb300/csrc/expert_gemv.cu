@@ -1,0 +1,208 @@
+// Expert projections on CUDA cores (every shape), the token gather and the
+// weighted combine.
+//
+// w13_swiglu_rows: one warp per (gate row i, up row I+i) pair and a chunk of
+//   up to 4 token rows of one expert; lanes split K in 32-element MX blocks
+//   (16 packed bytes + 1 E8M0 byte), decode E2M1 pairs with the hardware
+//   cvt.rn.f16x2.e2m1x2, accumulate in fp32, reduce across the warp and apply
+//   SwiGLU; h is rounded to bf16 (the layer's one rounding point).
+// w2_rows: the same pattern over W2 rows, fp32 y in sorted-row order.
+// combine: out[t] = sum_j w[t, j] * y[slot_pos[t*k + j]] in slot order
+//   (deterministic: no atomics, the MI250 blog's section 3.2 / 4.2 rule).
+#include <cuda_fp16.h>
+
+#include "moe_fp4_internal.cuh"
+
+namespace moe_fp4 {
+namespace {
+
+constexpr int kRowsThreads = 256;  // 8 warps, one row (pair) each
+
+__device__ __forceinline__ uint4 ldg_nc_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// 16 packed bytes (32 E2M1 codes, K ascending) -> 32 fp32 values (unscaled)
+__device__ __forceinline__ void decode32(const uint4 p, float v[32]) {
+  const uint32_t w[4] = {p.x, p.y, p.z, p.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const uint32_t h2 = e2m1x2_to_f16x2((w[q] >> (8 * b)) & 0xFFu);
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+      v[q * 8 + b * 2 + 0] = f.x;
+      v[q * 8 + b * 2 + 1] = f.y;
+    }
+  }
+}
+
+// sum_{j<32} v[j] * x[j] with x 32 consecutive bf16 at p (64 bytes, 16-byte aligned)
+__device__ __forceinline__ float dot32_bf16(const float v[32], const uint16_t* p) {
+  float s = 0.f;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint4 q = *reinterpret_cast<const uint4*>(p + 8 * c);
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      s = fmaf(v[c * 8 + 2 * i + 0], bf16_to_f32(w[i] & 0xFFFFu), s);
+      s = fmaf(v[c * 8 + 2 * i + 1], bf16_to_f32(w[i] >> 16), s);
+    }
+  }
+  return s;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+__global__ void __launch_bounds__(kRowsThreads)
+w13_swiglu_rows_kernel(const uint16_t* __restrict__ x, const uint8_t* __restrict__ w13,
+                       const uint8_t* __restrict__ w13s, const int4* __restrict__ chunks,
+                       const int32_t* __restrict__ counts, const int32_t* __restrict__ sorted_slot,
+                       int k, int d, int I, uint16_t* __restrict__ h) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int i = blockIdx.x * (kRowsThreads / 32) + warp;
+  if (i >= I) return;
+  const int n_chunks = counts[1];
+  const int nkb = d / 32;
+  for (int c = blockIdx.y; c < n_chunks; c += gridDim.y) {
+    const int4 ch = chunks[c];
+    const int e = ch.x, row0 = ch.y, mt = ch.z;
+    int tok[kGemvTokens];
+#pragma unroll
+    for (int q = 0; q < kGemvTokens; ++q) tok[q] = q < mt ? sorted_slot[row0 + q] / k : 0;
+    const size_t gate_row = (size_t)e * 2 * I + i, up_row = gate_row + I;
+    const uint8_t* wg = w13 + gate_row * (d / 2);
+    const uint8_t* wu = w13 + up_row * (d / 2);
+    const uint8_t* sg = w13s + gate_row * nkb;
+    const uint8_t* su = w13s + up_row * nkb;
+    float ag[kGemvTokens] = {}, au[kGemvTokens] = {};
+    for (int kb = lane; kb < nkb; kb += 32) {
+      float vg[32], vu[32];
+      decode32(ldg_nc_v4(wg + kb * 16), vg);
+      decode32(ldg_nc_v4(wu + kb * 16), vu);
+      const float scg = e8m0_to_f32(sg[kb]), scu = e8m0_to_f32(su[kb]);
+#pragma unroll
+      for (int q = 0; q < kGemvTokens; ++q) {
+        if (q < mt) {
+          const uint16_t* xr = x + (size_t)tok[q] * d + kb * 32;
+          ag[q] = fmaf(scg, dot32_bf16(vg, xr), ag[q]);
+          au[q] = fmaf(scu, dot32_bf16(vu, xr), au[q]);
+        }
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < kGemvTokens; ++q) {
+      const float g = warp_sum(ag[q]), u = warp_sum(au[q]);
+      if (lane == 0 && q < mt) h[(size_t)(row0 + q) * I + i] = f32_to_bf16_rn(swiglu(g, u));
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kRowsThreads)
+w2_rows_kernel(const uint16_t* __restrict__ h, const uint8_t* __restrict__ w2,
+               const uint8_t* __restrict__ w2s, const int4* __restrict__ chunks,
+               const int32_t* __restrict__ counts, int d, int I, float* __restrict__ y) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = blockIdx.x * (kRowsThreads / 32) + warp;
+  if (n >= d) return;
+  const int n_chunks = counts[1];
+  const int nkb = I / 32;
+  for (int c = blockIdx.y; c < n_chunks; c += gridDim.y) {
+    const int4 ch = chunks[c];
+    const int e = ch.x, row0 = ch.y, mt = ch.z;
+    const size_t row = (size_t)e * d + n;
+    const uint8_t* wr = w2 + row * (I / 2);
+    const uint8_t* sr = w2s + row * nkb;
+    float acc[kGemvTokens] = {};
+    for (int kb = lane; kb < nkb; kb += 32) {
+      float v[32];
+      decode32(ldg_nc_v4(wr + kb * 16), v);
+      const float sc = e8m0_to_f32(sr[kb]);
+#pragma unroll
+      for (int q = 0; q < kGemvTokens; ++q)
+        if (q < mt) acc[q] = fmaf(sc, dot32_bf16(v, h + (size_t)(row0 + q) * I + kb * 32), acc[q]);
+    }
+#pragma unroll
+    for (int q = 0; q < kGemvTokens; ++q) {
+      const float s = warp_sum(acc[q]);
+      if (lane == 0 && q < mt) y[(size_t)(row0 + q) * d + n] = s;
+    }
+  }
+}
+
+// x_perm[r] = x[sorted_slot[r] / k]; one warp per row, 16-byte copies
+__global__ void __launch_bounds__(256)
+gather_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ sorted_slot, int S, int k,
+              int d, uint16_t* __restrict__ x_perm) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  const int nwarps = (gridDim.x * blockDim.x) >> 5;
+  const int vec = d / 8;
+  for (int r = warp; r < S; r += nwarps) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(sorted_slot[r] / k) * d);
+    uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)r * d);
+    for (int v = lane; v < vec; v += 32) dst[v] = src[v];
+  }
+}
+
+__global__ void __launch_bounds__(256)
+combine_kernel(const float* __restrict__ y, const float* __restrict__ topk_w,
+               const int32_t* __restrict__ slot_pos, int T, int k, int d, float* __restrict__ out) {
+  const int t = blockIdx.x;
+  if (t >= T) return;
+  const int vec = d / 4;
+  for (int v = threadIdx.x; v < vec; v += blockDim.x) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < k; ++j) {
+      const float w = topk_w[(size_t)t * k + j];
+      const float4 yv = reinterpret_cast<const float4*>(y + (size_t)slot_pos[(size_t)t * k + j] * d)[v];
+      acc.x = fmaf(w, yv.x, acc.x);
+      acc.y = fmaf(w, yv.y, acc.y);
+      acc.z = fmaf(w, yv.z, acc.z);
+      acc.w = fmaf(w, yv.w, acc.w);
+    }
+    reinterpret_cast<float4*>(out + (size_t)t * d)[v] = acc;
+  }
+}
+
+int grid_chunks(const Workspace& ws) { return ws.max_gemv_chunks < 65535 ? ws.max_gemv_chunks : 65535; }
+
+}  // namespace
+
+cudaError_t launch_gemv_w13(const moe_fp4_dims& d, const uint16_t* x, const uint8_t* w13,
+                            const uint8_t* w13s, const Workspace& ws, cudaStream_t st) {
+  dim3 grid((d.I + 7) / 8, grid_chunks(ws));
+  w13_swiglu_rows_kernel<<<grid, kRowsThreads, 0, st>>>(x, w13, w13s, ws.gemv_chunks, ws.counts,
+                                                        ws.sorted_slot, d.k, d.d, d.I, ws.h);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemv_w2(const moe_fp4_dims& d, const uint8_t* w2, const uint8_t* w2s,
+                           const Workspace& ws, cudaStream_t st) {
+  dim3 grid((d.d + 7) / 8, grid_chunks(ws));
+  w2_rows_kernel<<<grid, kRowsThreads, 0, st>>>(ws.h, w2, w2s, ws.gemv_chunks, ws.counts, d.d, d.I, ws.y);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const moe_fp4_dims& d, const uint16_t* x, const Workspace& ws, cudaStream_t st) {
+  const int S = d.T * d.k;
+  int blocks = (S + 7) / 8;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  gather_kernel<<<blocks, 256, 0, st>>>(x, ws.sorted_slot, S, d.k, d.d, ws.x_perm);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const moe_fp4_dims& d, float* out, const Workspace& ws, cudaStream_t st) {
+  combine_kernel<<<d.T, 256, 0, st>>>(ws.y, ws.topk_w, ws.slot_pos, d.T, d.k, d.d, out);
+  return cudaGetLastError();
+}
+
+}  // namespace moe_fp4

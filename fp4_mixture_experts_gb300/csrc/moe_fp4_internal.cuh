@@ -1,0 +1,92 @@
+// Internal declarations shared by the CUDA translation units of the FP4
+// routed-MoE library: workspace layout, launch helpers and small device
+// utilities (MXFP4 decoding, bf16 rounding).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe_fp4.h"
+
+namespace moe_fp4 {
+
+constexpr int kRouteTokensPerBlock = 32;   // tokens per routing block (8 warps x 4)
+constexpr int kRouteThreads = 256;
+constexpr int kGemvTokens = 4;             // token rows per GEMV chunk (registers hold x for 4 rows)
+constexpr int kTcTileN = 128;              // token rows per tensor-core tile (UMMA N)
+
+// Device error word values (moe_fp4_check).
+constexpr int kErrBadExpertId = 1;
+
+// Pointers into the caller's workspace; every region starts on a 256-byte boundary.
+struct Workspace {
+  int32_t* err;           // [4]    device error words
+  int32_t* counts;        // [4]    n_active, n_gemv_chunks, n_tc_tiles, 0
+  int32_t* active;        // [E]    experts with >= 1 row, ascending
+  int32_t* block_hist;    // [nb*E] per routing block expert counts, then bases
+  int32_t* topk_ids;      // [S]
+  float* topk_w;          // [S]
+  int32_t* offsets;       // [E+1]
+  int32_t* sorted_slot;   // [S]
+  int32_t* slot_pos;      // [S]
+  int4* gemv_chunks;      // [max_gemv_chunks]  (expert, first sorted row, rows, 0)
+  int4* tc_tiles;         // [max_tc_tiles]     (expert, first sorted row, rows, 0)
+  uint16_t* x_perm;       // [S, d] bf16 (tensor-core path)
+  uint16_t* h;            // [S, I] bf16
+  float* y;               // [S, d] fp32 expert outputs in sorted-row order
+  // staging for the host-buffer entry point (only laid out when requested)
+  uint16_t* stage_x;      // [T, d]
+  float* stage_logits;    // [T, E]
+  float* stage_out;       // [T, d]
+  size_t total;
+  int nb_route;
+  int max_gemv_chunks;
+  int max_tc_tiles;
+};
+
+// Lays the workspace out from `base` (nullptr: sizes only).  Returns false for
+// unsupported sizes.
+bool layout_workspace(const moe_fp4_dims& d, void* base, bool with_staging, Workspace* ws);
+
+// ---- launchers (one per kernel family; each returns cudaGetLastError()) ----
+cudaError_t launch_route(const moe_fp4_dims& d, const float* logits, const Workspace& ws, cudaStream_t st);
+cudaError_t launch_gather(const moe_fp4_dims& d, const uint16_t* x, const Workspace& ws, cudaStream_t st);
+cudaError_t launch_gemv_w13(const moe_fp4_dims& d, const uint16_t* x, const uint8_t* w13,
+                            const uint8_t* w13s, const Workspace& ws, cudaStream_t st);
+cudaError_t launch_gemv_w2(const moe_fp4_dims& d, const uint8_t* w2, const uint8_t* w2s,
+                           const Workspace& ws, cudaStream_t st);
+cudaError_t launch_combine(const moe_fp4_dims& d, float* out, const Workspace& ws, cudaStream_t st);
+
+// ---------------------------------------------------------------------------
+// device helpers
+// ---------------------------------------------------------------------------
+#ifdef __CUDACC__
+
+// Two E2M1 codes (one byte, low nibble first) -> two exact halves.
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b;\n\tcvt.u8.u32 b, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, b;\n}" : "=r"(r) : "r"(byte));
+  return r;
+}
+
+// E8M0 byte -> fp32 2^(s-127); 0 maps to the subnormal 2^-127, 0xFF to NaN.
+__device__ __forceinline__ float e8m0_to_f32(uint32_t s) {
+  uint32_t bits = s == 0 ? 0x00400000u : (s == 255 ? 0x7FC00000u : (s << 23));
+  return __uint_as_float(bits);
+}
+
+// bf16 bits -> fp32
+__device__ __forceinline__ float bf16_to_f32(uint32_t b16) { return __uint_as_float(b16 << 16); }
+
+// fp32 -> bf16 bits, round to nearest even (the CUDA intrinsic).
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+// silu(z) * u in fp32 with an IEEE exp and divide
+__device__ __forceinline__ float swiglu(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+
+#endif
+
+}  // namespace moe_fp4

@@ -1,0 +1,225 @@
+// Routing (top-k with a fixed tie-break and softmax over the picked logits)
+// and the stable counting sort of the T*k slots by expert.
+//
+// Top-k follows the MI250 correctness blog (section 4.1 table: fp32
+// comparison and a fixed tie-break; section 4.2: ties go to the lower
+// expert id, never to memory order).  The sort is the "expert sorting" step
+// of the DeepSeek-V4-Flash-on-gfx90a paper's prefill path: a stable
+// counting sort, so the permutation is unique and reproducible.
+//
+// Three kernels:
+//   route_hist  one warp per token: k rounds of a warp-wide argmax over the
+//               token's E logits, softmax of the k picked, per-block counts
+//   sort_scan   one block: per-expert totals, offsets, per-block bases, the
+//               list of non-empty experts and the work lists of the expert
+//               kernels (so the host never reads a count)
+//   scatter     one block per routing block: stable ranks by warp match,
+//               writes sorted_slot and its inverse
+#include "moe_fp4_internal.cuh"
+
+namespace moe_fp4 {
+namespace {
+
+constexpr int kWarps = kRouteThreads / 32;
+constexpr int kTokPerWarp = kRouteTokensPerBlock / kWarps;
+
+// Order-preserving map of a finite fp32 to uint32 (-0 folded onto +0).
+__device__ __forceinline__ uint32_t ordered_key(float v) {
+  uint32_t u = __float_as_uint(v == 0.0f ? 0.0f : v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__global__ void __launch_bounds__(kRouteThreads)
+route_hist_kernel(const float* __restrict__ logits, int T, int E, int k,
+                  int32_t* __restrict__ topk_ids, float* __restrict__ topk_w,
+                  int32_t* __restrict__ block_hist, int32_t* __restrict__ err) {
+  extern __shared__ float smem[];
+  // the error words start clear on every call (later kernels of the call set them)
+  if (blockIdx.x == 0 && threadIdx.x < 4) err[threadIdx.x] = 0;
+  float* rows = smem;                                   // [kWarps][E]
+  int* hist = reinterpret_cast<int*>(smem + kWarps * E);  // [E]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  float* row = rows + warp * E;
+  const int nv = (E + 31) >> 5;  // entries per lane: e = lane + 32 i
+  for (int tt = 0; tt < kTokPerWarp; ++tt) {
+    const int t = blockIdx.x * kRouteTokensPerBlock + warp * kTokPerWarp + tt;
+    if (t >= T) break;
+    const float* src = logits + (size_t)t * E;
+    for (int e = lane; e < E; e += 32) row[e] = src[e];
+    __syncwarp();
+    uint32_t taken = 0;  // bit i: entry lane + 32 i already picked
+    int my_id = 0;
+    float my_val = 0.f;
+    for (int r = 0; r < k; ++r) {
+      unsigned long long best = 0;
+      for (int i = 0; i < nv; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && !((taken >> i) & 1u)) {
+          unsigned long long key = ((unsigned long long)ordered_key(row[e]) << 32) | (0xFFFFFFFFu - (uint32_t)e);
+          best = key > best ? key : best;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+        best = other > best ? other : best;
+      }
+      const int e_star = (int)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFu));
+      if ((e_star & 31) == lane) taken |= 1u << (e_star >> 5);
+      if (lane == r) {
+        my_id = e_star;
+        my_val = row[e_star];
+      }
+    }
+    // softmax over the k picked logits, shifted by the slot-0 logit; the sum
+    // runs in slot order
+    const float m = __shfl_sync(0xFFFFFFFFu, my_val, 0);
+    const float ex = lane < k ? expf(my_val - m) : 0.f;
+    float sum = 0.f;
+    for (int j = 0; j < k; ++j) sum += __shfl_sync(0xFFFFFFFFu, ex, j);
+    if (lane < k) {
+      topk_ids[(size_t)t * k + lane] = my_id;
+      topk_w[(size_t)t * k + lane] = ex / sum;
+      atomicAdd(&hist[my_id], 1);
+    }
+    __syncwarp();
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) block_hist[(size_t)blockIdx.x * E + e] = hist[e];
+}
+
+// Exclusive scan over the block (blockDim.x <= 1024, a multiple of 32).
+__device__ int block_exclusive_scan(int v, int* scratch /* [32] */, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  __syncthreads();
+  if (lane == 31) scratch[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int nw = blockDim.x >> 5;
+    int w = lane < nw ? scratch[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int n = __shfl_up_sync(0xFFFFFFFFu, wi, o);
+      if (lane >= o) wi += n;
+    }
+    scratch[lane] = wi - w;  // exclusive prefix of warp totals
+    if (lane == 31) scratch[32] = wi;
+  }
+  __syncthreads();
+  const int res = scratch[warp] + incl - v;
+  *total = scratch[32];
+  __syncthreads();
+  return res;
+}
+
+__global__ void __launch_bounds__(1024)
+sort_scan_kernel(int32_t* __restrict__ block_hist, int nb, int E, int32_t* __restrict__ offsets,
+                 int32_t* __restrict__ active, int32_t* __restrict__ counts,
+                 int4* __restrict__ gemv_chunks, int4* __restrict__ tc_tiles) {
+  __shared__ int scratch[33];
+  const int e = threadIdx.x;
+  const bool ok = e < E;
+  int cnt = 0;
+  if (ok)
+    for (int b = 0; b < nb; ++b) cnt += block_hist[(size_t)b * E + e];
+  int total;
+  const int off = block_exclusive_scan(ok ? cnt : 0, scratch, &total);
+  if (ok) {
+    offsets[e] = off;
+    int run = off;
+    for (int b = 0; b < nb; ++b) {
+      const int c = block_hist[(size_t)b * E + e];
+      block_hist[(size_t)b * E + e] = run;
+      run += c;
+    }
+  }
+  if (e == 0) offsets[E] = total;
+  // non-empty experts
+  int n_active;
+  const int apos = block_exclusive_scan(ok && cnt > 0 ? 1 : 0, scratch, &n_active);
+  if (ok && cnt > 0) active[apos] = e;
+  // GEMV chunks of up to kGemvTokens rows
+  const int nch = ok ? (cnt + kGemvTokens - 1) / kGemvTokens : 0;
+  int n_chunks;
+  const int cpos = block_exclusive_scan(nch, scratch, &n_chunks);
+  for (int c = 0; c < nch; ++c)
+    gemv_chunks[cpos + c] = make_int4(e, off + c * kGemvTokens, min(kGemvTokens, cnt - c * kGemvTokens), 0);
+  // tensor-core tiles of up to kTcTileN rows
+  const int ntl = ok ? (cnt + kTcTileN - 1) / kTcTileN : 0;
+  int n_tiles;
+  const int tpos = block_exclusive_scan(ntl, scratch, &n_tiles);
+  for (int c = 0; c < ntl; ++c)
+    tc_tiles[tpos + c] = make_int4(e, off + c * kTcTileN, min(kTcTileN, cnt - c * kTcTileN), 0);
+  if (e == 0) {
+    counts[0] = n_active;
+    counts[1] = n_chunks;
+    counts[2] = n_tiles;
+    counts[3] = 0;
+  }
+}
+
+__global__ void __launch_bounds__(kRouteThreads)
+scatter_kernel(const int32_t* __restrict__ topk_ids, const int32_t* __restrict__ block_base, int T,
+               int E, int k, int32_t* __restrict__ sorted_slot, int32_t* __restrict__ slot_pos,
+               int32_t* __restrict__ err) {
+  extern __shared__ int sm[];
+  int* running = sm;            // [E]
+  int* wcnt = sm + E;           // [kWarps][E]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) running[e] = block_base[(size_t)blockIdx.x * E + e];
+  for (int i = threadIdx.x; i < kWarps * E; i += blockDim.x) wcnt[i] = 0;
+  __syncthreads();
+  const long f_begin = (long)blockIdx.x * kRouteTokensPerBlock * k;
+  const long f_end = min((long)(blockIdx.x + 1) * kRouteTokensPerBlock, (long)T) * k;
+  for (long f0 = f_begin; f0 < f_end; f0 += blockDim.x) {
+    const long f = f0 + threadIdx.x;
+    int e = f < f_end ? topk_ids[f] : -1;
+    if (e >= E || e < -1) {  // corrupted id: report and drop
+      atomicOr(err, kErrBadExpertId);
+      e = -1;
+    }
+    const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    const bool leader = rank == 0;
+    if (e >= 0 && leader) wcnt[warp * E + e] = __popc(peers);
+    __syncthreads();
+    if (e >= 0) {
+      int pos = running[e] + rank;
+      for (int w = 0; w < warp; ++w) pos += wcnt[w * E + e];
+      sorted_slot[pos] = (int32_t)f;
+      slot_pos[f] = pos;
+    }
+    __syncthreads();
+    if (e >= 0 && leader) {
+      atomicAdd(&running[e], __popc(peers));
+      wcnt[warp * E + e] = 0;
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_route(const moe_fp4_dims& d, const float* logits, const Workspace& ws, cudaStream_t st) {
+  const int nb = ws.nb_route;
+  size_t smem1 = (size_t)(kWarps * d.E) * sizeof(float) + (size_t)d.E * sizeof(int);
+  route_hist_kernel<<<nb, kRouteThreads, smem1, st>>>(logits, d.T, d.E, d.k, ws.topk_ids, ws.topk_w,
+                                                     ws.block_hist, ws.err);
+  sort_scan_kernel<<<1, 1024, 0, st>>>(ws.block_hist, nb, d.E, ws.offsets, ws.active, ws.counts,
+                                       ws.gemv_chunks, ws.tc_tiles);
+  size_t smem3 = (size_t)(kWarps + 1) * d.E * sizeof(int);
+  scatter_kernel<<<nb, kRouteThreads, smem3, st>>>(ws.topk_ids, ws.block_hist, d.T, d.E, d.k,
+                                                   ws.sorted_slot, ws.slot_pos, ws.err);
+  return cudaGetLastError();
+}
+
+}  // namespace moe_fp4

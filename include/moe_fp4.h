@@ -1,0 +1,162 @@
+/*
+ * moe_fp4.h — C ABI of the FP4 routed mixture-of-experts layer for GB300 (sm_103a).
+ *
+ * The layer is the routed-expert block of DeepSeek-V4-Flash-style inference
+ * ("DeepSeek-V4-Flash on AMD gfx90a: Correctness Recovery and Inference
+ * Performance Engineering", abstract: FP4 routed mixture-of-experts with packed
+ * FP4 weights and expert sorting; the "MXFP4 MoE" path of the vLLM-on-MI300X
+ * write-up).  Per token it
+ *   1. picks the top-k experts of the router logits, ordered by (logit desc,
+ *      expert index asc), and weights them by the softmax over the k picked
+ *      logits (fp32 comparison, ties to the lower expert id: MI250 correctness
+ *      blog, section 4.1 table and section 4.2);
+ *   2. sorts the T*k (token, slot) pairs by expert with a stable counting sort
+ *      and builds per-expert offsets ("retuned expert sorting");
+ *   3. for every expert, multiplies its tokens by the packed-FP4 W13 (gate and
+ *      up) and applies SwiGLU, h = bf16(silu(g) * u);
+ *   4. multiplies h by the packed-FP4 W2 (down) and combines the k expert
+ *      outputs of each token with its routing weights, in slot order.
+ *
+ * Formats (MXFP4, OCP Microscaling v1.0):
+ *   - weights: two E2M1 codes per byte along K, the LOW nibble holds the even
+ *     K element; code bit 3 = sign, bits 0..2 index {0, .5, 1, 1.5, 2, 3, 4, 6};
+ *   - scales: E8M0 bytes, value 2^(s-127), one per 32 consecutive K elements
+ *     of a row.  Bytes 0xFF (NaN) and scales that push an element outside the
+ *     normal bf16 range (s > 130 with the largest codes) are outside the
+ *     contract: results are unspecified, nothing faults.
+ *   - x is bf16 (raw IEEE binary32 upper halves), router logits and all
+ *     outputs are fp32 except h (bf16).  Router logits must be finite.
+ *
+ * Tensor layouts (all row-major, C-contiguous, device memory unless stated):
+ *   x              bf16   [T, d]
+ *   router_logits  fp32   [T, E]
+ *   w13            uint8  [E, 2I, d/2]   rows [0, I) = gate, rows [I, 2I) = up
+ *   w13_scale      uint8  [E, 2I, d/32]
+ *   w2             uint8  [E, d, I/2]    row n = output feature n, packed along I
+ *   w2_scale       uint8  [E, d, I/32]
+ *   out            fp32   [T, d]         fully overwritten
+ *   topk_ids       int32  [T, k]         slot 0 = highest logit
+ *   topk_weights   fp32   [T, k]
+ *   expert_offsets int32  [E + 1]        expert e owns sorted rows [off[e], off[e+1])
+ *   sorted_slot    int32  [T*k]          sorted row r -> flat slot t*k + j,
+ *                                        increasing within each expert
+ *   h              bf16   [T*k, I]       SwiGLU output in sorted-row order
+ *
+ * Ownership and threading: the caller owns every buffer and the stream.  The
+ * library allocates nothing; all scratch lives in the caller's workspace
+ * (moe_fp4_workspace_bytes).  moe_fp4_route and moe_fp4_forward only enqueue
+ * work on the given stream and never synchronise.  Calls that use different
+ * workspaces may run concurrently; calls sharing a workspace must be ordered
+ * on one stream.
+ *
+ * Errors: every function returns a moe_fp4_status.  Argument checks happen on
+ * the host before anything is enqueued; on error nothing is launched.  A
+ * failed launch returns MOE_FP4_ERR_CUDA (the CUDA error is left for the
+ * caller's next CUDA call to see).  Kernels never trap.
+ */
+#ifndef MOE_FP4_H_
+#define MOE_FP4_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Problem sizes.  T tokens, d hidden size, I expert intermediate size,
+ * E experts, k experts per token. */
+typedef struct moe_fp4_dims {
+  int32_t T, d, I, E, k;
+} moe_fp4_dims;
+
+typedef enum moe_fp4_status {
+  MOE_FP4_OK = 0,
+  MOE_FP4_ERR_INVALID_ARG = -1,  /* null pointer, bad size, misaligned pointer */
+  MOE_FP4_ERR_UNSUPPORTED = -2,  /* sizes the kernels do not cover (see moe_fp4_workspace_bytes) */
+  MOE_FP4_ERR_WORKSPACE = -3,    /* workspace too small */
+  MOE_FP4_ERR_CUDA = -4,         /* a CUDA runtime call failed */
+  MOE_FP4_ERR_DEVICE = -5        /* a kernel reported an error word (moe_fp4_check) */
+} moe_fp4_status;
+
+/* Flags for moe_fp4_forward.  Both expert paths give results within the same
+ * tolerance of the definition; the default picks by shape (expected rows per
+ * expert = T*k/E): the streaming GEMV path for few rows, the tensor-core path
+ * otherwise. */
+#define MOE_FP4_FLAG_FORCE_GEMV 0x1u    /* CUDA-core streaming path (d, I multiples of 1024) */
+#define MOE_FP4_FLAG_FORCE_TC   0x2u    /* tcgen05 tensor-core path */
+
+/* Bytes of device workspace a call with these sizes needs (256-byte aligned
+ * base required).  Returns 0 when the sizes are invalid or unsupported:
+ * T >= 1, 1 <= k <= min(E, 32), 1 <= E <= 1024, d and I multiples of 128,
+ * 128 <= d <= 16384, 128 <= I <= 16384, T*k < 2^31, T*k*max(d, I) < 2^40. */
+size_t moe_fp4_workspace_bytes(const moe_fp4_dims* dims);
+
+/* Steps 1-2 only (routing and the expert sort), so that routing can be
+ * checked bit-exactly on its own (the paper's fixed-token and hash checks).
+ * topk_ids, topk_weights, expert_offsets and sorted_slot are required
+ * device outputs.  Pointers: 4-byte aligned; workspace 256-byte aligned. */
+int moe_fp4_route(const moe_fp4_dims* dims, const float* router_logits,
+                  int32_t* topk_ids, float* topk_weights, int32_t* expert_offsets,
+                  int32_t* sorted_slot, void* workspace, size_t workspace_bytes,
+                  void* cuda_stream);
+
+/* The whole layer (steps 1-4) on device buffers.  out is required; the
+ * routing outputs and h are optional (NULL: kept in the workspace only).
+ * x, w13, w2, out and h must be 16-byte aligned, scales 4-byte aligned,
+ * workspace 256-byte aligned.  flags: 0 or one MOE_FP4_FLAG_FORCE_*. */
+int moe_fp4_forward(const moe_fp4_dims* dims, const void* x_bf16, const float* router_logits,
+                    const uint8_t* w13, const uint8_t* w13_scale,
+                    const uint8_t* w2, const uint8_t* w2_scale, float* out,
+                    int32_t* topk_ids, float* topk_weights, int32_t* expert_offsets,
+                    int32_t* sorted_slot, void* h_bf16, unsigned flags,
+                    void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+/* moe_fp4_forward that also records caller-created CUDA events (cudaEvent_t
+ * handles, MOE_FP4_NUM_STAGE_EVENTS of them) on the stream between its
+ * stages, so that a caller can time each kernel in place:
+ *   events[0] before routing and the expert sort (3 kernels)
+ *   events[1] before the token gather (tensor-core path only; else empty)
+ *   events[2] before W13 + SwiGLU
+ *   events[3] before W2
+ *   events[4] before the combine
+ *   events[5] after the combine
+ * Same arguments, checks and results as moe_fp4_forward. */
+#define MOE_FP4_NUM_STAGE_EVENTS 6
+int moe_fp4_forward_profiled(const moe_fp4_dims* dims, const void* x_bf16, const float* router_logits,
+                             const uint8_t* w13, const uint8_t* w13_scale,
+                             const uint8_t* w2, const uint8_t* w2_scale, float* out,
+                             int32_t* topk_ids, float* topk_weights, int32_t* expert_offsets,
+                             int32_t* sorted_slot, void* h_bf16, unsigned flags,
+                             void* workspace, size_t workspace_bytes, void* cuda_stream,
+                             void* const* stage_events);
+
+/* Bytes of device workspace moe_fp4_forward_host needs: the forward workspace
+ * plus device staging for x, router_logits and out. */
+size_t moe_fp4_host_workspace_bytes(const moe_fp4_dims* dims);
+
+/* The whole layer with HOST x, router_logits and out (weights stay on the
+ * device).  Copies x and the logits to device staging inside the workspace,
+ * runs moe_fp4_forward, copies out back and synchronises the stream before
+ * returning.  Host buffers may be pageable or pinned (pinned is faster). */
+int moe_fp4_forward_host(const moe_fp4_dims* dims, const void* x_bf16_host,
+                         const float* router_logits_host,
+                         const uint8_t* w13, const uint8_t* w13_scale,
+                         const uint8_t* w2, const uint8_t* w2_scale, float* out_host,
+                         unsigned flags, void* workspace, size_t workspace_bytes,
+                         void* cuda_stream);
+
+/* Synchronises the stream and reads the device error word of the workspace
+ * (set by a kernel that met an index out of range, e.g. a corrupted expert
+ * id); returns MOE_FP4_OK, MOE_FP4_ERR_DEVICE or MOE_FP4_ERR_CUDA, and clears
+ * the word. */
+int moe_fp4_check(void* workspace, void* cuda_stream);
+
+/* Static text for a status code. */
+const char* moe_fp4_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_FP4_H_ */

@@ -1,0 +1,87 @@
+"""The C ABI without a GPU: the library loads, exports every declared entry
+point, sizes workspaces and rejects bad arguments before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import fp4_mixture_experts_gb300 as moe
+from fp4_mixture_experts_gb300 import build as build_mod
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(moe.lib_path()):
+        build_mod.build()
+    return moe.load_library()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "moe_fp4.h")).read()
+    return sorted(set(re.findall(r"^(?:size_t|int|const char\*)\s+(moe_fp4_\w+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_binding_symbols():
+    assert declared_functions() == sorted(moe.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_workspace_sizes(lib):
+    assert moe.workspace_bytes(32, 4096, 2048, 256, 8) > 0
+    assert moe.host_workspace_bytes(32, 4096, 2048, 256, 8) > moe.workspace_bytes(32, 4096, 2048, 256, 8)
+    # grows with T
+    assert moe.workspace_bytes(64, 4096, 2048, 256, 8) > moe.workspace_bytes(32, 4096, 2048, 256, 8)
+    for bad in [(0, 256, 128, 8, 2), (16, 100, 128, 8, 2), (16, 256, 96, 8, 2), (16, 256, 128, 8, 9),
+                (16, 256, 128, 2000, 2), (16, 256, 128, 8, 0), (16, 256, 128, 64, 33)]:
+        assert moe.workspace_bytes(*bad) == 0, bad
+
+
+def test_status_strings(lib):
+    for s in (0, -1, -2, -3, -4, -5, 7):
+        assert isinstance(moe.status_string(s), str) and moe.status_string(s)
+
+
+
+def test_bad_arguments_are_rejected_on_the_host(lib):
+    P = ctypes.c_void_p
+    d = moe.Dims(16, 256, 128, 8, 2)
+    fake = 0x100000  # never dereferenced: every call below fails its host-side checks
+    args = [P(fake)] * 7
+    none = [None] * 5
+    # null out
+    rc = lib.moe_fp4_forward(ctypes.byref(d), *args[:6], None, *none, 0, P(fake), 1 << 30, None)
+    assert rc == -1
+    # unknown flags
+    rc = lib.moe_fp4_forward(ctypes.byref(d), *args, *none, 0x80, P(fake), 1 << 30, None)
+    assert rc == -1
+    # both path flags
+    rc = lib.moe_fp4_forward(ctypes.byref(d), *args, *none, 0x3, P(fake), 1 << 30, None)
+    assert rc == -1
+    # unsupported sizes
+    bad = moe.Dims(16, 100, 128, 8, 2)
+    rc = lib.moe_fp4_forward(ctypes.byref(bad), *args, *none, 0, P(fake), 1 << 30, None)
+    assert rc == -2
+    # misaligned x
+    rc = lib.moe_fp4_forward(ctypes.byref(d), P(fake + 2), *args[1:], *none, 0, P(fake), 1 << 30, None)
+    assert rc == -1
+    # misaligned workspace
+    rc = lib.moe_fp4_forward(ctypes.byref(d), *args, *none, 0, P(fake + 16), 1 << 30, None)
+    assert rc == -1
+    # workspace too small
+    rc = lib.moe_fp4_forward(ctypes.byref(d), *args, *none, 0, P(fake), 64, None)
+    assert rc == -3
+    # the GEMV path needs d and I multiples of 1024
+    rc = lib.moe_fp4_forward(ctypes.byref(d), *args, *none, 0x1, P(fake), 1 << 30, None)
+    assert rc == -2
+    # route: null outputs
+    rc = lib.moe_fp4_route(ctypes.byref(d), P(fake), None, P(fake), P(fake), P(fake), P(fake), 1 << 30, None)
+    assert rc == -1
+    rc = lib.moe_fp4_check(None, None)
+    assert rc == -1

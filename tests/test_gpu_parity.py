@@ -1,0 +1,216 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Routing ids, the expert permutation, the offsets and their FNV-1a hash must
+be bit-exact; routing weights agree to fp32 rounding; h agrees up to rare
+one-ulp bf16 flips (fp32 vs fp64 sums before the rounding); out must reach
+relative L2 <= 5e-3, cosine >= 0.9999 and max abs <= 2e-2.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from moe_inputs import make_config, make_layer, routing_sample_tokens
+
+from _layer_util import assert_out_close, bf16_bits, out_metrics, to_device
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+GEMV = 0x1
+TC = 0x2
+
+
+@pytest.fixture(scope="module")
+def moe():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    import fp4_mixture_experts_gb300 as m
+    m.load_library()
+    return m
+
+
+def run_gpu(moe, L, flags=0, return_h=True):
+    D = to_device(L)
+    r = moe.forward(D["x"], D["logits"], D["w13"], D["w13_scale"], D["w2"], D["w2_scale"], L.k, flags=flags,
+                    return_routing=True, return_h=return_h)
+    torch.cuda.synchronize()
+    return {k: v for k, v in r.items()}
+
+
+def check_routing(r, ref):
+    ids = r["topk_ids"].cpu().numpy()
+    ss = r["sorted_slot"].cpu().numpy()
+    off = r["expert_offsets"].cpu().numpy()
+    np.testing.assert_array_equal(ids, ref["topk_ids"])
+    np.testing.assert_array_equal(off, ref["expert_offsets"])
+    np.testing.assert_array_equal(ss, ref["sorted_slot"])
+    assert oracle.route_hash(ids, ss, off) == oracle.route_hash(ref["topk_ids"], ref["sorted_slot"],
+                                                                ref["expert_offsets"])
+    np.testing.assert_allclose(r["topk_weights"].cpu().numpy(), ref["topk_w"], rtol=2e-6, atol=1e-7)
+
+
+def check_h(r, ref):
+    got = oracle.bf16_bits_to_f64(bf16_bits(r["h"]))
+    want = ref["h"]
+    mism = got != want
+    if mism.any():
+        # a mismatch may only be a one-ulp flip of the bf16 rounding
+        ulp = np.ldexp(1.0, np.frexp(np.maximum(np.abs(want[mism]), 1e-30))[1] - 8)
+        assert (np.abs(got[mism] - want[mism]) <= ulp * 1.0001).all(), "h differs by more than one bf16 ulp"
+        assert mism.mean() < 1e-3, f"too many h flips: {mism.mean()}"
+
+
+def full_check(moe, L, flags=0):
+    ref = oracle.forward(L.x_bf16, L.router_logits, L.w13, L.w13_scale, L.w2, L.w2_scale, L.k)
+    r = run_gpu(moe, L, flags)
+    check_routing(r, ref)
+    check_h(r, ref)
+    return assert_out_close(r["out"].cpu().numpy(), ref["out"], f"flags={flags}")
+
+
+# ----------------------------------------------------------------------------
+def test_tiny_config(moe):
+    full_check(moe, make_config("tiny"))
+
+
+@pytest.mark.parametrize("flags", [GEMV, TC])
+def test_several_tiles_ragged(moe, flags):
+    # 300 tokens x 4 slots over 16 experts: ~75 rows per expert, ragged chunk and tile tails
+    L = make_layer(T=300, d=1024, I=1024, E=16, k=4, seed=3)
+    full_check(moe, L, flags)
+
+
+@pytest.mark.parametrize("flags", [0, TC])
+def test_non_1024_multiples(moe, flags):
+    L = make_layer(T=37, d=384, I=640, E=12, k=3, seed=4)
+    full_check(moe, L, flags)
+
+
+@pytest.mark.parametrize("flags", [GEMV, TC])
+def test_single_token(moe, flags):
+    full_check(moe, make_layer(T=1, d=1024, I=1024, E=8, k=2, seed=5), flags)
+
+
+@pytest.mark.parametrize("flags", [GEMV, TC])
+def test_top1_and_single_expert(moe, flags):
+    full_check(moe, make_layer(T=20, d=1024, I=1024, E=6, k=1, seed=6), flags)
+    full_check(moe, make_layer(T=20, d=1024, I=1024, E=1, k=1, seed=7), flags)
+
+
+@pytest.mark.parametrize("flags", [GEMV, TC])
+def test_all_tokens_one_expert_and_empty_experts(moe, flags):
+    L = make_layer(T=70, d=1024, I=1024, E=32, k=2, seed=8)
+    L.router_logits[:, 5] += 50.0     # expert 5 first for every token
+    L.router_logits[:, 9] += 40.0     # expert 9 second
+    full_check(moe, L, flags)
+
+
+def test_ties_and_signed_zero(moe):
+    L = make_layer(T=40, d=1024, I=1024, E=16, k=4, seed=9)
+    L.router_logits[:10] = 0.0
+    L.router_logits[10:20, ::2] = 1.5
+    L.router_logits[20:30] = np.where(np.arange(16) % 2, -0.0, 0.0).astype(np.float32)
+    full_check(moe, L)
+
+
+def test_k_equals_E(moe):
+    full_check(moe, make_layer(T=9, d=1024, I=1024, E=5, k=5, seed=10), GEMV)
+    full_check(moe, make_layer(T=9, d=256, I=256, E=5, k=5, seed=10), TC)
+
+
+@pytest.mark.parametrize("flags", [GEMV, TC])
+def test_w2_layout_probe(moe, flags):
+    """A single nonzero W2 code must land on its own output column only."""
+    L = make_layer(T=24, d=1024, I=1024, E=4, k=2, seed=11)
+    e_star, n0, m0 = 1, 517, 301
+    L.w2[:] = 0
+    L.w2[e_star, n0, m0 // 2] = 0x50
+    r = run_gpu(moe, L, flags)
+    ref = oracle.forward(L.x_bf16, L.router_logits, L.w13, L.w13_scale, L.w2, L.w2_scale, L.k)
+    out = r["out"].cpu().numpy()
+    assert set(np.nonzero(np.abs(out).sum(0))[0].tolist()) <= {n0}
+    assert_out_close(out, ref["out"], "w2 probe")
+
+
+@pytest.mark.parametrize("flags", [GEMV, TC])
+def test_w13_nibble_and_gate_up_probe(moe, flags):
+    L = make_layer(T=12, d=1024, I=1024, E=2, k=1, seed=12)
+    L.w13[:] = 0
+    L.w13[:, 7, 100] = 0x04        # gate row 7, K=200 (low nibble): 2.0
+    L.w13[:, 1024 + 7, 100] = 0xB0  # up row 7, K=201 (high nibble): -1.5
+    L.w13[:, 1024 + 9, 33] = 0x22   # up row 9 only: h must stay 0 (silu(0) = 0)
+    r = run_gpu(moe, L, flags)
+    ref = oracle.forward(L.x_bf16, L.router_logits, L.w13, L.w13_scale, L.w2, L.w2_scale, L.k)
+    check_h(r, ref)
+    h = oracle.bf16_bits_to_f64(bf16_bits(r["h"]))
+    assert not np.delete(h, 7, axis=1).any()
+
+
+def test_zero_codes_give_zero(moe):
+    L = make_layer(T=16, d=1024, I=1024, E=4, k=2, seed=13)
+    L.w2[:] = 0x88
+    for flags in (GEMV, TC):
+        r = run_gpu(moe, L, flags)
+        assert not r["out"].cpu().numpy().any()
+
+
+def test_run_twice_bit_identical(moe):
+    L = make_layer(T=200, d=1024, I=1024, E=16, k=4, seed=14)
+    for flags in (GEMV, TC):
+        a = run_gpu(moe, L, flags)["out"].cpu().numpy()
+        b = run_gpu(moe, L, flags)["out"].cpu().numpy()
+        assert np.array_equal(a, b)
+
+
+def test_route_entry_point(moe):
+    L = make_layer(T=333, d=128, I=128, E=64, k=6, seed=15)
+    ids, w, off, ss = moe.route(torch.from_numpy(L.router_logits).cuda(), L.k)
+    torch.cuda.synchronize()
+    ref_ids, ref_w = oracle.route(L.router_logits, L.k)
+    ref_off, ref_ss, _ = oracle.expert_sort(ref_ids, L.E)
+    np.testing.assert_array_equal(ids.cpu().numpy(), ref_ids)
+    np.testing.assert_array_equal(off.cpu().numpy(), ref_off)
+    np.testing.assert_array_equal(ss.cpu().numpy(), ref_ss)
+    np.testing.assert_allclose(w.cpu().numpy(), ref_w, rtol=2e-6, atol=1e-7)
+
+
+def test_forward_host_matches_forward(moe):
+    L = make_layer(T=40, d=1024, I=1024, E=16, k=4, seed=16)
+    D = to_device(L)
+    dev_out = moe.forward(D["x"], D["logits"], D["w13"], D["w13_scale"], D["w2"], D["w2_scale"], L.k)
+    xh = torch.from_numpy(L.x_bf16.view(np.int16)).view(torch.bfloat16).pin_memory()
+    lh = torch.from_numpy(L.router_logits).pin_memory()
+    host_out = moe.forward_host(xh, lh, D["w13"], D["w13_scale"], D["w2"], D["w2_scale"], L.k)
+    torch.cuda.synchronize()
+    assert np.array_equal(host_out.numpy(), dev_out.cpu().numpy())
+
+
+def test_check_reports_clean_workspace(moe):
+    L = make_layer(T=16, d=1024, I=1024, E=4, k=2, seed=17)
+    D = to_device(L)
+    ws = torch.empty(moe.workspace_bytes(L.T, L.d, L.I, L.E, L.k), dtype=torch.uint8, device="cuda")
+    moe.forward(D["x"], D["logits"], D["w13"], D["w13_scale"], D["w2"], D["w2_scale"], L.k, workspace=ws)
+    moe.check(ws)
+
+
+# ----------------------------------------------------------------------------
+# the five named workloads at full size
+# ----------------------------------------------------------------------------
+def test_decode_config_full(moe):
+    L = make_config("decode")
+    m = full_check(moe, L)
+    print("decode", m)
+
+
+@pytest.mark.parametrize("name,n_tok", [("prefill", 6), ("skewed", 6), ("large", 4)])
+def test_full_size_routing_exact_and_sampled_out(moe, name, n_tok):
+    L = make_config(name)
+    r = run_gpu(moe, L, return_h=False)
+    ids, w = oracle.route(L.router_logits, L.k)
+    off, ss, _ = oracle.expert_sort(ids, L.E)
+    check_routing(r, dict(topk_ids=ids, topk_w=w, expert_offsets=off, sorted_slot=ss))
+    toks = routing_sample_tokens(L.T, n_tok)
+    _, _, want = oracle.forward_tokens(L.x_bf16, L.router_logits, L.w13, L.w13_scale, L.w2, L.w2_scale, L.k, toks)
+    got = r["out"][torch.from_numpy(toks).cuda()].cpu().numpy()
+    m = assert_out_close(got, want, name)
+    print(name, m)
