@@ -94,9 +94,15 @@ int run_forward(const moe_fp4_dims& d, const void* x, const float* logits, const
   mark(1);
   if (use_gemv_path(d, flags)) {
     mark(2);
-    e = launch_gemv_w13(d, xb, w13, w13s, ws, st);
-    mark(3);
-    if (e == cudaSuccess) e = launch_gemv_w2(d, w2, w2s, ws, st);
+    if (stream_path_supported(d)) {
+      e = launch_stream_w13(d, xb, w13, w13s, ws, st);
+      mark(3);
+      if (e == cudaSuccess) e = launch_stream_w2(d, w2, w2s, ws, st);
+    } else {
+      e = launch_gemv_w13(d, xb, w13, w13s, ws, st);
+      mark(3);
+      if (e == cudaSuccess) e = launch_gemv_w2(d, w2, w2s, ws, st);
+    }
   } else {
     mark(2);
     e = launch_gemv_w13(d, xb, w13, w13s, ws, st);
@@ -168,7 +174,7 @@ int moe_fp4_forward_profiled(const moe_fp4_dims* dims, const void* x_bf16, const
   Workspace ws;
   if (!layout_workspace(d, workspace, false, &ws)) return MOE_FP4_ERR_UNSUPPORTED;
   if (!aligned(workspace, 256) || !aligned(x_bf16, 16) || !aligned(w13, 16) || !aligned(w2, 16) ||
-      !aligned(out, 16) || !aligned(router_logits, 4) || !aligned(w13_scale, 4) || !aligned(w2_scale, 4) ||
+      !aligned(out, 16) || !aligned(router_logits, 4) || !aligned(w13_scale, 16) || !aligned(w2_scale, 16) ||
       (h_bf16 && !aligned(h_bf16, 16)) || (topk_ids && !aligned(topk_ids, 4)) ||
       (topk_weights && !aligned(topk_weights, 4)) || (expert_offsets && !aligned(expert_offsets, 4)) ||
       (sorted_slot && !aligned(sorted_slot, 4)))
@@ -201,8 +207,8 @@ int moe_fp4_forward_host(const moe_fp4_dims* dims, const void* x_bf16_host, cons
   const moe_fp4_dims d = *dims;
   Workspace ws;
   if (!layout_workspace(d, workspace, true, &ws)) return MOE_FP4_ERR_UNSUPPORTED;
-  if (!aligned(workspace, 256) || !aligned(w13, 16) || !aligned(w2, 16) || !aligned(w13_scale, 4) ||
-      !aligned(w2_scale, 4))
+  if (!aligned(workspace, 256) || !aligned(w13, 16) || !aligned(w2, 16) || !aligned(w13_scale, 16) ||
+      !aligned(w2_scale, 16))
     return MOE_FP4_ERR_INVALID_ARG;
   if ((flags & MOE_FP4_FLAG_FORCE_GEMV) && (d.d % 1024 != 0 || d.I % 1024 != 0)) return MOE_FP4_ERR_UNSUPPORTED;
   if (workspace_bytes < ws.total) return MOE_FP4_ERR_WORKSPACE;

@@ -18,6 +18,7 @@ constexpr int kTcTileN = 128;              // token rows per tensor-core tile (U
 
 // Device error word values (moe_fp4_check).
 constexpr int kErrBadExpertId = 1;
+constexpr int kErrWaitTimeout = 2;
 
 // Pointers into the caller's workspace; every region starts on a 256-byte boundary.
 struct Workspace {
@@ -56,6 +57,11 @@ cudaError_t launch_gemv_w13(const moe_fp4_dims& d, const uint16_t* x, const uint
                             const uint8_t* w13s, const Workspace& ws, cudaStream_t st);
 cudaError_t launch_gemv_w2(const moe_fp4_dims& d, const uint8_t* w2, const uint8_t* w2s,
                            const Workspace& ws, cudaStream_t st);
+bool stream_path_supported(const moe_fp4_dims& d);
+cudaError_t launch_stream_w13(const moe_fp4_dims& d, const uint16_t* x, const uint8_t* w13, const uint8_t* w13s,
+                              const Workspace& ws, cudaStream_t st);
+cudaError_t launch_stream_w2(const moe_fp4_dims& d, const uint8_t* w2, const uint8_t* w2s, const Workspace& ws,
+                             cudaStream_t st);
 cudaError_t launch_combine(const moe_fp4_dims& d, float* out, const Workspace& ws, cudaStream_t st);
 
 // ---------------------------------------------------------------------------

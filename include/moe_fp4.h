@@ -103,8 +103,8 @@ int moe_fp4_route(const moe_fp4_dims* dims, const float* router_logits,
 
 /* The whole layer (steps 1-4) on device buffers.  out is required; the
  * routing outputs and h are optional (NULL: kept in the workspace only).
- * x, w13, w2, out and h must be 16-byte aligned, scales 4-byte aligned,
- * workspace 256-byte aligned.  flags: 0 or one MOE_FP4_FLAG_FORCE_*. */
+ * x, w13, w13_scale, w2, w2_scale, out and h must be 16-byte aligned,
+ * the routing outputs 4-byte aligned, the workspace 256-byte aligned.  flags: 0 or one MOE_FP4_FLAG_FORCE_*. */
 int moe_fp4_forward(const moe_fp4_dims* dims, const void* x_bf16, const float* router_logits,
                     const uint8_t* w13, const uint8_t* w13_scale,
                     const uint8_t* w2, const uint8_t* w2_scale, float* out,

