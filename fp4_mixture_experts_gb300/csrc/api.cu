@@ -104,10 +104,11 @@ int run_forward(const moe_fp4_dims& d, const void* x, const float* logits, const
       if (e == cudaSuccess) e = launch_gemv_w2(d, w2, w2s, ws, st);
     }
   } else {
+    e = launch_gather(d, xb, ws, st);
     mark(2);
-    e = launch_gemv_w13(d, xb, w13, w13s, ws, st);
+    if (e == cudaSuccess) e = launch_tc_w13(d, w13, w13s, ws, st);
     mark(3);
-    if (e == cudaSuccess) e = launch_gemv_w2(d, w2, w2s, ws, st);
+    if (e == cudaSuccess) e = launch_tc_w2(d, w2, w2s, ws, st);
   }
   mark(4);
   if (e == cudaSuccess) e = launch_combine(d, out, ws, st);
