@@ -366,6 +366,41 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+PROFILE_CASES = {
+    # name: (workload, experts override, tokens override) -- smaller expert counts keep
+    # ncu captures to about a GB on the device while the weights stay larger than L2
+    "decode": ("decode", None, None),
+    "prefill": ("prefill", None, None),
+    "decode-e64": ("decode", 64, 32),
+    "prefill-e64": ("prefill", 64, 1152),
+}
+
+
+def run_profile_case(args):
+    """Run `--steps` forward passes of one case with no timing or JSON output:
+    the command that ncu captures."""
+    import torch
+
+    import fp4_mixture_experts_gb300 as moe
+    from moe_inputs import make_layer
+    name, E, T = PROFILE_CASES[args.profile_case]
+    c = dict(CONFIGS[name])
+    if E is not None:
+        c["E"], c["T"] = E, T
+    L = make_layer(**c)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    x = t(L.x_bf16.view(np.int16)).view(torch.bfloat16)
+    args_ = (x, t(L.router_logits), t(L.w13), t(L.w13_scale), t(L.w2), t(L.w2_scale), L.k)
+    ws = torch.empty(moe.workspace_bytes(L.T, L.d, L.I, L.E, L.k), dtype=torch.uint8, device="cuda")
+    out = torch.empty(L.T, L.d, dtype=torch.float32, device="cuda")
+    for _ in range(args.warmup + args.steps):
+        moe.forward(*args_, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    moe.check(ws)
+    print(f"profile case {args.profile_case}: T={L.T} d={L.d} I={L.I} E={L.E} k={L.k}, "
+          f"{args.warmup + args.steps} forward passes, out rms {out.float().pow(2).mean().sqrt().item():.3f}")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -375,10 +410,14 @@ def main():
     ap.add_argument("--no-prefill", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES), default=None,
+                    help="only run forward passes of one case (for ncu), no measurement")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
-    if args.impl == "reference":
+    if args.profile_case:
+        run_profile_case(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

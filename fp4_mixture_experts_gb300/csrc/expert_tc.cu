@@ -325,7 +325,7 @@ tc_kernel(const __grid_constant__ CUtensorMap map_raw, const __grid_constant__ C
             if (c0 + j < n) {
               float* yrow = P.y_out + (size_t)(row0 + c0 + j) * P.d;
               yrow[nrow] = a0[j];
-              yrow[nrow + P.acc1_offset] = a1[j];
+              if (nrow + P.acc1_offset < P.d) yrow[nrow + P.acc1_offset] = a1[j];  // last block may hold 128 rows
             }
           }
         }
@@ -428,7 +428,7 @@ cudaError_t launch_tc_w2(const moe_fp4_dims& d, const uint8_t* w2, const uint8_t
   P.y_out = ws.y;
   P.K = d.I;
   P.rows_per_expert = d.d;
-  P.mblocks = d.d / (2 * kBM);
+  P.mblocks = (d.d + 2 * kBM - 1) / (2 * kBM);  // d % 256 == 128 leaves a 128-row last block
   P.block_rows = 2 * kBM;
   P.acc1_offset = kBM;
   P.I = d.I;
