@@ -8,18 +8,24 @@
 // token rows of one expert:
 //   - one producer warp streams the stage's packed rows and E8M0 scales into a
 //     4-deep shared-memory ring with 1-D bulk TMA copies (cp.async.bulk,
-//     mbarrier transaction counts), so ~130 KB of weights per SM are in flight;
+//     full/empty mbarriers with transaction counts), so ~130 KB of weights per
+//     SM are in flight;
 //   - the consumer threads split K into 32-element MX blocks (one 16-byte
-//     packed chunk and one scale per thread and row); each holds its block of
-//     the chunk's activations in registers as fp32 pairs, decodes E2M1 pairs
-//     with cvt.rn.f16x2.e2m1x2, multiplies with the packed fp32 FMA
-//     (fma.rn.f32x2), applies the block scale once per block, and keeps fp32
-//     partial sums for several rows and tokens;
+//     packed chunk and one scale per thread and row).  Each holds its block of
+//     the chunk's activations in registers as f16 pairs, scaled by a power of
+//     two per (token, block) so that every bf16 value lands exactly in f16
+//     range; E2M1 pairs are decoded by cvt.rn.f16x2.e2m1x2 (exact) and
+//     multiplied with the mixed-precision fma.rn.f32.f16 (exact f16 x f16
+//     products, fp32 accumulation), so no fp32 conversion of the weights is
+//     needed; the block sums are scaled once by 2^(s-127) times the
+//     activation scale;
 //   - partial sums are reduced with a warp butterfly (reduce-scatter) and a
-//     small shared-memory pass across warps; the W13 epilogue applies SwiGLU
-//     and rounds h to bf16, the W2 epilogue writes fp32 y.
+//     small shared-memory pass across the warps of a row group, synchronised
+//     by a per-group named barrier; the W13 epilogue applies SwiGLU and rounds
+//     h to bf16, the W2 epilogue writes fp32 y.
 // Every mbarrier wait is bounded: past the limit the thread records an error
-// word and the CTA stops issuing work (moe_fp4_check reports it).
+// word; the threads of a row group take the exit decision together (barrier
+// with an OR vote), so no barrier is left waiting (moe_fp4_check reports it).
 #include <cuda_fp16.h>
 
 #include "moe_fp4_internal.cuh"
@@ -32,7 +38,7 @@ constexpr int kPairsW13 = 4;        // (gate, up) row pairs per consumer thread 
 constexpr int kRowsW2 = 8;          // W2 rows per consumer thread per stage
 constexpr int kMaxConsumers = 256;  // K-split threads x row groups
 constexpr uint32_t kWaitLimit = 1u << 22;  // try_wait rounds before giving up (~seconds)
-constexpr int kRingOffset = 128 + kMaxConsumers * sizeof(float);  // barriers, reduction buffer
+constexpr int kRingOffset = 128 + 2 * kMaxConsumers * sizeof(float);  // barriers, reduction buffers
 
 struct StreamParams {
   const uint8_t* w;        // packed weights of all experts
@@ -94,18 +100,18 @@ __device__ __forceinline__ uint64_t evict_first_policy() {
   return p;
 }
 
-__device__ __forceinline__ void consumer_sync(int n_threads) {
-  asm volatile("bar.sync 1, %0;" ::"r"(n_threads) : "memory");
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-// Barrier among the consumer threads that also ORs a predicate over them, so
-// that every consumer takes the same exit decision.
-__device__ __forceinline__ bool consumer_sync_or(int n_threads, bool pred) {
+// Named barrier `id` over `n_threads` threads that also ORs a predicate, so
+// that every thread of the group takes the same exit decision.
+__device__ __forceinline__ bool group_sync_or(int id, int n_threads, bool pred) {
   uint32_t r;
   asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 2, %2, p;\n\tselp.u32 %0, 1, 0, q;\n}"
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n}"
       : "=r"(r)
-      : "r"((uint32_t)pred), "r"(n_threads)
+      : "r"((uint32_t)pred), "r"(id), "r"(n_threads)
       : "memory");
   return r != 0;
 }
@@ -135,49 +141,76 @@ __device__ __forceinline__ float warp_reduce_scatter(float (&v)[V], int lane) {
   return v[0];
 }
 
-// Load this thread's 32 activations of every token row of the chunk as fp32 pairs.
-__device__ __forceinline__ void load_act(float2 (&x)[kGemvTokens][16], const uint16_t* act, int4 rows,
-                                         int mt, int K, int kb) {
-#pragma unroll
-  for (int t = 0; t < kGemvTokens; ++t) {
-    if (t < mt) {
-      const int row = t == 0 ? rows.x : t == 1 ? rows.y : t == 2 ? rows.z : rows.w;
-      const uint4* p = reinterpret_cast<const uint4*>(act + (size_t)row * K + kb * 32);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint4 q = p[c];
-        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) x[t][c * 4 + i] = make_float2(bf16_to_f32(w[i] & 0xFFFFu), bf16_to_f32(w[i] >> 16));
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 16; ++j) x[t][j] = make_float2(0.f, 0.f);
-    }
-  }
+// 2^e as fp32 for any e the kernel meets (exponent-field build when normal)
+__device__ __forceinline__ float pow2f(int e) {
+  return (e >= -126 && e <= 127) ? __uint_as_float((uint32_t)(e + 127) << 23) : ldexpf(1.0f, e);
 }
 
-// One row's 32-element block (16 packed bytes at `row`) dotted with MT token
-// rows; returns the unscaled block sums.
-template <int MT>
-__device__ __forceinline__ void block_dot(const uint8_t* row, const float2 (&x)[kGemvTokens][16], float (&s)[MT]) {
-  const uint4 q = *reinterpret_cast<const uint4*>(row);
-  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-  float2 acc[MT];
+// This thread's 32 activations of one token row, as 16 f16 pairs scaled by a
+// power of two: value = f16 * 2^xe.  The largest magnitude lands in
+// [2^14, 2^15), so every bf16 value of the block within 2^38 of it is exact.
+__device__ __forceinline__ void load_x_block(uint32_t (&xh)[16], int& xe, const uint16_t* src) {
+  uint32_t w[16];
 #pragma unroll
-  for (int t = 0; t < MT; ++t) acc[t] = make_float2(0.f, 0.f);
+  for (int c = 0; c < 4; ++c) {
+    const uint4 q = reinterpret_cast<const uint4*>(src)[c];
+    w[4 * c + 0] = q.x;
+    w[4 * c + 1] = q.y;
+    w[4 * c + 2] = q.z;
+    w[4 * c + 3] = q.w;
+  }
+  uint32_t emax = 1;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    emax = max(emax, (w[i] >> 7) & 0xFFu);
+    emax = max(emax, (w[i] >> 23) & 0xFFu);
+  }
+  const int shift = 141 - (int)emax;  // 2^shift * 2^(emax-127) = 2^14
+  const float f1 = pow2f(shift / 2), f2 = pow2f(shift - shift / 2);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const float lo = bf16_to_f32(w[i] & 0xFFFFu) * f1 * f2;
+    const float hi = bf16_to_f32(w[i] >> 16) * f1 * f2;
+    const __half2 h = __floats2half2_rn(lo, hi);
+    xh[i] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  xe = -shift;
+}
+
+__device__ __forceinline__ float fma_f16(uint16_t a, uint16_t b, float c) {
+  asm("fma.rn.f32.f16 %0, %1, %2, %0;" : "+f"(c) : "h"(a), "h"(b));
+  return c;
+}
+
+__device__ __forceinline__ void split16(uint32_t v, uint16_t& lo, uint16_t& hi) {
+  asm("mov.b32 {%0, %1}, %2;" : "=h"(lo), "=h"(hi) : "r"(v));
+}
+
+// One row's 32-element block (16 packed bytes) dotted with MT token rows:
+// unscaled sums s[t] = sum_j e2m1_j * xh_t[j] (exact products, fp32 sums).
+template <int MT>
+__device__ __forceinline__ void block_dot(const uint4 q, const uint32_t (&xh)[kGemvTokens][16], float (&s)[MT]) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  float a0[MT], a1[MT];
+#pragma unroll
+  for (int t = 0; t < MT; ++t) a0[t] = a1[t] = 0.f;
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-      const uint32_t h2 = e2m1x2_to_f16x2((w[c] >> (8 * b)) & 0xFFu);
-      const float2 wf = __half22float2(*reinterpret_cast<const __half2*>(&h2));
+      uint16_t wl, wh;
+      split16(e2m1x2_to_f16x2((w[c] >> (8 * b)) & 0xFFu), wl, wh);
 #pragma unroll
-      for (int t = 0; t < MT; ++t) acc[t] = __ffma2_rn(wf, x[t][c * 4 + b], acc[t]);
+      for (int t = 0; t < MT; ++t) {
+        uint16_t xl, xh_;
+        split16(xh[t][c * 4 + b], xl, xh_);
+        a0[t] = fma_f16(wl, xl, a0[t]);
+        a1[t] = fma_f16(wh, xh_, a1[t]);
+      }
     }
   }
 #pragma unroll
-  for (int t = 0; t < MT; ++t) s[t] = acc[t].x + acc[t].y;
+  for (int t = 0; t < MT; ++t) s[t] = a0[t] + a1[t];
 }
 
 // ---------------------------------------------------------------------------
@@ -185,7 +218,8 @@ __device__ __forceinline__ void block_dot(const uint8_t* row, const float2 (&x)[
 // ---------------------------------------------------------------------------
 template <int MT>
 __device__ __forceinline__ void w13_stage(const StreamParams& P, const uint8_t* slot, int rgi, int kb, int lane,
-                                          int warp_in_rg, const float2 (&x)[kGemvTokens][16], float* red) {
+                                          const uint32_t (&xh)[kGemvTokens][16], const int (&xe)[kGemvTokens],
+                                          float* red_w) {
   constexpr int V = 2 * kPairsW13 * MT;  // (pair, token, gate/up)
   float v[V];
   const int row_bytes = P.K / 2, nkb = P.nkb, rps = P.rows_per_stage;
@@ -197,20 +231,21 @@ __device__ __forceinline__ void w13_stage(const StreamParams& P, const uint8_t* 
     for (int gu = 0; gu < 2; ++gu) {
       const int r = gu * rps + pr;
       float s[MT];
-      block_dot<MT>(slot + (size_t)r * row_bytes + kb * 16, x, s);
-      const float sc = e8m0_to_f32(scales[r * nkb + kb]);
+      block_dot<MT>(*reinterpret_cast<const uint4*>(slot + (size_t)r * row_bytes + kb * 16), xh, s);
+      const int se = (int)scales[r * nkb + kb] - 127;
 #pragma unroll
-      for (int t = 0; t < MT; ++t) v[(p * MT + t) * 2 + gu] = sc * s[t];
+      for (int t = 0; t < MT; ++t) v[(p * MT + t) * 2 + gu] = s[t] * pow2f(se + xe[t]);
     }
   }
   const float r = warp_reduce_scatter<V>(v, lane);
   constexpr int kLanesPerValue = 32 / V;
-  if ((lane % kLanesPerValue) == 0) red[(rgi * (nkb / 32) + warp_in_rg) * 32 + lane / kLanesPerValue] = r;
+  if ((lane % kLanesPerValue) == 0) red_w[lane / kLanesPerValue] = r;
 }
 
 template <int MT>
 __device__ __forceinline__ void w2_stage(const StreamParams& P, const uint8_t* slot, int rgi, int kb, int lane,
-                                         int warp_in_rg, const float2 (&x)[kGemvTokens][16], float* red) {
+                                         const uint32_t (&xh)[kGemvTokens][16], const int (&xe)[kGemvTokens],
+                                         float* red_w) {
   constexpr int V = kRowsW2 * MT;  // (row, token)
   float v[V];
   const int row_bytes = P.K / 2, nkb = P.nkb, rps = P.rows_per_stage;
@@ -219,14 +254,14 @@ __device__ __forceinline__ void w2_stage(const StreamParams& P, const uint8_t* s
   for (int p = 0; p < kRowsW2; ++p) {
     const int r = rgi * kRowsW2 + p;
     float s[MT];
-    block_dot<MT>(slot + (size_t)r * row_bytes + kb * 16, x, s);
-    const float sc = e8m0_to_f32(scales[r * nkb + kb]);
+    block_dot<MT>(*reinterpret_cast<const uint4*>(slot + (size_t)r * row_bytes + kb * 16), xh, s);
+    const int se = (int)scales[r * nkb + kb] - 127;
 #pragma unroll
-    for (int t = 0; t < MT; ++t) v[p * MT + t] = sc * s[t];
+    for (int t = 0; t < MT; ++t) v[p * MT + t] = s[t] * pow2f(se + xe[t]);
   }
   const float r = warp_reduce_scatter<V>(v, lane);
   constexpr int kLanesPerValue = 32 / V;
-  if ((lane % kLanesPerValue) == 0) red[(rgi * (nkb / 32) + warp_in_rg) * 32 + lane / kLanesPerValue] = r;
+  if ((lane % kLanesPerValue) == 0) red_w[lane / kLanesPerValue] = r;
 }
 
 template <bool W13>
@@ -252,40 +287,71 @@ __device__ __forceinline__ void issue_stage(const StreamParams& P, long long u, 
   }
 }
 
-// All threads are consumers (K-split x row groups, at most 8 warps so that a
-// thread may hold up to 255 registers).  Thread 0 also issues the bulk copies:
-// the ring is refilled right after the per-stage barrier, when every thread is
-// done reading the slot, kStages items ahead of the compute.
+// Consumers: rg row groups of nkb threads (K split in 32-element blocks), at
+// most 256; one producer warp after them issues the bulk copies.
 template <bool W13>
-__global__ void __launch_bounds__(kMaxConsumers, 1) stream_kernel(const StreamParams P) {
+__global__ void __launch_bounds__(kMaxConsumers + 32, 1) stream_kernel(const StreamParams P) {
   extern __shared__ __align__(128) uint8_t smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-  float* red = reinterpret_cast<float*>(smem + 128);  // [rg][warps per rg][32]
+  uint64_t* empty = full + kStages;
+  float* red = reinterpret_cast<float*>(smem + 128);  // [2 buffers][consumer warps][32]
   uint8_t* ring = smem + kRingOffset;
-  const int tid = threadIdx.x, lane = tid & 31;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n_cons = P.rg * P.nkb;
+  const int n_cons_warps = n_cons / 32;
   const int n_chunks = P.counts[1];
   const int spc = P.rows_per_expert / P.rows_per_stage;  // stages per chunk
   const long long n_items = (long long)n_chunks * spc;
   const long long u0 = n_items * blockIdx.x / gridDim.x;
   const long long u1 = n_items * (blockIdx.x + 1) / gridDim.x;
-  const int nkb = P.nkb, rps = P.rows_per_stage;
-  uint64_t pol = 0;
   if (tid == 0) {
-    for (int i = 0; i < kStages; ++i) mbar_init(&full[i], 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], n_cons_warps);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    pol = evict_first_policy();
-    for (int i = 0; i < kStages && u0 + i < u1; ++i)
-      issue_stage<W13>(P, u0 + i, spc, ring + (size_t)i * P.stage_bytes, &full[i], pol);
   }
   __syncthreads();
-  if (tid >= n_cons) return;
 
-  const int rgi = tid / nkb, kb = tid % nkb, warp_in_rg = (tid % nkb) / 32;
+  if (warp == n_cons_warps) {
+    // ---------------- producer warp ----------------
+    if (lane == 0) {
+      const uint64_t pol = evict_first_policy();
+      int slot = 0;
+      uint32_t phase = 0, pending = 0, last_phase = 0;
+      bool ok = true;
+      for (long long u = u0; u < u1; ++u) {
+        if (!mbar_wait(&empty[slot], phase ^ 1u)) {
+          atomicOr(P.err, kErrWaitTimeout);
+          ok = false;
+          break;
+        }
+        issue_stage<W13>(P, u, spc, ring + (size_t)slot * P.stage_bytes, &full[slot], pol);
+        pending |= 1u << slot;
+        last_phase = (last_phase & ~(1u << slot)) | (phase << slot);
+        if (++slot == kStages) {
+          slot = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) {
+        // let the copies this CTA issued land before it exits (bounded waits)
+        for (int i = 0; i < kStages; ++i)
+          if (pending & (1u << i)) mbar_wait(&full[i], (last_phase >> i) & 1u);
+      }
+    }
+    return;
+  }
+
+  // ---------------- consumer threads ----------------
+  const int nkb = P.nkb, rps = P.rows_per_stage;
+  const int rgi = tid / nkb, kb = tid % nkb, warp_in_rg = kb / 32;
   const int wpr = nkb / 32;  // warps per row group
-  float2 x[kGemvTokens][16];
+  const int lt = kb;         // thread index within the row group
+  uint32_t xh[kGemvTokens][16];
+  int xe[kGemvTokens];
   int cur = -1, row0 = 0, mt = 0;
-  int slot = 0;
+  int slot = 0, buf = 0;
   uint32_t phase = 0;
   for (long long u = u0; u < u1; ++u) {
     const int c = (int)(u / spc), s = (int)(u % spc);
@@ -293,75 +359,78 @@ __global__ void __launch_bounds__(kMaxConsumers, 1) stream_kernel(const StreamPa
       const int4 ch = P.chunks[c];
       row0 = ch.y;
       mt = ch.z;
-      auto act_row = [&](int t) { return t < mt ? (W13 ? P.sorted_slot[row0 + t] / P.k : row0 + t) : 0; };
-      load_act(x, P.act, make_int4(act_row(0), act_row(1), act_row(2), act_row(3)), mt, P.K, kb);
+#pragma unroll
+      for (int t = 0; t < kGemvTokens; ++t) {
+        if (t < mt) {
+          const int row = W13 ? P.sorted_slot[row0 + t] / P.k : row0 + t;
+          load_x_block(xh[t], xe[t], P.act + (size_t)row * P.K + kb * 32);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) xh[t][j] = 0u;
+          xe[t] = 0;
+        }
+      }
       cur = c;
     }
     const bool ok = mbar_wait(&full[slot], phase);
-    uint8_t* sp = ring + (size_t)slot * P.stage_bytes;
+    const uint8_t* sp = ring + (size_t)slot * P.stage_bytes;
+    float* red_w = red + (buf * n_cons_warps + rgi * wpr + warp_in_rg) * 32;
     if (ok) {
       if (W13) {
         switch (mt) {
-          case 1: w13_stage<1>(P, sp, rgi, kb, lane, warp_in_rg, x, red); break;
-          case 2: w13_stage<2>(P, sp, rgi, kb, lane, warp_in_rg, x, red); break;
-          default: w13_stage<4>(P, sp, rgi, kb, lane, warp_in_rg, x, red); break;
+          case 1: w13_stage<1>(P, sp, rgi, kb, lane, xh, xe, red_w); break;
+          case 2: w13_stage<2>(P, sp, rgi, kb, lane, xh, xe, red_w); break;
+          default: w13_stage<4>(P, sp, rgi, kb, lane, xh, xe, red_w); break;
         }
       } else {
         switch (mt) {
-          case 1: w2_stage<1>(P, sp, rgi, kb, lane, warp_in_rg, x, red); break;
-          case 2: w2_stage<2>(P, sp, rgi, kb, lane, warp_in_rg, x, red); break;
-          default: w2_stage<4>(P, sp, rgi, kb, lane, warp_in_rg, x, red); break;
+          case 1: w2_stage<1>(P, sp, rgi, kb, lane, xh, xe, red_w); break;
+          case 2: w2_stage<2>(P, sp, rgi, kb, lane, xh, xe, red_w); break;
+          default: w2_stage<4>(P, sp, rgi, kb, lane, xh, xe, red_w); break;
         }
       }
     }
-    // every thread is done reading the slot; all leave together on a timeout
-    if (consumer_sync_or(n_cons, !ok)) {
-      if (tid == 0) {
-        atomicOr(P.err, kErrWaitTimeout);
-        // let the copies already issued land before the CTA exits (bounded)
-        for (int i = 0; i < kStages; ++i) {
-          const long long v = u + i;
-          if (v < u1) mbar_wait(&full[(slot + i) % kStages], ((slot + i) / kStages) & 1 ? phase ^ 1u : phase);
-        }
-      }
-      break;
-    }
-    if (tid == 0 && u + kStages < u1) issue_stage<W13>(P, u + kStages, spc, sp, &full[slot], pol);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);
     if (++slot == kStages) {
       slot = 0;
       phase ^= 1u;
     }
-    // epilogue: one thread per (row or pair, token) output of each row group
+    if (group_sync_or(1 + rgi, nkb, !ok)) {
+      if (lt == 0) atomicOr(P.err, kErrWaitTimeout);
+      break;
+    }
+    // epilogue of this row group; the reduction buffer is double-buffered, so
+    // the group's next stage can write the other half meanwhile
+    const float* red_g = red + (buf * n_cons_warps + rgi * wpr) * 32;
     const int mtp = mt == 3 ? 4 : mt;  // token count of the template the stage used
     if (W13) {
-      const int per_rg = kPairsW13 * mtp;
-      for (int o = tid; o < P.rg * per_rg; o += n_cons) {
-        const int g = o / per_rg, j = o % per_rg;  // j = pair * mtp + token
-        const int p = j / mtp, t = j % mtp;
+      const int outs = kPairsW13 * mtp;
+      if (lt < outs) {
+        const int p = lt / mtp, t = lt % mtp;  // lt = pair * mtp + token
         if (t < mt) {
           float gs = 0.f, us = 0.f;
           for (int w = 0; w < wpr; ++w) {
-            gs += red[(g * wpr + w) * 32 + 2 * j];
-            us += red[(g * wpr + w) * 32 + 2 * j + 1];
+            gs += red_g[w * 32 + 2 * lt];
+            us += red_g[w * 32 + 2 * lt + 1];
           }
-          const int i = s * rps + g * kPairsW13 + p;
+          const int i = s * rps + rgi * kPairsW13 + p;
           P.h_out[(size_t)(row0 + t) * P.I + i] = f32_to_bf16_rn(swiglu(gs, us));
         }
       }
     } else {
-      const int per_rg = kRowsW2 * mtp;
-      for (int o = tid; o < P.rg * per_rg; o += n_cons) {
-        const int g = o / per_rg, j = o % per_rg;  // j = row * mtp + token
-        const int p = j / mtp, t = j % mtp;
+      const int outs = kRowsW2 * mtp;
+      if (lt < outs) {
+        const int p = lt / mtp, t = lt % mtp;  // lt = row * mtp + token
         if (t < mt) {
           float ys = 0.f;
-          for (int w = 0; w < wpr; ++w) ys += red[(g * wpr + w) * 32 + j];
-          const int n = s * rps + g * kRowsW2 + p;
+          for (int w = 0; w < wpr; ++w) ys += red_g[w * 32 + lt];
+          const int n = s * rps + rgi * kRowsW2 + p;
           P.y_out[(size_t)(row0 + t) * P.d + n] = ys;
         }
       }
     }
-    consumer_sync(n_cons);
+    buf ^= 1;
   }
 }
 
@@ -386,7 +455,7 @@ cudaError_t launch_stream(StreamParams P, cudaStream_t st) {
     cudaFuncSetAttribute(stream_kernel<W13>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     configured = true;
   }
-  stream_kernel<W13><<<num_sms(), P.rg * P.nkb, smem, st>>>(P);
+  stream_kernel<W13><<<num_sms(), P.rg * P.nkb + 32, smem, st>>>(P);
   return cudaGetLastError();
 }
 
