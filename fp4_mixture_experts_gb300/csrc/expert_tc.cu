@@ -28,6 +28,7 @@
 #include <cuda_fp16.h>
 
 #include "moe_fp4_internal.cuh"
+#include "ptx_sm103.cuh"
 
 namespace moe_fp4 {
 namespace {
@@ -39,7 +40,6 @@ constexpr int kStagesTc = 3;
 constexpr int kNumDequantWarps = 4;
 constexpr int kTcThreads = (2 + kNumDequantWarps) * 32;
 constexpr uint32_t kTmemCols = 256;      // 2 accumulators x 128 columns
-constexpr uint32_t kWaitLimitTc = 1u << 22;
 
 constexpr int kATileBytes = kBM * kBK * 2;        // 16 KB bf16
 constexpr int kBTileBytes = kBN * kBK * 2;        // 16 KB bf16
@@ -64,50 +64,6 @@ struct TcParams {
   int acc1_offset;         // row offset of accumulator 1 (I for up rows, 128 for W2)
   int I, d;
 };
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// Bounded wait.  Returns false on timeout (after raising the abort flag) or
-// when another role already aborted.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int32_t* err) {
-  for (uint32_t i = 0; i < kWaitLimitTc; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63) == 63 && *abort_flag) return false;
-  }
-  *abort_flag = 1;
-  atomicOr(err, kErrWaitTimeout);
-  return false;
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          smem_u32(dst)),
-      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
-      : "memory");
-}
 
 // UMMA shared-memory descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
 __device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) {
@@ -235,7 +191,7 @@ tc_kernel(const __grid_constant__ CUtensorMap map_raw, const __grid_constant__ C
       for (int ks = 0; ks < nk; ++ks) {
         const int s = ks % kStagesTc;
         const uint32_t ph = (ks / kStagesTc) & 1;
-        if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, P.err)) break;
+        if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, P.err, kErrWaitTimeout)) break;
         mbar_expect_tx(&full[s], 2 * kRawTileBytes + kBTileBytes);
         tma_load_2d(smem + kOffRaw + (s * 2 + 0) * kRawTileBytes, &map_raw, ks * (kBK / 2), wrow0, &full[s]);
         tma_load_2d(smem + kOffRaw + (s * 2 + 1) * kRawTileBytes, &map_raw, ks * (kBK / 2), wrow0 + P.acc1_offset,
@@ -251,7 +207,7 @@ tc_kernel(const __grid_constant__ CUtensorMap map_raw, const __grid_constant__ C
       for (int ks = 0; ks < nk && ok; ++ks) {
         const int s = ks % kStagesTc;
         const uint32_t ph = (ks / kStagesTc) & 1;
-        if (!mbar_wait(&full[s], ph, abort_flag, P.err) || !mbar_wait(&a_ready[s], ph, abort_flag, P.err)) {
+        if (!mbar_wait(&full[s], ph, abort_flag, P.err, kErrWaitTimeout) || !mbar_wait(&a_ready[s], ph, abort_flag, P.err, kErrWaitTimeout)) {
           ok = false;
           break;
         }
@@ -269,7 +225,7 @@ tc_kernel(const __grid_constant__ CUtensorMap map_raw, const __grid_constant__ C
       }
       umma_commit(acc_full);
       // the accumulators must be final before TMEM can be freed, also on an abort
-      mbar_wait(acc_full, 0, abort_flag, P.err);
+      mbar_wait(acc_full, 0, abort_flag, P.err, kErrWaitTimeout);
     }
   } else {
     // ---------------- dequantisers, then the epilogue ----------------
@@ -284,7 +240,7 @@ tc_kernel(const __grid_constant__ CUtensorMap map_raw, const __grid_constant__ C
       const uint32_t ph = (ks / kStagesTc) & 1;
       const uint32_t sc00 = srow0[2 * ks], sc01 = srow0[2 * ks + 1];
       const uint32_t sc10 = srow1[2 * ks], sc11 = srow1[2 * ks + 1];
-      if (!mbar_wait(&full[s], ph, abort_flag, P.err)) {
+      if (!mbar_wait(&full[s], ph, abort_flag, P.err, kErrWaitTimeout)) {
         ok = false;
         break;
       }
@@ -305,7 +261,7 @@ tc_kernel(const __grid_constant__ CUtensorMap map_raw, const __grid_constant__ C
       if (lane == 0) mbar_arrive(&a_ready[s]);
     }
     // epilogue: this warp reads TMEM lanes 32*(warp % 4) .. +31
-    if (ok && mbar_wait(acc_full, 0, abort_flag, P.err)) {
+    if (ok && mbar_wait(acc_full, 0, abort_flag, P.err, kErrWaitTimeout)) {
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       const int q = warp & 3;
       const int r = q * 32 + lane;  // row within the block
@@ -338,37 +294,6 @@ tc_kernel(const __grid_constant__ CUtensorMap map_raw, const __grid_constant__ C
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
   }
-}
-
-// ---------------------------------------------------------------------------
-// host side: tensor maps
-// ---------------------------------------------------------------------------
-using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  }
-  return fn;
-}
-
-bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
-                 uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {row_bytes};
-  const cuuint32_t box[2] = {box_inner, box_outer};
-  const cuuint32_t es[2] = {1, 1};
-  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <bool W13>

@@ -3,6 +3,7 @@
 // utilities (MXFP4 decoding, bf16 rounding).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -13,7 +14,7 @@ namespace moe_fp4 {
 
 constexpr int kRouteTokensPerBlock = 32;   // tokens per routing block (8 warps x 4)
 constexpr int kRouteThreads = 256;
-constexpr int kGemvTokens = 4;             // token rows per GEMV chunk (registers hold x for 4 rows)
+constexpr int kGemvTokens = 8;             // token rows per streaming-GEMV chunk (the MMA N = 8)
 constexpr int kTcTileN = 128;              // token rows per tensor-core tile (UMMA N)
 
 // Device error word values (moe_fp4_check).
@@ -49,6 +50,12 @@ struct Workspace {
 // Lays the workspace out from `base` (nullptr: sizes only).  Returns false for
 // unsupported sizes.
 bool layout_workspace(const moe_fp4_dims& d, void* base, bool with_staging, Workspace* ws);
+
+// TMA tensor map of a 2-D row-major array (inner = contiguous dimension, in
+// elements); false if the driver rejects it.
+bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                 uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw);
+int num_sms();
 
 // ---- launchers (one per kernel family; each returns cudaGetLastError()) ----
 cudaError_t launch_route(const moe_fp4_dims& d, const float* logits, const Workspace& ws, cudaStream_t st);
