@@ -68,13 +68,15 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
 }
 
-// E8M0 byte -> 2^(s-127) in fp32 (0 -> the subnormal 2^-127)
-__device__ __forceinline__ float e8m0f(uint32_t s) {
-  return s == 0 ? __uint_as_float(0x00400000u) : __uint_as_float(s << 23);
+// Byte i (0..3) of w, an E8M0 value s, as the fp32 factor 2^(s-126) = 2 * 2^(s-127):
+// (s + 1) << 23 is a normal fp32 for every s in [0, 253] (0 needs no special
+// case); the factor 2 is taken back in the token scale.  One byte permute
+// and one integer multiply-add.
+__device__ __forceinline__ float scale2_of(uint32_t w, int i) {
+  uint32_t b;
+  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(b) : "r"(w), "r"(0x4440u + i));
+  return __uint_as_float(b * (1u << 23) + (1u << 23));
 }
-
-// byte `i` (0..3) of a word, as an E8M0 factor
-__device__ __forceinline__ float scale_of(uint32_t w, int i) { return e8m0f((w >> (8 * i)) & 0xFFu); }
 
 // Item geometry.  W13: rows [i0, i0+64) of gate and up; W2: rows [n0, n0+128).
 template <bool W13>
@@ -156,6 +158,12 @@ stream_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__
   // rows of this thread inside the stage's 128 rows (A-fragment rows g and g+8)
   const int rowA = W13 ? warp * 8 + g : warp * 16 + g;         // gate row / first W2 row
   const int rowB = W13 ? 64 + warp * 8 + g : warp * 16 + g + 8; // up row / second W2 row
+  // swizzled byte offsets of this thread's 4 packed bytes, per 16-byte chunk
+  const int box_stride = W13 ? 8192 : 16384;
+  const int ra = W13 ? rowA & 63 : rowA, rbw = W13 ? rowB & 63 : rowB;
+  const int baseA = (W13 ? (rowA >> 6) * 16384 : 0) + ra * 128 + 4 * t;
+  const int baseB = (W13 ? (rowB >> 6) * 16384 : 0) + rbw * 128 + 4 * t;
+  const int swA_ = ra & 7, swB_ = rbw & 7;
   int cur = -1, row0 = 0, mt = 0;
   int slot = 0;
   uint32_t phase = 0;
@@ -193,7 +201,7 @@ stream_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__
           }
           reinterpret_cast<uint4*>(xrow)[v] = make_uint4(o[0], o[1], o[2], o[3]);
         }
-        if (lane == 0) tok_scale[warp] = pow2f(-shift);
+        if (lane == 0) tok_scale[warp] = pow2f(-shift - 1);  // 2^-shift / 2 (scale2_of carries a factor 2)
       } else {
         for (int v = lane; v < P.K / 8; v += 32) reinterpret_cast<uint4*>(xrow)[v] = make_uint4(0, 0, 0, 0);
         if (lane == 0) tok_scale[warp] = 0.f;
@@ -209,10 +217,8 @@ stream_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__
       if (ok) {
         const uint8_t* st = ring + (size_t)slot * kStageBytes;
         // packed rows: two 128-byte-swizzled boxes (K 0..255, 256..511) of 128 (or 2 x 64) rows
-        const uint8_t* boxA = W13 ? st + (rowA >> 6) * 16384 : st;
-        const uint8_t* boxB = W13 ? st + (rowB >> 6) * 16384 : st;
-        const int ra = W13 ? rowA & 63 : rowA, rbw = W13 ? rowB & 63 : rowB;
-        const int box_stride = W13 ? 8192 : 16384;
+        const uint8_t* pa = st + baseA;
+        const uint8_t* pb = st + baseB;
         const uint4 sA = *reinterpret_cast<const uint4*>(st + kStageA + rowA * 16);
         const uint4 sB = *reinterpret_cast<const uint4*>(st + kStageA + rowB * 16);
         const uint32_t swA[4] = {sA.x, sA.y, sA.z, sA.w}, swB[4] = {sB.x, sB.y, sB.z, sB.w};
@@ -220,22 +226,20 @@ stream_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__
 #pragma unroll
         for (int blk = 0; blk < 16; ++blk) {
           const int half = blk >> 3, chunk = blk & 7;
-          const uint32_t wa = *reinterpret_cast<const uint32_t*>(boxA + half * box_stride + ra * 128 +
-                                                                 ((chunk ^ (ra & 7)) << 4) + 4 * t);
-          const uint32_t wb = *reinterpret_cast<const uint32_t*>(boxB + half * box_stride + rbw * 128 +
-                                                                 ((chunk ^ (rbw & 7)) << 4) + 4 * t);
+          const uint32_t wa = *reinterpret_cast<const uint32_t*>(pa + half * box_stride + ((chunk ^ swA_) << 4));
+          const uint32_t wb = *reinterpret_cast<const uint32_t*>(pb + half * box_stride + ((chunk ^ swB_) << 4));
           const uint4 xf = *reinterpret_cast<const uint4*>(xk + blk * 64);
           const float zero[4] = {0.f, 0.f, 0.f, 0.f};
           float cb[4];
-          uint32_t a[4] = {e2m1x2_h2(wa & 0xFFu), e2m1x2_h2(wb & 0xFFu), e2m1x2_h2((wa >> 8) & 0xFFu),
-                           e2m1x2_h2((wb >> 8) & 0xFFu)};
+          // the conversion reads the low byte of its operand (no mask needed)
+          uint32_t a[4] = {e2m1x2_h2(wa), e2m1x2_h2(wb), e2m1x2_h2(wa >> 8), e2m1x2_h2(wb >> 8)};
           mma_16816(cb, a, xf.x, xf.y, zero);
-          a[0] = e2m1x2_h2((wa >> 16) & 0xFFu);
-          a[1] = e2m1x2_h2((wb >> 16) & 0xFFu);
+          a[0] = e2m1x2_h2(wa >> 16);
+          a[1] = e2m1x2_h2(wb >> 16);
           a[2] = e2m1x2_h2(wa >> 24);
           a[3] = e2m1x2_h2(wb >> 24);
           mma_16816(cb, a, xf.z, xf.w, cb);
-          const float fa = scale_of(swA[blk >> 2], blk & 3), fb = scale_of(swB[blk >> 2], blk & 3);
+          const float fa = scale2_of(swA[blk >> 2], blk & 3), fb = scale2_of(swB[blk >> 2], blk & 3);
           acc[0] = fmaf(cb[0], fa, acc[0]);
           acc[1] = fmaf(cb[1], fa, acc[1]);
           acc[2] = fmaf(cb[2], fb, acc[2]);

@@ -21,9 +21,9 @@
  *   - weights: two E2M1 codes per byte along K, the LOW nibble holds the even
  *     K element; code bit 3 = sign, bits 0..2 index {0, .5, 1, 1.5, 2, 3, 4, 6};
  *   - scales: E8M0 bytes, value 2^(s-127), one per 32 consecutive K elements
- *     of a row.  Bytes 0xFF (NaN) and scales that push an element outside the
- *     normal bf16 range (s > 130 with the largest codes) are outside the
- *     contract: results are unspecified, nothing faults.
+ *     of a row; s in [0, 253].  Bytes 254 and 255 (NaN), and scales that push
+ *     a product or sum past the fp32 range, are outside the contract: results
+ *     are unspecified, nothing faults.
  *   - x is bf16 (raw IEEE binary32 upper halves), router logits and all
  *     outputs are fp32 except h (bf16).  Router logits must be finite.
  *
