@@ -54,6 +54,7 @@ bool layout_workspace(const moe_fp4_dims& d, void* base, bool with_staging, Work
   ws->gemv_chunks = (int4*)take((size_t)ws->max_gemv_chunks * sizeof(int4));
   ws->tc_tiles = (int4*)take((size_t)ws->max_tc_tiles * sizeof(int4));
   ws->x_perm = (uint16_t*)take(S * d.d * sizeof(uint16_t));
+  ws->x_scale = (float*)take(S * sizeof(float));
   ws->h = (uint16_t*)take(S * d.I * sizeof(uint16_t));
   ws->y = (float*)take(S * d.d * sizeof(float));
   if (with_staging) {

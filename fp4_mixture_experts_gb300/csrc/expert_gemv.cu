@@ -139,17 +139,41 @@ w2_rows_kernel(const uint16_t* __restrict__ h, const uint8_t* __restrict__ w2,
   }
 }
 
-// x_perm[r] = x[sorted_slot[r] / k]; one warp per row, 16-byte copies
+// x_perm[r] = x[sorted_slot[r] / k] as f16 scaled by 2^shift_r, with
+// x_scale[r] = 2^-shift_r; the row's largest magnitude lands in [2^14, 2^15),
+// so every bf16 value within 2^31 of it converts exactly.  One warp per row.
 __global__ void __launch_bounds__(256)
-gather_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ sorted_slot, int S, int k,
-              int d, uint16_t* __restrict__ x_perm) {
+gather_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ sorted_slot, int S, int k, int d,
+              uint16_t* __restrict__ x_perm, float* __restrict__ x_scale) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   const int nwarps = (gridDim.x * blockDim.x) >> 5;
   const int vec = d / 8;
   for (int r = warp; r < S; r += nwarps) {
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(sorted_slot[r] / k) * d);
     uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)r * d);
-    for (int v = lane; v < vec; v += 32) dst[v] = src[v];
+    uint32_t emax = 1;
+    for (int v = lane; v < vec; v += 32) {
+      const uint4 q = src[v];
+      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) emax = max(emax, max((w[i] >> 7) & 0xFFu, (w[i] >> 23) & 0xFFu));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) emax = max(emax, __shfl_xor_sync(0xFFFFFFFFu, emax, o));
+    const int shift = 141 - (int)emax;
+    const float f1 = ldexpf(1.0f, shift / 2), f2 = ldexpf(1.0f, shift - shift / 2);
+    for (int v = lane; v < vec; v += 32) {
+      const uint4 q = src[v];
+      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+      uint32_t o[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const __half2 h = __floats2half2_rn(bf16_to_f32(w[i] & 0xFFFFu) * f1 * f2, bf16_to_f32(w[i] >> 16) * f1 * f2);
+        o[i] = *reinterpret_cast<const uint32_t*>(&h);
+      }
+      dst[v] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    if (lane == 0) x_scale[r] = ldexpf(1.0f, -shift);
   }
 }
 
@@ -195,8 +219,8 @@ cudaError_t launch_gemv_w2(const moe_fp4_dims& d, const uint8_t* w2, const uint8
 cudaError_t launch_gather(const moe_fp4_dims& d, const uint16_t* x, const Workspace& ws, cudaStream_t st) {
   const int S = d.T * d.k;
   int blocks = (S + 7) / 8;
-  if (blocks > 152 * 16) blocks = 152 * 16;
-  gather_kernel<<<blocks, 256, 0, st>>>(x, ws.sorted_slot, S, d.k, d.d, ws.x_perm);
+  if (blocks > num_sms() * 16) blocks = num_sms() * 16;
+  gather_kernel<<<blocks, 256, 0, st>>>(x, ws.sorted_slot, S, d.k, d.d, ws.x_perm, ws.x_scale);
   return cudaGetLastError();
 }
 

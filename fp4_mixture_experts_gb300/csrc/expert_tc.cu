@@ -8,20 +8,24 @@
 // token tile: gate and up rows of W13 (so SwiGLU fuses into the epilogue), or
 // two adjacent 128-row blocks of W2.
 //
-// Warp roles (192 threads):
-//   warp 0      TMA producer: per 64-wide K step, the token tile (bf16, 128-byte
-//               swizzle) and the two packed weight tiles (128 rows x 32 bytes)
-//   warp 1      TMEM allocator and MMA issuer: 2 x 4 tcgen05.mma.kind::f16
-//               (M=128, N=tile, K=16) per K step, fp32 accumulators in TMEM;
-//               tcgen05.commit frees the stage
-//   warps 2..5  dequantisers: one thread per weight row; E2M1 pairs decoded by
-//               cvt.rn.f16x2.e2m1x2, moved to bf16 and scaled exactly by the
-//               E8M0 power of two (mul.bf16x2), stored in the UMMA K-major
-//               128-byte-swizzled layout; then the epilogue (tcgen05.ld,
-//               SwiGLU + bf16 rounding of h, or fp32 y)
+// Warp roles (320 threads):
+//   warp 0      TMA producer: per 64-wide K step, the token tile (up to 256
+//               rows, 128-byte swizzle) and the two packed weight tiles (128
+//               rows x 32 bytes each)
+//   warp 1      TMEM allocator (512 columns) and MMA issuer: 2 x 4
+//               tcgen05.mma.kind::f16 (M=128, N=tile, K=16) per K step, fp32
+//               accumulators in TMEM; tcgen05.commit frees the stage
+//   warps 2..9  dequantisers: one thread per weight row; E2M1 pairs decoded by
+//               cvt.rn.f16x2.e2m1x2 and scaled exactly by a power of two
+//               (mul.f16x2 for W13, mul.bf16x2 after a bf16 re-encoding for
+//               W2), stored in the UMMA K-major 128-byte-swizzled layout; then
+//               the epilogue (tcgen05.ld, SwiGLU + bf16 rounding of h, or y)
 // Weights are dequantised exactly (an E2M1 value times a power of two has
-// 2 significant bits), so the MMA multiplies the same bf16 products the
-// definition does and accumulates them in fp32.  Every mbarrier wait is
+// 2 significant bits), so the MMA multiplies exact products and accumulates
+// them in fp32.  W13 runs on f16 operands: the weight row is scaled by
+// 2^(s - s_ref) (exact within 36 binades of the row's largest scale) and the
+// activation row by the gather's power of two; both factors come back in the
+// epilogue.  Every mbarrier wait is
 // bounded; a timeout sets the error word and an abort flag that releases the
 // other roles, and TMEM is always freed.
 #include <cuda.h>
@@ -35,19 +39,21 @@ namespace {
 
 constexpr int kBM = 128;                 // weight rows per accumulator
 constexpr int kBK = 64;                  // K elements per stage
-constexpr int kBN = kTcTileN;            // token rows per tile (<= 128)
+constexpr int kBN = kTcTileN;            // token rows per tile (<= 256)
 constexpr int kStagesTc = 3;
-constexpr int kNumDequantWarps = 4;
-constexpr int kTcThreads = (2 + kNumDequantWarps) * 32;
-constexpr uint32_t kTmemCols = 256;      // 2 accumulators x 128 columns
+constexpr int kDqWarps = 8;
+constexpr int kTcThreads = (2 + kDqWarps) * 32;
+constexpr uint32_t kTmemCols = 512;      // 2 accumulators x 256 columns
 
-constexpr int kATileBytes = kBM * kBK * 2;        // 16 KB bf16
-constexpr int kBTileBytes = kBN * kBK * 2;        // 16 KB bf16
+constexpr int kATileBytes = kBM * kBK * 2;        // 16 KB
+constexpr int kBHalfBytes = 128 * kBK * 2;        // 16 KB: 128 token rows
+constexpr int kBTileBytes = kBN * kBK * 2;        // 32 KB
 constexpr int kRawTileBytes = kBM * kBK / 2;      // 4 KB packed
 constexpr int kOffA = 0;                                       // [stage][acc]
 constexpr int kOffB = kOffA + kStagesTc * 2 * kATileBytes;     // [stage]
 constexpr int kOffRaw = kOffB + kStagesTc * kBTileBytes;       // [stage][acc]
-constexpr int kOffBar = kOffRaw + kStagesTc * 2 * kRawTileBytes;
+constexpr int kOffRowScale = kOffRaw + kStagesTc * 2 * kRawTileBytes;
+constexpr int kOffBar = kOffRowScale + 2 * kBM * 4;
 constexpr int kSmemTc = kOffBar + 256 + 1024;                  // + barriers, slack for 1 KB alignment
 
 struct TcParams {
@@ -57,6 +63,7 @@ struct TcParams {
   int32_t* err;
   uint16_t* h_out;         // W13: h [S, I]
   float* y_out;            // W2: y [S, d]
+  const float* x_scale;    // W13: per sorted row, the inverse activation scale
   int K;                   // reduction length
   int rows_per_expert;     // rows of the weight tensor per expert (2I or d)
   int mblocks;             // CTAs per token tile along the weight rows
@@ -76,12 +83,13 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) {
   return d;
 }
 
-// Instruction descriptor of kind::f16: bf16 x bf16 -> f32, both K-major.
-__device__ __forceinline__ uint32_t idesc_bf16(int M, int N) {
-  return (1u << 4)                      // D format f32
-         | (1u << 7) | (1u << 10)       // A, B format bf16
-         | ((uint32_t)(N >> 3) << 17)   // N
-         | ((uint32_t)(M >> 4) << 24);  // M
+// Instruction descriptor of kind::f16 with f32 accumulation, both operands
+// K-major; A and B share one type (f16 = 0, bf16 = 1).
+__device__ __forceinline__ uint32_t idesc_f16kind(int M, int N, uint32_t ab_type) {
+  return (1u << 4)                                // D format f32
+         | (ab_type << 7) | (ab_type << 10)       // A, B format
+         | ((uint32_t)(N >> 3) << 17)             // N
+         | ((uint32_t)(M >> 4) << 24);            // M
 }
 
 __device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
@@ -144,11 +152,41 @@ __device__ __forceinline__ uint4 dequant8(uint32_t packed, uint32_t s) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-template <bool W13>
+__device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// f16x2 (m, m) with m = 2^e for e in [-24, 15]: normal for e >= -14,
+// subnormal below; 0 for e < -24
+__device__ __forceinline__ uint32_t f16x2_pow2(int e) {
+  const uint32_t b = e >= -14 ? (uint32_t)(e + 15) << 10 : (e >= -24 ? 1u << (e + 24) : 0u);
+  return b | (b << 16);
+}
+
+// 4 packed bytes (8 E2M1 codes, K ascending) -> 8 exact f16 values times 2^e
+// (e = s - s_ref of the row; exact while e >= -23)
+__device__ __forceinline__ uint4 dequant8_f16(uint32_t packed, int e) {
+  const uint32_t m = f16x2_pow2(e);
+  uint32_t o[4];
+#pragma unroll
+  for (int b = 0; b < 4; ++b) o[b] = f16x2_mul(e2m1x2_to_f16x2(packed >> (8 * b)), m);
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Tile of one CTA: token rows [row0, row0 + n) of one expert (n <= 256) times
+// two 128-row weight blocks.  F16 (W13): operands f16, weight rows scaled by
+// 2^(s - s_ref(row)) with s_ref = (largest E8M0 of the row) - 13, activations
+// by the per-row power of two of the gather; both undone in the epilogue (per
+// TMEM lane and column), then SwiGLU.  Otherwise (W2): operands bf16
+// (weights exactly 2^(s-127) * code, h as written), epilogue writes fp32 y.
+template <bool F16>
 __global__ void __launch_bounds__(kTcThreads, 1)
 tc_kernel(const __grid_constant__ CUtensorMap map_raw, const __grid_constant__ CUtensorMap map_b, const TcParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float* rowscale = reinterpret_cast<float*>(smem + kOffRowScale);  // [2][128]
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint64_t* a_ready = full + kStagesTc;
   uint64_t* empty = a_ready + kStagesTc;
@@ -159,21 +197,22 @@ tc_kernel(const __grid_constant__ CUtensorMap map_raw, const __grid_constant__ C
   const int tile = blockIdx.x / P.mblocks, mb = blockIdx.x % P.mblocks;
   if (tile >= P.counts[2]) return;
   const int4 tl = P.tiles[tile];
-  const int e = tl.x, row0 = tl.y, n = tl.z;
+  const int row0 = tl.y, n = tl.z;
   const int n_mma = (n + 15) & ~15;
-  const int wrow0 = e * P.rows_per_expert + mb * P.block_rows;
+  const bool two_b = n > 128;
+  const int wrow0 = tl.x * P.rows_per_expert + mb * P.block_rows;
   const int nk = P.K / kBK;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStagesTc; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&a_ready[s], kNumDequantWarps);
+      mbar_init(&a_ready[s], kDqWarps);
       mbar_init(&empty[s], 1);
     }
     mbar_init(acc_full, 1);
     *abort_flag = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_fence_init();
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -188,29 +227,30 @@ tc_kernel(const __grid_constant__ CUtensorMap map_raw, const __grid_constant__ C
   if (warp == 0) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
+      const uint32_t bytes = 2 * kRawTileBytes + (two_b ? 2 : 1) * kBHalfBytes;
       for (int ks = 0; ks < nk; ++ks) {
         const int s = ks % kStagesTc;
         const uint32_t ph = (ks / kStagesTc) & 1;
         if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, P.err, kErrWaitTimeout)) break;
-        mbar_expect_tx(&full[s], 2 * kRawTileBytes + kBTileBytes);
-        tma_load_2d(smem + kOffRaw + (s * 2 + 0) * kRawTileBytes, &map_raw, ks * (kBK / 2), wrow0, &full[s]);
-        tma_load_2d(smem + kOffRaw + (s * 2 + 1) * kRawTileBytes, &map_raw, ks * (kBK / 2), wrow0 + P.acc1_offset,
-                    &full[s]);
-        tma_load_2d(smem + kOffB + s * kBTileBytes, &map_b, ks * kBK, row0, &full[s]);
+        mbar_expect_tx(&full[s], bytes);
+        uint8_t* raw = smem + kOffRaw + s * 2 * kRawTileBytes;
+        uint8_t* b = smem + kOffB + s * kBTileBytes;
+        tma_load_2d(raw, &map_raw, ks * (kBK / 2), wrow0, &full[s]);
+        tma_load_2d(raw + kRawTileBytes, &map_raw, ks * (kBK / 2), wrow0 + P.acc1_offset, &full[s]);
+        tma_load_2d(b, &map_b, ks * kBK, row0, &full[s]);
+        if (two_b) tma_load_2d(b + kBHalfBytes, &map_b, ks * kBK, row0 + 128, &full[s]);
       }
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(kBM, n_mma);
-      bool ok = true;
-      for (int ks = 0; ks < nk && ok; ++ks) {
+      const uint32_t idesc = idesc_f16kind(kBM, n_mma, F16 ? 0u : 1u);
+      for (int ks = 0; ks < nk; ++ks) {
         const int s = ks % kStagesTc;
         const uint32_t ph = (ks / kStagesTc) & 1;
-        if (!mbar_wait(&full[s], ph, abort_flag, P.err, kErrWaitTimeout) || !mbar_wait(&a_ready[s], ph, abort_flag, P.err, kErrWaitTimeout)) {
-          ok = false;
+        if (!mbar_wait(&full[s], ph, abort_flag, P.err, kErrWaitTimeout) ||
+            !mbar_wait(&a_ready[s], ph, abort_flag, P.err, kErrWaitTimeout))
           break;
-        }
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const uint32_t b_addr = smem_u32(smem + kOffB + s * kBTileBytes);
 #pragma unroll
@@ -218,7 +258,7 @@ tc_kernel(const __grid_constant__ CUtensorMap map_raw, const __grid_constant__ C
           const uint32_t a_addr = smem_u32(smem + kOffA + (s * 2 + acc) * kATileBytes);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
-            umma_bf16(tmem + acc * 128, desc_sw128(a_addr + kk * 32), desc_sw128(b_addr + kk * 32), idesc,
+            umma_bf16(tmem + acc * 256, desc_sw128(a_addr + kk * 32), desc_sw128(b_addr + kk * 32), idesc,
                       (ks > 0 || kk > 0) ? 1u : 0u);
         }
         umma_commit(&empty[s]);
@@ -228,54 +268,77 @@ tc_kernel(const __grid_constant__ CUtensorMap map_raw, const __grid_constant__ C
       mbar_wait(acc_full, 0, abort_flag, P.err, kErrWaitTimeout);
     }
   } else {
-    // ---------------- dequantisers, then the epilogue ----------------
-    const int t = threadIdx.x - 64;       // weight row within the 128-row block
-    const int kpr = P.K / 32;             // scale bytes per row
-    const uint8_t* srow0 = P.scales + (size_t)(wrow0 + t) * kpr;
-    const uint8_t* srow1 = P.scales + (size_t)(wrow0 + P.acc1_offset + t) * kpr;
-    const int sw = t & 7;
+    // ---------------- dequantisers (one weight row each), then the epilogue ----------------
+    const int dq = warp - 2;
+    const int acc = dq >> 2;                 // 0: first block (gate), 1: second block (up)
+    const int r = (dq & 3) * 32 + lane;      // row within the 128-row block
+    const int wrow = wrow0 + acc * P.acc1_offset + r;
+    const int kpr = P.K / 32;                // scale bytes per row
+    const uint8_t* srow = P.scales + (size_t)wrow * kpr;
+    int s_ref = 0;
+    if (F16) {
+      uint32_t smax = 0;
+      for (int i = 0; i < kpr; i += 4) {
+        const uint32_t w4 = *reinterpret_cast<const uint32_t*>(srow + i);
+        smax = max(smax, max(max(w4 & 0xFFu, (w4 >> 8) & 0xFFu), max((w4 >> 16) & 0xFFu, w4 >> 24)));
+      }
+      s_ref = (int)smax - 13;
+      rowscale[acc * 128 + r] = pow2f(s_ref - 127);
+    }
+    const int sw = r & 7;
+    const int c_first = (lane >> 2) & 1;    // conflict-free order of the two 16-byte halves
+    uint32_t sc_next = *reinterpret_cast<const uint16_t*>(srow);
     bool ok = true;
     for (int ks = 0; ks < nk; ++ks) {
       const int s = ks % kStagesTc;
       const uint32_t ph = (ks / kStagesTc) & 1;
-      const uint32_t sc00 = srow0[2 * ks], sc01 = srow0[2 * ks + 1];
-      const uint32_t sc10 = srow1[2 * ks], sc11 = srow1[2 * ks + 1];
+      const uint32_t sc = sc_next;
+      if (ks + 1 < nk) sc_next = *reinterpret_cast<const uint16_t*>(srow + 2 * (ks + 1));
       if (!mbar_wait(&full[s], ph, abort_flag, P.err, kErrWaitTimeout)) {
         ok = false;
         break;
       }
+      const uint8_t* raw = smem + kOffRaw + (s * 2 + acc) * kRawTileBytes + r * 32;
+      const uint4 h0 = *reinterpret_cast<const uint4*>(raw + 16 * c_first);
+      const uint4 h1 = *reinterpret_cast<const uint4*>(raw + 16 * (c_first ^ 1));
+      const uint4 lo = c_first ? h1 : h0, hi = c_first ? h0 : h1;
+      const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+      uint8_t* arow = smem + kOffA + (s * 2 + acc) * kATileBytes + (r >> 3) * 1024 + (r & 7) * 128;
+      const uint32_t s0 = sc & 0xFFu, s1 = sc >> 8;
 #pragma unroll
-      for (int acc = 0; acc < 2; ++acc) {
-        const uint4* raw = reinterpret_cast<const uint4*>(smem + kOffRaw + (s * 2 + acc) * kRawTileBytes + t * 32);
-        const uint4 r0 = raw[0], r1 = raw[1];
-        const uint32_t w[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
-        uint8_t* arow = smem + kOffA + (s * 2 + acc) * kATileBytes + (t >> 3) * 1024 + (t & 7) * 128;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint32_t sc = acc == 0 ? (c < 4 ? sc00 : sc01) : (c < 4 ? sc10 : sc11);
-          *reinterpret_cast<uint4*>(arow + ((c ^ sw) << 4)) = dequant8(w[c], sc);
-        }
+      for (int c = 0; c < 8; ++c) {
+        const uint32_t sb = c < 4 ? s0 : s1;
+        const uint4 v = F16 ? dequant8_f16(w[c], (int)sb - s_ref) : dequant8(w[c], sb);
+        *reinterpret_cast<uint4*>(arow + ((c ^ sw) << 4)) = v;
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
       if (lane == 0) mbar_arrive(&a_ready[s]);
     }
-    // epilogue: this warp reads TMEM lanes 32*(warp % 4) .. +31
+    // the row scales written above must be visible to every epilogue warp
+    asm volatile("bar.sync 1, %0;" ::"r"(kDqWarps * 32) : "memory");
     if (ok && mbar_wait(acc_full, 0, abort_flag, P.err, kErrWaitTimeout)) {
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const int q = warp & 3;
-      const int r = q * 32 + lane;  // row within the block
-      for (int c0 = 0; c0 < n_mma; c0 += 32) {
+      const int q = warp & 3;               // TMEM lane quadrant this warp may read
+      const int rr = q * 32 + lane;         // weight row of this thread's TMEM lane
+      const int c_begin = (dq >> 2) * 128;  // this warp's half of the columns
+      const float rs0 = F16 ? rowscale[rr] : 1.f, rs1 = F16 ? rowscale[128 + rr] : 1.f;
+      for (int c0 = c_begin; c0 < c_begin + 128 && c0 < n_mma; c0 += 32) {
         float a0[32], a1[32];
         tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + c0, a0);
-        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + 128 + c0, a1);
-        if (W13) {
-          const int i = mb * kBM + r;
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + 256 + c0, a1);
+        if (F16) {
+          const float xs_l = c0 + lane < n ? P.x_scale[row0 + c0 + lane] : 0.f;
+          const int i = mb * kBM + rr;
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (c0 + j < n) P.h_out[(size_t)(row0 + c0 + j) * P.I + i] = f32_to_bf16_rn(swiglu(a0[j], a1[j]));
+          for (int j = 0; j < 32; ++j) {
+            const float xs = __shfl_sync(0xFFFFFFFFu, xs_l, j);
+            if (c0 + j < n)
+              P.h_out[(size_t)(row0 + c0 + j) * P.I + i] =
+                  f32_to_bf16_rn(swiglu(a0[j] * rs0 * xs, a1[j] * rs1 * xs));
+          }
         } else {
-          const int nrow = mb * P.block_rows + r;
+          const int nrow = mb * P.block_rows + rr;
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             if (c0 + j < n) {
@@ -296,16 +359,16 @@ tc_kernel(const __grid_constant__ CUtensorMap map_raw, const __grid_constant__ C
   }
 }
 
-template <bool W13>
+template <bool F16>
 cudaError_t launch_tc(const CUtensorMap& raw, const CUtensorMap& b, const TcParams& P, int max_tiles, cudaStream_t st) {
   static bool configured = false;
   if (!configured) {
-    cudaFuncSetAttribute(tc_kernel<W13>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTc);
+    cudaFuncSetAttribute(tc_kernel<F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTc);
     configured = true;
   }
   const long long grid = (long long)max_tiles * P.mblocks;
   if (grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-  tc_kernel<W13><<<(unsigned)grid, kTcThreads, kSmemTc, st>>>(raw, b, P);
+  tc_kernel<F16><<<(unsigned)grid, kTcThreads, kSmemTc, st>>>(raw, b, P);
   return cudaGetLastError();
 }
 
@@ -317,7 +380,7 @@ cudaError_t launch_tc_w13(const moe_fp4_dims& d, const uint8_t* w13, const uint8
   CUtensorMap raw, b;
   if (!make_map_2d(&raw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w13, d.d / 2, (uint64_t)d.E * 2 * d.I, d.d / 2, kBK / 2, kBM,
                    CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !make_map_2d(&b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ws.x_perm, d.d, S, (uint64_t)d.d * 2, kBK, kBN,
+      !make_map_2d(&b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws.x_perm, d.d, S, (uint64_t)d.d * 2, kBK, 128,
                    CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   TcParams P{};
@@ -326,6 +389,7 @@ cudaError_t launch_tc_w13(const moe_fp4_dims& d, const uint8_t* w13, const uint8
   P.counts = ws.counts;
   P.err = ws.err;
   P.h_out = ws.h;
+  P.x_scale = ws.x_scale;
   P.K = d.d;
   P.rows_per_expert = 2 * d.I;
   P.mblocks = d.I / kBM;
@@ -342,7 +406,7 @@ cudaError_t launch_tc_w2(const moe_fp4_dims& d, const uint8_t* w2, const uint8_t
   CUtensorMap raw, b;
   if (!make_map_2d(&raw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w2, d.I / 2, (uint64_t)d.E * d.d, d.I / 2, kBK / 2, kBM,
                    CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !make_map_2d(&b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ws.h, d.I, S, (uint64_t)d.I * 2, kBK, kBN,
+      !make_map_2d(&b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ws.h, d.I, S, (uint64_t)d.I * 2, kBK, 128,
                    CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   TcParams P{};

@@ -15,7 +15,7 @@ namespace moe_fp4 {
 constexpr int kRouteTokensPerBlock = 32;   // tokens per routing block (8 warps x 4)
 constexpr int kRouteThreads = 256;
 constexpr int kGemvTokens = 8;             // token rows per streaming-GEMV chunk (the MMA N = 8)
-constexpr int kTcTileN = 128;              // token rows per tensor-core tile (UMMA N)
+constexpr int kTcTileN = 256;              // max token rows per tensor-core tile (UMMA N)
 
 // Device error word values (moe_fp4_check).
 constexpr int kErrBadExpertId = 1;
@@ -34,7 +34,8 @@ struct Workspace {
   int32_t* slot_pos;      // [S]
   int4* gemv_chunks;      // [max_gemv_chunks]  (expert, first sorted row, rows, 0)
   int4* tc_tiles;         // [max_tc_tiles]     (expert, first sorted row, rows, 0)
-  uint16_t* x_perm;       // [S, d] bf16 (tensor-core path)
+  uint16_t* x_perm;       // [S, d] f16, each row scaled by a power of two (tensor-core path)
+  float* x_scale;         // [S]    the inverse of that power of two
   uint16_t* h;            // [S, I] bf16
   float* y;               // [S, d] fp32 expert outputs in sorted-row order
   // staging for the host-buffer entry point (only laid out when requested)

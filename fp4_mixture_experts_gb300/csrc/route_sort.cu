@@ -29,6 +29,43 @@ __device__ __forceinline__ uint32_t ordered_key(float v) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Top-k of one token's E logits (staged in `row`, shared memory) by (value
+// desc, index asc) and the softmax over the k picked, shifted by the slot-0
+// logit with the sum in slot order.  Lane j < k returns slot j.
+__device__ __forceinline__ void topk_softmax_warp(const float* row, int E, int k, int lane, int& id, float& w) {
+  const int nv = (E + 31) >> 5;  // entries per lane: e = lane + 32 i
+  uint32_t taken = 0;            // bit i: entry lane + 32 i already picked
+  int my_id = 0;
+  float my_val = 0.f;
+  for (int r = 0; r < k; ++r) {
+    unsigned long long best = 0;
+    for (int i = 0; i < nv; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !((taken >> i) & 1u)) {
+        unsigned long long key = ((unsigned long long)ordered_key(row[e]) << 32) | (0xFFFFFFFFu - (uint32_t)e);
+        best = key > best ? key : best;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+      best = other > best ? other : best;
+    }
+    const int e_star = (int)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFu));
+    if ((e_star & 31) == lane) taken |= 1u << (e_star >> 5);
+    if (lane == r) {
+      my_id = e_star;
+      my_val = row[e_star];
+    }
+  }
+  const float m = __shfl_sync(0xFFFFFFFFu, my_val, 0);
+  const float ex = lane < k ? expf(my_val - m) : 0.f;
+  float sum = 0.f;
+  for (int j = 0; j < k; ++j) sum += __shfl_sync(0xFFFFFFFFu, ex, j);
+  id = my_id;
+  w = ex / sum;
+}
+
 __global__ void __launch_bounds__(kRouteThreads)
 route_hist_kernel(const float* __restrict__ logits, int T, int E, int k,
                   int32_t* __restrict__ topk_ids, float* __restrict__ topk_w,
@@ -36,53 +73,25 @@ route_hist_kernel(const float* __restrict__ logits, int T, int E, int k,
   extern __shared__ float smem[];
   // the error words start clear on every call (later kernels of the call set them)
   if (blockIdx.x == 0 && threadIdx.x < 4) err[threadIdx.x] = 0;
-  float* rows = smem;                                   // [kWarps][E]
+  float* rows = smem;                                     // [kWarps][E]
   int* hist = reinterpret_cast<int*>(smem + kWarps * E);  // [E]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
   float* row = rows + warp * E;
-  const int nv = (E + 31) >> 5;  // entries per lane: e = lane + 32 i
   for (int tt = 0; tt < kTokPerWarp; ++tt) {
     const int t = blockIdx.x * kRouteTokensPerBlock + warp * kTokPerWarp + tt;
     if (t >= T) break;
     const float* src = logits + (size_t)t * E;
     for (int e = lane; e < E; e += 32) row[e] = src[e];
     __syncwarp();
-    uint32_t taken = 0;  // bit i: entry lane + 32 i already picked
-    int my_id = 0;
-    float my_val = 0.f;
-    for (int r = 0; r < k; ++r) {
-      unsigned long long best = 0;
-      for (int i = 0; i < nv; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E && !((taken >> i) & 1u)) {
-          unsigned long long key = ((unsigned long long)ordered_key(row[e]) << 32) | (0xFFFFFFFFu - (uint32_t)e);
-          best = key > best ? key : best;
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
-        best = other > best ? other : best;
-      }
-      const int e_star = (int)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFu));
-      if ((e_star & 31) == lane) taken |= 1u << (e_star >> 5);
-      if (lane == r) {
-        my_id = e_star;
-        my_val = row[e_star];
-      }
-    }
-    // softmax over the k picked logits, shifted by the slot-0 logit; the sum
-    // runs in slot order
-    const float m = __shfl_sync(0xFFFFFFFFu, my_val, 0);
-    const float ex = lane < k ? expf(my_val - m) : 0.f;
-    float sum = 0.f;
-    for (int j = 0; j < k; ++j) sum += __shfl_sync(0xFFFFFFFFu, ex, j);
+    int id;
+    float w;
+    topk_softmax_warp(row, E, k, lane, id, w);
     if (lane < k) {
-      topk_ids[(size_t)t * k + lane] = my_id;
-      topk_w[(size_t)t * k + lane] = ex / sum;
-      atomicAdd(&hist[my_id], 1);
+      topk_ids[(size_t)t * k + lane] = id;
+      topk_w[(size_t)t * k + lane] = w;
+      atomicAdd(&hist[id], 1);
     }
     __syncwarp();
   }
@@ -154,11 +163,12 @@ sort_scan_kernel(int32_t* __restrict__ block_hist, int nb, int E, int32_t* __res
   for (int c = 0; c < nch; ++c)
     gemv_chunks[cpos + c] = make_int4(e, off + c * kGemvTokens, min(kGemvTokens, cnt - c * kGemvTokens), 0);
   // tensor-core tiles of up to kTcTileN rows
+  // tensor-core tiles: ceil(cnt / kTcTileN) tiles of equal size (rounded up to 16)
   const int ntl = ok ? (cnt + kTcTileN - 1) / kTcTileN : 0;
+  const int per = ntl ? (((cnt + ntl - 1) / ntl + 15) & ~15) : 0;
   int n_tiles;
   const int tpos = block_exclusive_scan(ntl, scratch, &n_tiles);
-  for (int c = 0; c < ntl; ++c)
-    tc_tiles[tpos + c] = make_int4(e, off + c * kTcTileN, min(kTcTileN, cnt - c * kTcTileN), 0);
+  for (int c = 0; c < ntl; ++c) tc_tiles[tpos + c] = make_int4(e, off + c * per, min(per, cnt - c * per), 0);
   if (e == 0) {
     counts[0] = n_active;
     counts[1] = n_chunks;
@@ -207,10 +217,105 @@ scatter_kernel(const int32_t* __restrict__ topk_ids, const int32_t* __restrict__
   }
 }
 
+
+// One block does everything when all tokens fit one routing block (T <= 32,
+// the decode shape): routing by 32 warps, per-expert totals, offsets and work
+// lists, then the stable scatter by a single warp walking the slots in order.
+__global__ void __launch_bounds__(1024)
+route_small_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ topk_ids,
+                   float* __restrict__ topk_w, int32_t* __restrict__ offsets, int32_t* __restrict__ active,
+                   int32_t* __restrict__ counts, int4* __restrict__ gemv_chunks, int4* __restrict__ tc_tiles,
+                   int32_t* __restrict__ sorted_slot, int32_t* __restrict__ slot_pos, int32_t* __restrict__ err) {
+  extern __shared__ int smem_small[];
+  int* hist = smem_small;                            // [E] counts, then running positions
+  int* ids_s = hist + E;                             // [T*k]
+  float* rows = reinterpret_cast<float*>(ids_s + kRouteTokensPerBlock * 32);  // [32 warps][E]
+  __shared__ int scratch[33];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x < 4) err[threadIdx.x] = 0;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  if (warp < T) {
+    float* row = rows + warp * E;
+    const float* src = logits + (size_t)warp * E;
+    for (int e = lane; e < E; e += 32) row[e] = src[e];
+    __syncwarp();
+    int id;
+    float w;
+    topk_softmax_warp(row, E, k, lane, id, w);
+    if (lane < k) {
+      topk_ids[warp * k + lane] = id;
+      topk_w[warp * k + lane] = w;
+      ids_s[warp * k + lane] = id;
+      atomicAdd(&hist[id], 1);
+    }
+  }
+  __syncthreads();
+  const int e = threadIdx.x;
+  const bool ok = e < E;
+  const int cnt = ok ? hist[e] : 0;
+  int total;
+  const int off = block_exclusive_scan(cnt, scratch, &total);
+  if (ok) offsets[e] = off;
+  if (e == 0) offsets[E] = total;
+  int n_active;
+  const int apos = block_exclusive_scan(ok && cnt > 0 ? 1 : 0, scratch, &n_active);
+  if (ok && cnt > 0) active[apos] = e;
+  const int nch = ok ? (cnt + kGemvTokens - 1) / kGemvTokens : 0;
+  int n_chunks;
+  const int cpos = block_exclusive_scan(nch, scratch, &n_chunks);
+  for (int c = 0; c < nch; ++c)
+    gemv_chunks[cpos + c] = make_int4(e, off + c * kGemvTokens, min(kGemvTokens, cnt - c * kGemvTokens), 0);
+  // tensor-core tiles: ceil(cnt / kTcTileN) tiles of equal size (rounded up to 16)
+  const int ntl = ok ? (cnt + kTcTileN - 1) / kTcTileN : 0;
+  const int per = ntl ? (((cnt + ntl - 1) / ntl + 15) & ~15) : 0;
+  int n_tiles;
+  const int tpos = block_exclusive_scan(ntl, scratch, &n_tiles);
+  for (int c = 0; c < ntl; ++c) tc_tiles[tpos + c] = make_int4(e, off + c * per, min(per, cnt - c * per), 0);
+  if (e == 0) {
+    counts[0] = n_active;
+    counts[1] = n_chunks;
+    counts[2] = n_tiles;
+    counts[3] = 0;
+  }
+  if (ok) hist[e] = off;  // running position of each expert
+  __syncthreads();
+  if (warp == 0) {
+    const int S = T * k;
+    for (int f0 = 0; f0 < S; f0 += 32) {
+      const int f = f0 + lane;
+      const int ef = f < S ? ids_s[f] : -1;
+      const unsigned peers = __match_any_sync(0xFFFFFFFFu, ef);
+      const int rank = __popc(peers & ((1u << lane) - 1u));
+      if (ef >= 0) {
+        const int pos = hist[ef] + rank;
+        sorted_slot[pos] = f;
+        slot_pos[f] = pos;
+      }
+      __syncwarp();
+      if (ef >= 0 && rank == 0) hist[ef] += __popc(peers);
+      __syncwarp();
+    }
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_route(const moe_fp4_dims& d, const float* logits, const Workspace& ws, cudaStream_t st) {
   const int nb = ws.nb_route;
+  if (nb == 1) {
+    const size_t smem = (size_t)d.E * sizeof(int) + kRouteTokensPerBlock * 32 * sizeof(int) +
+                        (size_t)32 * d.E * sizeof(float);
+    static bool configured = false;
+    if (!configured) {
+      cudaFuncSetAttribute(route_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
+      configured = true;
+    }
+    route_small_kernel<<<1, 1024, smem, st>>>(logits, d.T, d.E, d.k, ws.topk_ids, ws.topk_w, ws.offsets, ws.active,
+                                              ws.counts, ws.gemv_chunks, ws.tc_tiles, ws.sorted_slot, ws.slot_pos,
+                                              ws.err);
+    return cudaGetLastError();
+  }
   size_t smem1 = (size_t)(kWarps * d.E) * sizeof(float) + (size_t)d.E * sizeof(int);
   route_hist_kernel<<<nb, kRouteThreads, smem1, st>>>(logits, d.T, d.E, d.k, ws.topk_ids, ws.topk_w,
                                                      ws.block_hist, ws.err);
