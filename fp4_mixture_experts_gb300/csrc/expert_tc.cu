@@ -8,14 +8,17 @@
 // token tile: gate and up rows of W13 (so SwiGLU fuses into the epilogue), or
 // two adjacent 128-row blocks of W2.
 //
-// Warp roles (320 threads):
-//   warp 0      TMA producer: per 64-wide K step, the token tile (up to 256
-//               rows, 128-byte swizzle) and the two packed weight tiles (128
-//               rows x 32 bytes each)
+// Warp roles (352 threads), three decoupled rings per 64-wide K step:
+//   warp 0      TMA producer of the packed weight tiles (2 x 128 rows x 32
+//               bytes, 6-deep ring: the HBM stream)
+//   warp 10     TMA producer of the token tile (up to 256 rows, 128-byte
+//               swizzle, 3-deep ring: mostly L2 hits, shared by the CTAs of
+//               one expert)
 //   warp 1      TMEM allocator (512 columns) and MMA issuer: 2 x 4
 //               tcgen05.mma.kind::f16 (M=128, N=tile, K=16) per K step, fp32
-//               accumulators in TMEM; tcgen05.commit frees the stage
-//   warps 2..9  dequantisers: one thread per weight row; E2M1 pairs decoded by
+//               accumulators in TMEM; tcgen05.commit frees the token and
+//               weight slots
+//   warps 2..9  dequantisers (2-deep ring of dequantised tiles): one thread per weight row; E2M1 pairs decoded by
 //               cvt.rn.f16x2.e2m1x2 and scaled exactly by a power of two
 //               (mul.f16x2 for W13, mul.bf16x2 after a bf16 re-encoding for
 //               W2), stored in the UMMA K-major 128-byte-swizzled layout; then
@@ -40,9 +43,11 @@ namespace {
 constexpr int kBM = 128;                 // weight rows per accumulator
 constexpr int kBK = 64;                  // K elements per stage
 constexpr int kBN = kTcTileN;            // token rows per tile (<= 256)
-constexpr int kStagesTc = 3;
+constexpr int kStagesA = 2;              // dequantised weight tiles (dequant -> MMA)
+constexpr int kStagesB = 3;              // token tiles (TMA -> MMA)
+constexpr int kStagesRaw = 6;            // packed weight tiles (TMA -> dequant)
 constexpr int kDqWarps = 8;
-constexpr int kTcThreads = (2 + kDqWarps) * 32;
+constexpr int kTcThreads = (3 + kDqWarps) * 32;  // raw producer, MMA, 8 dequant, token producer
 constexpr uint32_t kTmemCols = 512;      // 2 accumulators x 256 columns
 
 constexpr int kATileBytes = kBM * kBK * 2;        // 16 KB
@@ -50,9 +55,9 @@ constexpr int kBHalfBytes = 128 * kBK * 2;        // 16 KB: 128 token rows
 constexpr int kBTileBytes = kBN * kBK * 2;        // 32 KB
 constexpr int kRawTileBytes = kBM * kBK / 2;      // 4 KB packed
 constexpr int kOffA = 0;                                       // [stage][acc]
-constexpr int kOffB = kOffA + kStagesTc * 2 * kATileBytes;     // [stage]
-constexpr int kOffRaw = kOffB + kStagesTc * kBTileBytes;       // [stage][acc]
-constexpr int kOffRowScale = kOffRaw + kStagesTc * 2 * kRawTileBytes;
+constexpr int kOffB = kOffA + kStagesA * 2 * kATileBytes;      // [stage]
+constexpr int kOffRaw = kOffB + kStagesB * kBTileBytes;        // [stage][acc]
+constexpr int kOffRowScale = kOffRaw + kStagesRaw * 2 * kRawTileBytes;
 constexpr int kOffBar = kOffRowScale + 2 * kBM * 4;
 constexpr int kSmemTc = kOffBar + 256 + 1024;                  // + barriers, slack for 1 KB alignment
 
@@ -187,10 +192,13 @@ tc_kernel(const __grid_constant__ CUtensorMap map_raw, const __grid_constant__ C
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* rowscale = reinterpret_cast<float*>(smem + kOffRowScale);  // [2][128]
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint64_t* a_ready = full + kStagesTc;
-  uint64_t* empty = a_ready + kStagesTc;
-  uint64_t* acc_full = empty + kStagesTc;
+  uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* raw_empty = raw_full + kStagesRaw;
+  uint64_t* b_full = raw_empty + kStagesRaw;
+  uint64_t* b_empty = b_full + kStagesB;
+  uint64_t* a_full = b_empty + kStagesB;
+  uint64_t* a_empty = a_full + kStagesA;
+  uint64_t* acc_full = a_empty + kStagesA;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -205,10 +213,17 @@ tc_kernel(const __grid_constant__ CUtensorMap map_raw, const __grid_constant__ C
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStagesTc; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&a_ready[s], kDqWarps);
-      mbar_init(&empty[s], 1);
+    for (int s = 0; s < kStagesRaw; ++s) {
+      mbar_init(&raw_full[s], 1);
+      mbar_init(&raw_empty[s], kDqWarps);
+    }
+    for (int s = 0; s < kStagesB; ++s) {
+      mbar_init(&b_full[s], 1);
+      mbar_init(&b_empty[s], 1);
+    }
+    for (int s = 0; s < kStagesA; ++s) {
+      mbar_init(&a_full[s], kDqWarps);
+      mbar_init(&a_empty[s], 1);
     }
     mbar_init(acc_full, 1);
     *abort_flag = 0;
@@ -225,20 +240,30 @@ tc_kernel(const __grid_constant__ CUtensorMap map_raw, const __grid_constant__ C
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    // ---------------- TMA producer ----------------
+    // ---------------- TMA producer: packed weights ----------------
     if (lane == 0) {
-      const uint32_t bytes = 2 * kRawTileBytes + (two_b ? 2 : 1) * kBHalfBytes;
       for (int ks = 0; ks < nk; ++ks) {
-        const int s = ks % kStagesTc;
-        const uint32_t ph = (ks / kStagesTc) & 1;
-        if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, P.err, kErrWaitTimeout)) break;
-        mbar_expect_tx(&full[s], bytes);
+        const int s = ks % kStagesRaw;
+        const uint32_t ph = (ks / kStagesRaw) & 1;
+        if (!mbar_wait(&raw_empty[s], ph ^ 1u, abort_flag, P.err, kErrWaitTimeout)) break;
+        mbar_expect_tx(&raw_full[s], 2 * kRawTileBytes);
         uint8_t* raw = smem + kOffRaw + s * 2 * kRawTileBytes;
+        tma_load_2d(raw, &map_raw, ks * (kBK / 2), wrow0, &raw_full[s]);
+        tma_load_2d(raw + kRawTileBytes, &map_raw, ks * (kBK / 2), wrow0 + P.acc1_offset, &raw_full[s]);
+      }
+    }
+  } else if (warp == 2 + kDqWarps) {
+    // ---------------- TMA producer: token tiles ----------------
+    if (lane == 0) {
+      const uint32_t bytes = (two_b ? 2 : 1) * kBHalfBytes;
+      for (int ks = 0; ks < nk; ++ks) {
+        const int s = ks % kStagesB;
+        const uint32_t ph = (ks / kStagesB) & 1;
+        if (!mbar_wait(&b_empty[s], ph ^ 1u, abort_flag, P.err, kErrWaitTimeout)) break;
+        mbar_expect_tx(&b_full[s], bytes);
         uint8_t* b = smem + kOffB + s * kBTileBytes;
-        tma_load_2d(raw, &map_raw, ks * (kBK / 2), wrow0, &full[s]);
-        tma_load_2d(raw + kRawTileBytes, &map_raw, ks * (kBK / 2), wrow0 + P.acc1_offset, &full[s]);
-        tma_load_2d(b, &map_b, ks * kBK, row0, &full[s]);
-        if (two_b) tma_load_2d(b + kBHalfBytes, &map_b, ks * kBK, row0 + 128, &full[s]);
+        tma_load_2d(b, &map_b, ks * kBK, row0, &b_full[s]);
+        if (two_b) tma_load_2d(b + kBHalfBytes, &map_b, ks * kBK, row0 + 128, &b_full[s]);
       }
     }
   } else if (warp == 1) {
@@ -246,22 +271,22 @@ tc_kernel(const __grid_constant__ CUtensorMap map_raw, const __grid_constant__ C
     if (lane == 0) {
       const uint32_t idesc = idesc_f16kind(kBM, n_mma, F16 ? 0u : 1u);
       for (int ks = 0; ks < nk; ++ks) {
-        const int s = ks % kStagesTc;
-        const uint32_t ph = (ks / kStagesTc) & 1;
-        if (!mbar_wait(&full[s], ph, abort_flag, P.err, kErrWaitTimeout) ||
-            !mbar_wait(&a_ready[s], ph, abort_flag, P.err, kErrWaitTimeout))
+        const int sa = ks % kStagesA, sb = ks % kStagesB;
+        if (!mbar_wait(&b_full[sb], (ks / kStagesB) & 1, abort_flag, P.err, kErrWaitTimeout) ||
+            !mbar_wait(&a_full[sa], (ks / kStagesA) & 1, abort_flag, P.err, kErrWaitTimeout))
           break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const uint32_t b_addr = smem_u32(smem + kOffB + s * kBTileBytes);
+        const uint32_t b_addr = smem_u32(smem + kOffB + sb * kBTileBytes);
 #pragma unroll
         for (int acc = 0; acc < 2; ++acc) {
-          const uint32_t a_addr = smem_u32(smem + kOffA + (s * 2 + acc) * kATileBytes);
+          const uint32_t a_addr = smem_u32(smem + kOffA + (sa * 2 + acc) * kATileBytes);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
             umma_bf16(tmem + acc * 256, desc_sw128(a_addr + kk * 32), desc_sw128(b_addr + kk * 32), idesc,
                       (ks > 0 || kk > 0) ? 1u : 0u);
         }
-        umma_commit(&empty[s]);
+        umma_commit(&b_empty[sb]);
+        umma_commit(&a_empty[sa]);
       }
       umma_commit(acc_full);
       // the accumulators must be final before TMEM can be freed, also on an abort
@@ -278,33 +303,64 @@ tc_kernel(const __grid_constant__ CUtensorMap map_raw, const __grid_constant__ C
     int s_ref = 0;
     if (F16) {
       uint32_t smax = 0;
-      for (int i = 0; i < kpr; i += 4) {
-        const uint32_t w4 = *reinterpret_cast<const uint32_t*>(srow + i);
-        smax = max(smax, max(max(w4 & 0xFFu, (w4 >> 8) & 0xFFu), max((w4 >> 16) & 0xFFu, w4 >> 24)));
+      auto max4 = [](uint32_t m, uint32_t w4) {
+        return max(m, max(max(w4 & 0xFFu, (w4 >> 8) & 0xFFu), max((w4 >> 16) & 0xFFu, w4 >> 24)));
+      };
+      if ((kpr & 15) == 0) {
+        for (int i = 0; i < kpr; i += 16) {
+          const uint4 q = *reinterpret_cast<const uint4*>(srow + i);
+          smax = max4(max4(max4(max4(smax, q.x), q.y), q.z), q.w);
+        }
+      } else {
+        for (int i = 0; i < kpr; i += 4) smax = max4(smax, *reinterpret_cast<const uint32_t*>(srow + i));
       }
       s_ref = (int)smax - 13;
       rowscale[acc * 128 + r] = pow2f(s_ref - 127);
     }
     const int sw = r & 7;
     const int c_first = (lane >> 2) & 1;    // conflict-free order of the two 16-byte halves
-    uint32_t sc_next = *reinterpret_cast<const uint16_t*>(srow);
+    // scale bytes: 16 at a time (8 K steps) when rows are 16-byte aligned, else 2 per step
+    const bool vec_scales = (kpr & 15) == 0;
+    uint4 sg_cur = make_uint4(0, 0, 0, 0), sg_next = make_uint4(0, 0, 0, 0);
+    uint32_t sc_next = 0;
+    if (vec_scales) {
+      sg_next = *reinterpret_cast<const uint4*>(srow);
+    } else {
+      sc_next = *reinterpret_cast<const uint16_t*>(srow);
+    }
     bool ok = true;
     for (int ks = 0; ks < nk; ++ks) {
-      const int s = ks % kStagesTc;
-      const uint32_t ph = (ks / kStagesTc) & 1;
-      const uint32_t sc = sc_next;
-      if (ks + 1 < nk) sc_next = *reinterpret_cast<const uint16_t*>(srow + 2 * (ks + 1));
-      if (!mbar_wait(&full[s], ph, abort_flag, P.err, kErrWaitTimeout)) {
+      const int s = ks % kStagesRaw, sa = ks % kStagesA;
+      uint32_t sc;
+      if (vec_scales) {
+        if ((ks & 7) == 0) {
+          sg_cur = sg_next;
+          if (ks + 8 < nk) sg_next = *reinterpret_cast<const uint4*>(srow + 2 * (ks + 8));
+        }
+        const uint32_t wsel = ((ks & 7) >> 1) == 0 ? sg_cur.x : ((ks & 7) >> 1) == 1 ? sg_cur.y
+                            : ((ks & 7) >> 1) == 2 ? sg_cur.z : sg_cur.w;
+        sc = (ks & 1) ? wsel >> 16 : wsel & 0xFFFFu;
+      } else {
+        sc = sc_next;
+        if (ks + 1 < nk) sc_next = *reinterpret_cast<const uint16_t*>(srow + 2 * (ks + 1));
+      }
+      if (!mbar_wait(&raw_full[s], (ks / kStagesRaw) & 1, abort_flag, P.err, kErrWaitTimeout)) {
         ok = false;
         break;
       }
       const uint8_t* raw = smem + kOffRaw + (s * 2 + acc) * kRawTileBytes + r * 32;
       const uint4 h0 = *reinterpret_cast<const uint4*>(raw + 16 * c_first);
       const uint4 h1 = *reinterpret_cast<const uint4*>(raw + 16 * (c_first ^ 1));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&raw_empty[s]);  // the packed bytes are in registers now
       const uint4 lo = c_first ? h1 : h0, hi = c_first ? h0 : h1;
       const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-      uint8_t* arow = smem + kOffA + (s * 2 + acc) * kATileBytes + (r >> 3) * 1024 + (r & 7) * 128;
-      const uint32_t s0 = sc & 0xFFu, s1 = sc >> 8;
+      if (!mbar_wait(&a_empty[sa], ((ks / kStagesA) & 1) ^ 1u, abort_flag, P.err, kErrWaitTimeout)) {
+        ok = false;
+        break;
+      }
+      uint8_t* arow = smem + kOffA + (sa * 2 + acc) * kATileBytes + (r >> 3) * 1024 + (r & 7) * 128;
+      const uint32_t s0 = sc & 0xFFu, s1 = (sc >> 8) & 0xFFu;
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         const uint32_t sb = c < 4 ? s0 : s1;
@@ -313,7 +369,7 @@ tc_kernel(const __grid_constant__ CUtensorMap map_raw, const __grid_constant__ C
       }
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
-      if (lane == 0) mbar_arrive(&a_ready[s]);
+      if (lane == 0) mbar_arrive(&a_full[sa]);
     }
     // the row scales written above must be visible to every epilogue warp
     asm volatile("bar.sync 1, %0;" ::"r"(kDqWarps * 32) : "memory");
