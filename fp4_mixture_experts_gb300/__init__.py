@@ -8,9 +8,9 @@ Importing the package does not need a GPU; calling a compute function
 without the built library raises.
 """
 from ._binding import (EXPORTED_SYMBOLS, FLAG_FORCE_GEMV, FLAG_FORCE_TC, Dims, MoeFp4Error, check, forward,
-                       forward_host, host_workspace_bytes, lib_path, load_library, route, status_string,
+                       forward_host, forward_noalloc, host_workspace_bytes, lib_path, load_library, route, status_string,
                        workspace_bytes)
 
 __all__ = ["EXPORTED_SYMBOLS", "FLAG_FORCE_GEMV", "FLAG_FORCE_TC", "Dims", "MoeFp4Error", "check", "forward",
-           "forward_host", "host_workspace_bytes", "lib_path", "load_library", "route", "status_string",
+           "forward_host", "forward_noalloc", "host_workspace_bytes", "lib_path", "load_library", "route", "status_string",
            "workspace_bytes"]

@@ -22,6 +22,7 @@ EXPORTED_SYMBOLS = (
     "moe_fp4_forward",
     "moe_fp4_forward_profiled",
     "moe_fp4_forward_host",
+    "moe_fp4_forward_noalloc",
     "moe_fp4_check",
     "moe_fp4_status_string",
 )
@@ -69,6 +70,8 @@ def load_library():
     lib.moe_fp4_forward_profiled.restype = ctypes.c_int
     lib.moe_fp4_forward_host.argtypes = [pd, P, P, P, P, P, P, P, ctypes.c_uint, P, ctypes.c_size_t, P]
     lib.moe_fp4_forward_host.restype = ctypes.c_int
+    lib.moe_fp4_forward_noalloc.argtypes = [pd, P, P, P, P, P, P, P, ctypes.c_uint, P]
+    lib.moe_fp4_forward_noalloc.restype = ctypes.c_int
     lib.moe_fp4_check.argtypes = [P, P]
     lib.moe_fp4_check.restype = ctypes.c_int
     lib.moe_fp4_status_string.argtypes = [ctypes.c_int]
@@ -209,6 +212,25 @@ def forward_host(x_bf16_host, router_logits_host, w13, w13_scale, w2, w2_scale, 
     if rc != 0:
         raise MoeFp4Error(rc, "moe_fp4_forward_host")
     return out_host
+
+
+def forward_noalloc(x_bf16, router_logits, w13, w13_scale, w2, w2_scale, k: int, out=None, flags: int = 0,
+                    stream=None):
+    """The whole layer with no workspace argument: the library's own fixed
+    device scratch is used (see moe_fp4_forward_noalloc in include/moe_fp4.h:
+    calls share it, so order them on one stream)."""
+    import torch
+    T, d = x_bf16.shape
+    E, twoI, _ = w13.shape
+    dims = _dims(T, d, twoI // 2, E, k)
+    if out is None:
+        out = torch.empty(T, d, dtype=torch.float32, device=x_bf16.device)
+    rc = load_library().moe_fp4_forward_noalloc(ctypes.byref(dims), _ptr(x_bf16), _ptr(router_logits), _ptr(w13),
+                                                _ptr(w13_scale), _ptr(w2), _ptr(w2_scale), _ptr(out), int(flags),
+                                                _stream(stream))
+    if rc != 0:
+        raise MoeFp4Error(rc, "moe_fp4_forward_noalloc")
+    return out
 
 
 def check(workspace, stream=None) -> None:

@@ -146,6 +146,29 @@ int moe_fp4_forward_host(const moe_fp4_dims* dims, const void* x_bf16_host,
                          unsigned flags, void* workspace, size_t workspace_bytes,
                          void* cuda_stream);
 
+/* The whole layer without any workspace argument, for callers that cannot
+ * allocate device memory: runtimes without an allocator, callers that must
+ * not call cudaMalloc inside a stream-ordered or captured region, plugins
+ * that are handed only input and output pointers.  (The paper has no
+ * counterpart; this is a deployment convenience.)
+ *
+ * Scratch: a fixed device array of MOE_FP4_NOALLOC_SCRATCH_BYTES inside this
+ * library, which every GPU that loads the library holds until the process
+ * exits.  Problems whose moe_fp4_workspace_bytes exceeds it are rejected with
+ * MOE_FP4_ERR_WORKSPACE before anything is enqueued (the decode shape T=32,
+ * d=4096, I=2048, E=256, k=8 needs about 7.4 MB).
+ * The first call on a device looks the array's device address up (with that
+ * device current); make that first call before any stream capture.
+ * All calls share the array and it keeps the last call's contents: calls
+ * that overlap on the GPU (other streams, other host threads) race and give
+ * wrong results; order them on one stream.  Otherwise the same arguments,
+ * checks and results as moe_fp4_forward, with no optional outputs. */
+#define MOE_FP4_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+int moe_fp4_forward_noalloc(const moe_fp4_dims* dims, const void* x_bf16, const float* router_logits,
+                            const uint8_t* w13, const uint8_t* w13_scale,
+                            const uint8_t* w2, const uint8_t* w2_scale, float* out,
+                            unsigned flags, void* cuda_stream);
+
 /* Synchronises the stream and reads the device error word of the workspace
  * (set by a kernel that met an index out of range, e.g. a corrupted expert
  * id); returns MOE_FP4_OK, MOE_FP4_ERR_DEVICE or MOE_FP4_ERR_CUDA, and clears
