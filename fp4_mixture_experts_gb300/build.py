@@ -29,8 +29,8 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
-def _compile(src: str, extra: list[str]) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+def _compile(src: str, extra: list[str], bdir: str) -> str:
+    obj = os.path.join(bdir, os.path.basename(src)[:-3] + ".o")
     cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
@@ -38,22 +38,25 @@ def _compile(src: str, extra: list[str]) -> str:
     return obj
 
 
-def build(verbose: bool = False, extra_flags: list[str] | None = None) -> str:
-    """Compile csrc/*.cu and link libmoe_fp4.so; returns the library path."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose: bool = False, extra_flags: list[str] | None = None, out: str | None = None,
+          build_dir: str | None = None) -> str:
+    """Compile csrc/*.cu and link libmoe_fp4.so (or `out`); returns the library path."""
+    lib_out = out or LIB
+    bdir = build_dir or BUILD
+    os.makedirs(bdir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     extra = list(extra_flags or [])
     with concurrent.futures.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra), srcs))
-    tmp = LIB + ".tmp"
+        objs = list(ex.map(lambda s: _compile(s, extra, bdir), srcs))
+    tmp = lib_out + ".tmp"
     cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-lcudart"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib_out)
     if verbose:
-        print(f"built {LIB}")
-    return LIB
+        print(f"built {lib_out}")
+    return lib_out
 
 
 if __name__ == "__main__":

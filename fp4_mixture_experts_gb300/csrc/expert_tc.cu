@@ -43,9 +43,18 @@ namespace {
 constexpr int kBM = 128;                 // weight rows per accumulator
 constexpr int kBK = 64;                  // K elements per stage
 constexpr int kBN = kTcTileN;            // token rows per tile (<= 256)
-constexpr int kStagesA = 2;              // dequantised weight tiles (dequant -> MMA)
-constexpr int kStagesB = 3;              // token tiles (TMA -> MMA)
-constexpr int kStagesRaw = 6;            // packed weight tiles (TMA -> dequant)
+#ifndef MOE_TC_STAGES_A
+#define MOE_TC_STAGES_A 2
+#endif
+#ifndef MOE_TC_STAGES_B
+#define MOE_TC_STAGES_B 3
+#endif
+#ifndef MOE_TC_STAGES_RAW
+#define MOE_TC_STAGES_RAW 6
+#endif
+constexpr int kStagesA = MOE_TC_STAGES_A;      // dequantised weight tiles (dequant -> MMA)
+constexpr int kStagesB = MOE_TC_STAGES_B;      // token tiles (TMA -> MMA)
+constexpr int kStagesRaw = MOE_TC_STAGES_RAW;  // packed weight tiles (TMA -> dequant)
 constexpr int kDqWarps = 8;
 constexpr int kTcThreads = (3 + kDqWarps) * 32;  // raw producer, MMA, 8 dequant, token producer
 constexpr uint32_t kTmemCols = 512;      // 2 accumulators x 256 columns
@@ -60,6 +69,7 @@ constexpr int kOffRaw = kOffB + kStagesB * kBTileBytes;        // [stage][acc]
 constexpr int kOffRowScale = kOffRaw + kStagesRaw * 2 * kRawTileBytes;
 constexpr int kOffBar = kOffRowScale + 2 * kBM * 4;
 constexpr int kSmemTc = kOffBar + 256 + 1024;                  // + barriers, slack for 1 KB alignment
+static_assert(kSmemTc <= 227 * 1024, "shared memory of the tensor-core kernel exceeds 227 KB");
 
 struct TcParams {
   const uint8_t* scales;   // E8M0 [rows][K/32]

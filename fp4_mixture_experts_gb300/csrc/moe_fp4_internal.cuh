@@ -15,7 +15,10 @@ namespace moe_fp4 {
 constexpr int kRouteTokensPerBlock = 32;   // tokens per routing block (8 warps x 4)
 constexpr int kRouteThreads = 256;
 constexpr int kGemvTokens = 8;             // token rows per streaming-GEMV chunk (the MMA N = 8)
-constexpr int kTcTileN = 256;              // max token rows per tensor-core tile (UMMA N)
+#ifndef MOE_TC_TILE_N
+#define MOE_TC_TILE_N 256
+#endif
+constexpr int kTcTileN = MOE_TC_TILE_N;    // max token rows per tensor-core tile (UMMA N, 128 or 256)
 
 // Device error word values (moe_fp4_check).
 constexpr int kErrBadExpertId = 1;
