@@ -11,17 +11,20 @@
 // Warp roles (352 threads), three decoupled rings per 64-wide K step:
 //   warp 0      TMA producer of the packed weight tiles (2 x 128 rows x 32
 //               bytes, 6-deep ring: the HBM stream)
-//   warp 10     TMA producer of the token tile (up to 256 rows, 128-byte
+//   warp 10     TMA producer of the token tile (up to 192 rows, 128-byte
 //               swizzle, 3-deep ring: mostly L2 hits, shared by the CTAs of
 //               one expert)
-//   warp 1      TMEM allocator (512 columns) and MMA issuer: 2 x 4
+//   warp 1      TMEM allocator (512 columns: two accumulators of up to 192
+//               columns and the A ring) and MMA issuer: 2 x 4
 //               tcgen05.mma.kind::f16 (M=128, N=tile, K=16) per K step, fp32
 //               accumulators in TMEM; tcgen05.commit frees the token and
 //               weight slots
-//   warps 2..9  dequantisers (2-deep ring of dequantised tiles): one thread per weight row; E2M1 pairs decoded by
+//   warps 2..9  dequantisers (2-deep ring of dequantised tiles, kept in TMEM so
+//               that the MMA reads its A operand from tensor memory and shared
+//               memory only carries the token tiles and the packed bytes): one thread per weight row; E2M1 pairs decoded by
 //               cvt.rn.f16x2.e2m1x2 and scaled exactly by a power of two
 //               (mul.f16x2 for W13, mul.bf16x2 after a bf16 re-encoding for
-//               W2), stored in the UMMA K-major 128-byte-swizzled layout; then
+//               W2), written to TMEM with tcgen05.st (lane = weight row); then
 //               the epilogue (tcgen05.ld, SwiGLU + bf16 rounding of h, or y)
 // Weights are dequantised exactly (an E2M1 value times a power of two has
 // 2 significant bits), so the MMA multiplies exact products and accumulates
@@ -42,7 +45,7 @@ namespace {
 
 constexpr int kBM = 128;                 // weight rows per accumulator
 constexpr int kBK = 64;                  // K elements per stage
-constexpr int kBN = kTcTileN;            // token rows per tile (<= 256)
+constexpr int kBN = kTcTileN;            // token rows per tile (<= 192: TMEM holds 2 accumulators + A)
 #ifndef MOE_TC_STAGES_A
 #define MOE_TC_STAGES_A 2
 #endif
@@ -57,14 +60,20 @@ constexpr int kStagesB = MOE_TC_STAGES_B;      // token tiles (TMA -> MMA)
 constexpr int kStagesRaw = MOE_TC_STAGES_RAW;  // packed weight tiles (TMA -> dequant)
 constexpr int kDqWarps = 8;
 constexpr int kTcThreads = (3 + kDqWarps) * 32;  // raw producer, MMA, 8 dequant, token producer
-constexpr uint32_t kTmemCols = 512;      // 2 accumulators x 256 columns
+// TMEM columns: accumulator 0 at [0, kBN), accumulator 1 at [kBN, 2 kBN),
+// dequantised weight tiles (A operands) at [2 kBN, ...): per (stage, acc) a
+// 128-lane x 32-column slot holding 64 K values of each row as f16/bf16 pairs.
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccCols = kBN;
+constexpr uint32_t kACol0 = 2 * kBN;
+constexpr uint32_t kASlotCols = kBK / 2;
+static_assert(kACol0 + kStagesA * 2 * kASlotCols <= kTmemCols, "TMEM columns exceeded");
 
-constexpr int kATileBytes = kBM * kBK * 2;        // 16 KB
-constexpr int kBHalfBytes = 128 * kBK * 2;        // 16 KB: 128 token rows
-constexpr int kBTileBytes = kBN * kBK * 2;        // 32 KB
+constexpr int kBBoxRows = 64;                     // token rows per TMA box
+constexpr int kBBoxBytes = kBBoxRows * kBK * 2;   // 8 KB
+constexpr int kBTileBytes = kBN * kBK * 2;        // token tile slot
 constexpr int kRawTileBytes = kBM * kBK / 2;      // 4 KB packed
-constexpr int kOffA = 0;                                       // [stage][acc]
-constexpr int kOffB = kOffA + kStagesA * 2 * kATileBytes;      // [stage]
+constexpr int kOffB = 0;                                       // [stage]
 constexpr int kOffRaw = kOffB + kStagesB * kBTileBytes;        // [stage][acc]
 constexpr int kOffRowScale = kOffRaw + kStagesRaw * 2 * kRawTileBytes;
 constexpr int kOffBar = kOffRowScale + 2 * kBM * 4;
@@ -112,6 +121,27 @@ __device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t a, uint64_t 
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem_d),
       "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]: the A operand is read from tensor memory
+__device__ __forceinline__ void umma_tmem_a(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+
+// this thread's TMEM lane, 32 consecutive 32-bit columns from taddr
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
       : "memory");
 }
 
@@ -217,7 +247,6 @@ tc_kernel(const __grid_constant__ CUtensorMap map_raw, const __grid_constant__ C
   const int4 tl = P.tiles[tile];
   const int row0 = tl.y, n = tl.z;
   const int n_mma = (n + 15) & ~15;
-  const bool two_b = n > 128;
   const int wrow0 = tl.x * P.rows_per_expert + mb * P.block_rows;
   const int nk = P.K / kBK;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -265,15 +294,14 @@ tc_kernel(const __grid_constant__ CUtensorMap map_raw, const __grid_constant__ C
   } else if (warp == 2 + kDqWarps) {
     // ---------------- TMA producer: token tiles ----------------
     if (lane == 0) {
-      const uint32_t bytes = (two_b ? 2 : 1) * kBHalfBytes;
+      const int boxes = (n_mma + kBBoxRows - 1) / kBBoxRows;
       for (int ks = 0; ks < nk; ++ks) {
         const int s = ks % kStagesB;
         const uint32_t ph = (ks / kStagesB) & 1;
         if (!mbar_wait(&b_empty[s], ph ^ 1u, abort_flag, P.err, kErrWaitTimeout)) break;
-        mbar_expect_tx(&b_full[s], bytes);
+        mbar_expect_tx(&b_full[s], boxes * kBBoxBytes);
         uint8_t* b = smem + kOffB + s * kBTileBytes;
-        tma_load_2d(b, &map_b, ks * kBK, row0, &b_full[s]);
-        if (two_b) tma_load_2d(b + kBHalfBytes, &map_b, ks * kBK, row0 + 128, &b_full[s]);
+        for (int i = 0; i < boxes; ++i) tma_load_2d(b + i * kBBoxBytes, &map_b, ks * kBK, row0 + i * kBBoxRows, &b_full[s]);
       }
     }
   } else if (warp == 1) {
@@ -289,11 +317,11 @@ tc_kernel(const __grid_constant__ CUtensorMap map_raw, const __grid_constant__ C
         const uint32_t b_addr = smem_u32(smem + kOffB + sb * kBTileBytes);
 #pragma unroll
         for (int acc = 0; acc < 2; ++acc) {
-          const uint32_t a_addr = smem_u32(smem + kOffA + (sa * 2 + acc) * kATileBytes);
+          const uint32_t a_tmem = tmem + kACol0 + (sa * 2 + acc) * kASlotCols;
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
-            umma_bf16(tmem + acc * 256, desc_sw128(a_addr + kk * 32), desc_sw128(b_addr + kk * 32), idesc,
-                      (ks > 0 || kk > 0) ? 1u : 0u);
+            umma_tmem_a(tmem + acc * kAccCols, a_tmem + kk * 8, desc_sw128(b_addr + kk * 32), idesc,
+                        (ks > 0 || kk > 0) ? 1u : 0u);
         }
         umma_commit(&b_empty[sb]);
         umma_commit(&a_empty[sa]);
@@ -306,7 +334,8 @@ tc_kernel(const __grid_constant__ CUtensorMap map_raw, const __grid_constant__ C
     // ---------------- dequantisers (one weight row each), then the epilogue ----------------
     const int dq = warp - 2;
     const int acc = dq >> 2;                 // 0: first block (gate), 1: second block (up)
-    const int r = (dq & 3) * 32 + lane;      // row within the 128-row block
+    const int q = warp & 3;                  // TMEM lane quadrant this warp may access
+    const int r = q * 32 + lane;             // row within the 128-row block = TMEM lane
     const int wrow = wrow0 + acc * P.acc1_offset + r;
     const int kpr = P.K / 32;                // scale bytes per row
     const uint8_t* srow = P.scales + (size_t)wrow * kpr;
@@ -327,7 +356,6 @@ tc_kernel(const __grid_constant__ CUtensorMap map_raw, const __grid_constant__ C
       s_ref = (int)smax - 13;
       rowscale[acc * 128 + r] = pow2f(s_ref - 127);
     }
-    const int sw = r & 7;
     const int c_first = (lane >> 2) & 1;    // conflict-free order of the two 16-byte halves
     // scale bytes: 16 at a time (8 K steps) when rows are 16-byte aligned, else 2 per step
     const bool vec_scales = (kpr & 15) == 0;
@@ -369,15 +397,20 @@ tc_kernel(const __grid_constant__ CUtensorMap map_raw, const __grid_constant__ C
         ok = false;
         break;
       }
-      uint8_t* arow = smem + kOffA + (sa * 2 + acc) * kATileBytes + (r >> 3) * 1024 + (r & 7) * 128;
       const uint32_t s0 = sc & 0xFFu, s1 = (sc >> 8) & 0xFFu;
+      uint32_t av[32];  // column j = K elements (2j, 2j+1) of this row
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         const uint32_t sb = c < 4 ? s0 : s1;
         const uint4 v = F16 ? dequant8_f16(w[c], (int)sb - s_ref) : dequant8(w[c], sb);
-        *reinterpret_cast<uint4*>(arow + ((c ^ sw) << 4)) = v;
+        av[4 * c + 0] = v.x;
+        av[4 * c + 1] = v.y;
+        av[4 * c + 2] = v.z;
+        av[4 * c + 3] = v.w;
       }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      tmem_st32(tmem + ((uint32_t)(q * 32) << 16) + kACol0 + (sa * 2 + acc) * kASlotCols, av);
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       __syncwarp();
       if (lane == 0) mbar_arrive(&a_full[sa]);
     }
@@ -385,14 +418,13 @@ tc_kernel(const __grid_constant__ CUtensorMap map_raw, const __grid_constant__ C
     asm volatile("bar.sync 1, %0;" ::"r"(kDqWarps * 32) : "memory");
     if (ok && mbar_wait(acc_full, 0, abort_flag, P.err, kErrWaitTimeout)) {
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const int q = warp & 3;               // TMEM lane quadrant this warp may read
-      const int rr = q * 32 + lane;         // weight row of this thread's TMEM lane
-      const int c_begin = (dq >> 2) * 128;  // this warp's half of the columns
+      const int rr = r;                          // weight row of this thread's TMEM lane
+      const int c_begin = (dq >> 2) * (kBN / 2);  // this warp's half of the columns
       const float rs0 = F16 ? rowscale[rr] : 1.f, rs1 = F16 ? rowscale[128 + rr] : 1.f;
-      for (int c0 = c_begin; c0 < c_begin + 128 && c0 < n_mma; c0 += 32) {
+      for (int c0 = c_begin; c0 < c_begin + kBN / 2 && c0 < n_mma; c0 += 32) {
         float a0[32], a1[32];
         tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + c0, a0);
-        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + 256 + c0, a1);
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + kAccCols + c0, a1);
         if (F16) {
           const float xs_l = c0 + lane < n ? P.x_scale[row0 + c0 + lane] : 0.f;
           const int i = mb * kBM + rr;
@@ -446,7 +478,7 @@ cudaError_t launch_tc_w13(const moe_fp4_dims& d, const uint8_t* w13, const uint8
   CUtensorMap raw, b;
   if (!make_map_2d(&raw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w13, d.d / 2, (uint64_t)d.E * 2 * d.I, d.d / 2, kBK / 2, kBM,
                    CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !make_map_2d(&b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws.x_perm, d.d, S, (uint64_t)d.d * 2, kBK, 128,
+      !make_map_2d(&b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws.x_perm, d.d, S, (uint64_t)d.d * 2, kBK, kBBoxRows,
                    CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   TcParams P{};
@@ -472,7 +504,7 @@ cudaError_t launch_tc_w2(const moe_fp4_dims& d, const uint8_t* w2, const uint8_t
   CUtensorMap raw, b;
   if (!make_map_2d(&raw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w2, d.I / 2, (uint64_t)d.E * d.d, d.I / 2, kBK / 2, kBM,
                    CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !make_map_2d(&b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ws.h, d.I, S, (uint64_t)d.I * 2, kBK, 128,
+      !make_map_2d(&b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ws.h, d.I, S, (uint64_t)d.I * 2, kBK, kBBoxRows,
                    CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   TcParams P{};

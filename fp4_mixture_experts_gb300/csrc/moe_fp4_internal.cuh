@@ -16,9 +16,9 @@ constexpr int kRouteTokensPerBlock = 32;   // tokens per routing block (8 warps 
 constexpr int kRouteThreads = 256;
 constexpr int kGemvTokens = 8;             // token rows per streaming-GEMV chunk (the MMA N = 8)
 #ifndef MOE_TC_TILE_N
-#define MOE_TC_TILE_N 256
+#define MOE_TC_TILE_N 192
 #endif
-constexpr int kTcTileN = MOE_TC_TILE_N;    // max token rows per tensor-core tile (UMMA N, 128 or 256)
+constexpr int kTcTileN = MOE_TC_TILE_N;    // max token rows per tensor-core tile (UMMA N, a multiple of 64)
 
 // Device error word values (moe_fp4_check).
 constexpr int kErrBadExpertId = 1;
