@@ -34,6 +34,7 @@ sys.path.insert(0, ROOT)
 from moe_inputs import CONFIGS, make_config  # noqa: E402
 
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 STAGES = ["route", "gather", "w13_swiglu", "w2", "combine"]
 
@@ -45,6 +46,21 @@ def peaks():
         return p, "measured"
     except (OSError, ValueError):
         return dict(FALLBACK_PEAKS), "fallback"
+
+
+def ncu_traffic(key):
+    """DRAM bytes per launch (read + write) of one kernel on one workload, from the
+    committed ncu capture, or None when the kernel's source changed since then."""
+    import hashlib
+    try:
+        with open(TRAFFIC_FILE) as f:
+            rec = json.load(f)[key]
+        with open(os.path.join(ROOT, rec["source"]), "rb") as f:
+            if hashlib.sha1(f.read()).hexdigest() != rec["source_sha1"]:
+                return None
+        return int(rec["dram_read_bytes"]) + int(rec["dram_write_bytes"])
+    except (OSError, ValueError, KeyError):
+        return None
 
 
 def expert_bytes(d, I):
@@ -227,7 +243,8 @@ def roofline_decode(res, pk, src):
     ach = w13_bytes / (st["w13_swiglu"] * 1e-3) / 1e9
     step_bytes = w13_bytes + w2_bytes
     return {"bound": "hbm", "kernel": "w13_swiglu", "achieved": round(ach, 1), "peak": pk["hbm_gbs"],
-            "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4), "traffic": None,
+            "unit": "GB/s", "frac": round(ach / pk["hbm_gbs"], 4),
+            "traffic": ncu_traffic("stream_kernel<W13>@decode"),
             "peak_source": f"{src} hbm_gbs (copy, burst)",
             "bytes_per_launch": w13_bytes,
             "step_bytes": step_bytes,
@@ -242,7 +259,8 @@ def roofline_prefill(res, pk, src):
     peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
     step_flops = 6.0 * L.T * L.k * L.d * L.I
     return {"bound": "tensor", "kernel": "w13_swiglu", "achieved": round(ach, 1), "peak": peak,
-            "unit": "TFLOP/s", "frac": round(ach / peak, 4), "traffic": None,
+            "unit": "TFLOP/s", "frac": round(ach / peak, 4),
+            "traffic": ncu_traffic("tc_kernel<W13>@prefill"),
             "peak_source": f"{src} bf16_tflops_sustained (cuBLAS bf16 loop)",
             "flops_per_launch": flops_w13,
             "step_frac": round(step_flops / (res["ms_total"] / res["steps"] * 1e-3) / 1e12 / peak, 4)}

@@ -8,20 +8,20 @@
 // token tile: gate and up rows of W13 (so SwiGLU fuses into the epilogue), or
 // two adjacent 128-row blocks of W2.
 //
-// Warp roles (352 threads), three decoupled rings per 64-wide K step:
-//   warp 0      TMA producer of the packed weight tiles (2 x 128 rows x 32
-//               bytes, 6-deep ring: the HBM stream)
-//   warp 10     TMA producer of the token tile (up to 192 rows, 128-byte
+// Warp roles (320 threads), per 64-wide K step:
+//   warp 9      TMA producer of the token tile (up to 192 rows, 128-byte
 //               swizzle, 3-deep ring: mostly L2 hits, shared by the CTAs of
 //               one expert)
-//   warp 1      TMEM allocator (512 columns: two accumulators of up to 192
+//   warp 0      TMEM allocator (512 columns: two accumulators of up to 192
 //               columns and the A ring) and MMA issuer: 2 x 4
 //               tcgen05.mma.kind::f16 (M=128, N=tile, K=16) per K step, fp32
 //               accumulators in TMEM; tcgen05.commit frees the token and
 //               weight slots
-//   warps 2..9  dequantisers (2-deep ring of dequantised tiles, kept in TMEM so
+//   warps 1..8  dequantisers (2-deep ring of dequantised tiles, kept in TMEM so
 //               that the MMA reads its A operand from tensor memory and shared
-//               memory only carries the token tiles and the packed bytes): one thread per weight row; E2M1 pairs decoded by
+//               memory only carries the token tiles); each thread streams its
+//               row's 32 packed bytes per K step (one 32-byte sector) straight
+//               into registers, 4 steps ahead: one thread per weight row; E2M1 pairs decoded by
 //               cvt.rn.f16x2.e2m1x2 and scaled exactly by a power of two
 //               (mul.f16x2 for W13, mul.bf16x2 after a bf16 re-encoding for
 //               W2), written to TMEM with tcgen05.st (lane = weight row); then
@@ -50,16 +50,16 @@ constexpr int kBN = kTcTileN;            // token rows per tile (<= 192: TMEM ho
 #define MOE_TC_STAGES_A 2
 #endif
 #ifndef MOE_TC_STAGES_B
-#define MOE_TC_STAGES_B 3
-#endif
-#ifndef MOE_TC_STAGES_RAW
-#define MOE_TC_STAGES_RAW 6
+#define MOE_TC_STAGES_B 4
 #endif
 constexpr int kStagesA = MOE_TC_STAGES_A;      // dequantised weight tiles (dequant -> MMA)
 constexpr int kStagesB = MOE_TC_STAGES_B;      // token tiles (TMA -> MMA)
-constexpr int kStagesRaw = MOE_TC_STAGES_RAW;  // packed weight tiles (TMA -> dequant)
+constexpr int kPrefetch = 4;                  // K steps of packed weights each dequantiser keeps in flight
 constexpr int kDqWarps = 8;
-constexpr int kTcThreads = (3 + kDqWarps) * 32;  // raw producer, MMA, 8 dequant, token producer
+constexpr int kMmaWarp = 0;                      // TMEM allocator and MMA issuer
+constexpr int kFirstDqWarp = 1;                  // dequantisers 1..8, then the epilogue
+constexpr int kBWarp = kFirstDqWarp + kDqWarps;  // token-tile TMA producer
+constexpr int kTcThreads = (kBWarp + 1) * 32;
 // TMEM columns: accumulator 0 at [0, kBN), accumulator 1 at [kBN, 2 kBN),
 // dequantised weight tiles (A operands) at [2 kBN, ...): per (stage, acc) a
 // 128-lane x 32-column slot holding 64 K values of each row as f16/bf16 pairs.
@@ -72,15 +72,14 @@ static_assert(kACol0 + kStagesA * 2 * kASlotCols <= kTmemCols, "TMEM columns exc
 constexpr int kBBoxRows = 64;                     // token rows per TMA box
 constexpr int kBBoxBytes = kBBoxRows * kBK * 2;   // 8 KB
 constexpr int kBTileBytes = kBN * kBK * 2;        // token tile slot
-constexpr int kRawTileBytes = kBM * kBK / 2;      // 4 KB packed
 constexpr int kOffB = 0;                                       // [stage]
-constexpr int kOffRaw = kOffB + kStagesB * kBTileBytes;        // [stage][acc]
-constexpr int kOffRowScale = kOffRaw + kStagesRaw * 2 * kRawTileBytes;
+constexpr int kOffRowScale = kOffB + kStagesB * kBTileBytes;
 constexpr int kOffBar = kOffRowScale + 2 * kBM * 4;
 constexpr int kSmemTc = kOffBar + 256 + 1024;                  // + barriers, slack for 1 KB alignment
 static_assert(kSmemTc <= 227 * 1024, "shared memory of the tensor-core kernel exceeds 227 KB");
 
 struct TcParams {
+  const uint8_t* w;        // packed E2M1 weights [rows][K/2]
   const uint8_t* scales;   // E8M0 [rows][K/32]
   const int4* tiles;       // (expert, first sorted row, rows, 0)
   const int32_t* counts;   // counts[2] = number of tiles
@@ -197,6 +196,15 @@ __device__ __forceinline__ uint4 dequant8(uint32_t packed, uint32_t s) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// 16-byte streaming load: read once, no L1 allocation, evict-first in L2
+__device__ __forceinline__ uint4 ldg_stream(const uint8_t* p, uint64_t pol) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p), "l"(pol));
+  return r;
+}
+
 __device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
@@ -228,13 +236,11 @@ __device__ __forceinline__ uint4 dequant8_f16(uint32_t packed, int e) {
 // (weights exactly 2^(s-127) * code, h as written), epilogue writes fp32 y.
 template <bool F16>
 __global__ void __launch_bounds__(kTcThreads, 1)
-tc_kernel(const __grid_constant__ CUtensorMap map_raw, const __grid_constant__ CUtensorMap map_b, const TcParams P) {
+tc_kernel(const __grid_constant__ CUtensorMap map_b, const TcParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float* rowscale = reinterpret_cast<float*>(smem + kOffRowScale);  // [2][128]
-  uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint64_t* raw_empty = raw_full + kStagesRaw;
-  uint64_t* b_full = raw_empty + kStagesRaw;
+  uint64_t* b_full = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint64_t* b_empty = b_full + kStagesB;
   uint64_t* a_full = b_empty + kStagesB;
   uint64_t* a_empty = a_full + kStagesA;
@@ -252,10 +258,6 @@ tc_kernel(const __grid_constant__ CUtensorMap map_raw, const __grid_constant__ C
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStagesRaw; ++s) {
-      mbar_init(&raw_full[s], 1);
-      mbar_init(&raw_empty[s], kDqWarps);
-    }
     for (int s = 0; s < kStagesB; ++s) {
       mbar_init(&b_full[s], 1);
       mbar_init(&b_empty[s], 1);
@@ -268,7 +270,7 @@ tc_kernel(const __grid_constant__ CUtensorMap map_raw, const __grid_constant__ C
     *abort_flag = 0;
     mbar_fence_init();
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                  "r"(kTmemCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
@@ -278,20 +280,7 @@ tc_kernel(const __grid_constant__ CUtensorMap map_raw, const __grid_constant__ C
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    // ---------------- TMA producer: packed weights ----------------
-    if (lane == 0) {
-      for (int ks = 0; ks < nk; ++ks) {
-        const int s = ks % kStagesRaw;
-        const uint32_t ph = (ks / kStagesRaw) & 1;
-        if (!mbar_wait(&raw_empty[s], ph ^ 1u, abort_flag, P.err, kErrWaitTimeout)) break;
-        mbar_expect_tx(&raw_full[s], 2 * kRawTileBytes);
-        uint8_t* raw = smem + kOffRaw + s * 2 * kRawTileBytes;
-        tma_load_2d(raw, &map_raw, ks * (kBK / 2), wrow0, &raw_full[s]);
-        tma_load_2d(raw + kRawTileBytes, &map_raw, ks * (kBK / 2), wrow0 + P.acc1_offset, &raw_full[s]);
-      }
-    }
-  } else if (warp == 2 + kDqWarps) {
+  if (warp == kBWarp) {
     // ---------------- TMA producer: token tiles ----------------
     if (lane == 0) {
       const int boxes = (n_mma + kBBoxRows - 1) / kBBoxRows;
@@ -304,7 +293,7 @@ tc_kernel(const __grid_constant__ CUtensorMap map_raw, const __grid_constant__ C
         for (int i = 0; i < boxes; ++i) tma_load_2d(b + i * kBBoxBytes, &map_b, ks * kBK, row0 + i * kBBoxRows, &b_full[s]);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       const uint32_t idesc = idesc_f16kind(kBM, n_mma, F16 ? 0u : 1u);
@@ -332,31 +321,45 @@ tc_kernel(const __grid_constant__ CUtensorMap map_raw, const __grid_constant__ C
     }
   } else {
     // ---------------- dequantisers (one weight row each), then the epilogue ----------------
-    const int dq = warp - 2;
+    const int dq = warp - kFirstDqWarp;
     const int acc = dq >> 2;                 // 0: first block (gate), 1: second block (up)
     const int q = warp & 3;                  // TMEM lane quadrant this warp may access
     const int r = q * 32 + lane;             // row within the 128-row block = TMEM lane
     const int wrow = wrow0 + acc * P.acc1_offset + r;
     const int kpr = P.K / 32;                // scale bytes per row
     const uint8_t* srow = P.scales + (size_t)wrow * kpr;
+    // packed bytes of this row: 32 per K step, one full 32-byte sector, read
+    // straight into registers kPrefetch steps ahead (no shared-memory staging)
+    const uint8_t* wrow_p = P.w + (size_t)wrow * (P.K / 2);
+    const uint64_t pol = l2_evict_first_policy();
+    uint4 pfl[kPrefetch], pfh[kPrefetch];
+#pragma unroll
+    for (int j = 0; j < kPrefetch; ++j) {
+      if (j < nk) {
+        pfl[j] = ldg_stream(wrow_p + 32 * j, pol);
+        pfh[j] = ldg_stream(wrow_p + 32 * j + 16, pol);
+      }
+    }
     int s_ref = 0;
     if (F16) {
       uint32_t smax = 0;
       auto max4 = [](uint32_t m, uint32_t w4) {
         return max(m, max(max(w4 & 0xFFu, (w4 >> 8) & 0xFFu), max((w4 >> 16) & 0xFFu, w4 >> 24)));
       };
-      if ((kpr & 15) == 0) {
-        for (int i = 0; i < kpr; i += 16) {
-          const uint4 q = *reinterpret_cast<const uint4*>(srow + i);
-          smax = max4(max4(max4(max4(smax, q.x), q.y), q.z), q.w);
-        }
+      if ((kpr & 15) == 0 && kpr <= 256) {
+        uint4 sv[16];  // all loads in flight at once
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (16 * i < kpr) sv[i] = *reinterpret_cast<const uint4*>(srow + 16 * i);
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (16 * i < kpr) smax = max4(max4(max4(max4(smax, sv[i].x), sv[i].y), sv[i].z), sv[i].w);
       } else {
         for (int i = 0; i < kpr; i += 4) smax = max4(smax, *reinterpret_cast<const uint32_t*>(srow + i));
       }
       s_ref = (int)smax - 13;
       rowscale[acc * 128 + r] = pow2f(s_ref - 127);
     }
-    const int c_first = (lane >> 2) & 1;    // conflict-free order of the two 16-byte halves
     // scale bytes: 16 at a time (8 K steps) when rows are 16-byte aligned, else 2 per step
     const bool vec_scales = (kpr & 15) == 0;
     uint4 sg_cur = make_uint4(0, 0, 0, 0), sg_next = make_uint4(0, 0, 0, 0);
@@ -367,66 +370,79 @@ tc_kernel(const __grid_constant__ CUtensorMap map_raw, const __grid_constant__ C
       sc_next = *reinterpret_cast<const uint16_t*>(srow);
     }
     bool ok = true;
-    for (int ks = 0; ks < nk; ++ks) {
-      const int s = ks % kStagesRaw, sa = ks % kStagesA;
-      uint32_t sc;
-      if (vec_scales) {
-        if ((ks & 7) == 0) {
-          sg_cur = sg_next;
-          if (ks + 8 < nk) sg_next = *reinterpret_cast<const uint4*>(srow + 2 * (ks + 8));
-        }
-        const uint32_t wsel = ((ks & 7) >> 1) == 0 ? sg_cur.x : ((ks & 7) >> 1) == 1 ? sg_cur.y
-                            : ((ks & 7) >> 1) == 2 ? sg_cur.z : sg_cur.w;
-        sc = (ks & 1) ? wsel >> 16 : wsel & 0xFFFFu;
-      } else {
-        sc = sc_next;
-        if (ks + 1 < nk) sc_next = *reinterpret_cast<const uint16_t*>(srow + 2 * (ks + 1));
-      }
-      if (!mbar_wait(&raw_full[s], (ks / kStagesRaw) & 1, abort_flag, P.err, kErrWaitTimeout)) {
-        ok = false;
-        break;
-      }
-      const uint8_t* raw = smem + kOffRaw + (s * 2 + acc) * kRawTileBytes + r * 32;
-      const uint4 h0 = *reinterpret_cast<const uint4*>(raw + 16 * c_first);
-      const uint4 h1 = *reinterpret_cast<const uint4*>(raw + 16 * (c_first ^ 1));
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&raw_empty[s]);  // the packed bytes are in registers now
-      const uint4 lo = c_first ? h1 : h0, hi = c_first ? h0 : h1;
-      const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-      if (!mbar_wait(&a_empty[sa], ((ks / kStagesA) & 1) ^ 1u, abort_flag, P.err, kErrWaitTimeout)) {
-        ok = false;
-        break;
-      }
-      const uint32_t s0 = sc & 0xFFu, s1 = (sc >> 8) & 0xFFu;
-      uint32_t av[32];  // column j = K elements (2j, 2j+1) of this row
+    for (int ks0 = 0; ks0 < nk && ok; ks0 += kPrefetch) {
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        const uint32_t sb = c < 4 ? s0 : s1;
-        const uint4 v = F16 ? dequant8_f16(w[c], (int)sb - s_ref) : dequant8(w[c], sb);
-        av[4 * c + 0] = v.x;
-        av[4 * c + 1] = v.y;
-        av[4 * c + 2] = v.z;
-        av[4 * c + 3] = v.w;
+      for (int j = 0; j < kPrefetch; ++j) {
+        const int ks = ks0 + j;
+        if (ks < nk && ok) {
+          const int sa = ks % kStagesA;
+          const uint4 lo = pfl[j], hi = pfh[j];
+          if (ks + kPrefetch < nk) {
+            pfl[j] = ldg_stream(wrow_p + 32 * (ks + kPrefetch), pol);
+            pfh[j] = ldg_stream(wrow_p + 32 * (ks + kPrefetch) + 16, pol);
+          }
+          uint32_t sc;
+          if (vec_scales) {
+            if ((ks & 7) == 0) {
+              sg_cur = sg_next;
+              if (ks + 8 < nk) sg_next = *reinterpret_cast<const uint4*>(srow + 2 * (ks + 8));
+            }
+            const uint32_t wsel = ((ks & 7) >> 1) == 0 ? sg_cur.x : ((ks & 7) >> 1) == 1 ? sg_cur.y
+                                : ((ks & 7) >> 1) == 2 ? sg_cur.z : sg_cur.w;
+            sc = (ks & 1) ? wsel >> 16 : wsel & 0xFFFFu;
+          } else {
+            sc = sc_next;
+            if (ks + 1 < nk) sc_next = *reinterpret_cast<const uint16_t*>(srow + 2 * (ks + 1));
+          }
+          const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+          if (!mbar_wait(&a_empty[sa], ((ks / kStagesA) & 1) ^ 1u, abort_flag, P.err, kErrWaitTimeout)) {
+            ok = false;
+          } else {
+            const uint32_t s0 = sc & 0xFFu, s1 = (sc >> 8) & 0xFFu;
+            uint32_t av[32];  // column j = K elements (2j, 2j+1) of this row
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const uint32_t sb = c < 4 ? s0 : s1;
+              const uint4 v = F16 ? dequant8_f16(w[c], (int)sb - s_ref) : dequant8(w[c], sb);
+              av[4 * c + 0] = v.x;
+              av[4 * c + 1] = v.y;
+              av[4 * c + 2] = v.z;
+              av[4 * c + 3] = v.w;
+            }
+            tmem_st32(tmem + ((uint32_t)(q * 32) << 16) + kACol0 + (sa * 2 + acc) * kASlotCols, av);
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&a_full[sa]);
+          }
+        }
       }
-      tmem_st32(tmem + ((uint32_t)(q * 32) << 16) + kACol0 + (sa * 2 + acc) * kASlotCols, av);
-      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&a_full[sa]);
+    }
+    // epilogue column scales, fetched before the accumulators are ready
+    const int c_begin = (dq >> 2) * (kBN / 2);  // this warp's half of the columns
+    float xs_pre[kBN / 64] = {};
+    if (F16) {
+#pragma unroll
+      for (int i = 0; i < kBN / 64; ++i) {
+        const int col = c_begin + 32 * i + lane;
+        if (col < n) xs_pre[i] = P.x_scale[row0 + col];
+      }
     }
     // the row scales written above must be visible to every epilogue warp
     asm volatile("bar.sync 1, %0;" ::"r"(kDqWarps * 32) : "memory");
     if (ok && mbar_wait(acc_full, 0, abort_flag, P.err, kErrWaitTimeout)) {
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       const int rr = r;                          // weight row of this thread's TMEM lane
-      const int c_begin = (dq >> 2) * (kBN / 2);  // this warp's half of the columns
       const float rs0 = F16 ? rowscale[rr] : 1.f, rs1 = F16 ? rowscale[128 + rr] : 1.f;
-      for (int c0 = c_begin; c0 < c_begin + kBN / 2 && c0 < n_mma; c0 += 32) {
+#pragma unroll
+      for (int ci = 0; ci < kBN / 64; ++ci) {
+        const int c0 = c_begin + 32 * ci;
+        if (c0 >= n_mma) break;
         float a0[32], a1[32];
         tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + c0, a0);
         tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + kAccCols + c0, a1);
         if (F16) {
-          const float xs_l = c0 + lane < n ? P.x_scale[row0 + c0 + lane] : 0.f;
+          const float xs_l = xs_pre[ci];
           const int i = mb * kBM + rr;
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
@@ -451,14 +467,14 @@ tc_kernel(const __grid_constant__ CUtensorMap map_raw, const __grid_constant__ C
   }
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
   }
 }
 
 template <bool F16>
-cudaError_t launch_tc(const CUtensorMap& raw, const CUtensorMap& b, const TcParams& P, int max_tiles, cudaStream_t st) {
+cudaError_t launch_tc(const CUtensorMap& b, const TcParams& P, int max_tiles, cudaStream_t st) {
   static bool configured = false;
   if (!configured) {
     cudaFuncSetAttribute(tc_kernel<F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTc);
@@ -466,7 +482,7 @@ cudaError_t launch_tc(const CUtensorMap& raw, const CUtensorMap& b, const TcPara
   }
   const long long grid = (long long)max_tiles * P.mblocks;
   if (grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-  tc_kernel<F16><<<(unsigned)grid, kTcThreads, kSmemTc, st>>>(raw, b, P);
+  tc_kernel<F16><<<(unsigned)grid, kTcThreads, kSmemTc, st>>>(b, P);
   return cudaGetLastError();
 }
 
@@ -475,13 +491,12 @@ cudaError_t launch_tc(const CUtensorMap& raw, const CUtensorMap& b, const TcPara
 cudaError_t launch_tc_w13(const moe_fp4_dims& d, const uint8_t* w13, const uint8_t* w13s, const Workspace& ws,
                           cudaStream_t st) {
   const size_t S = (size_t)d.T * d.k;
-  CUtensorMap raw, b;
-  if (!make_map_2d(&raw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w13, d.d / 2, (uint64_t)d.E * 2 * d.I, d.d / 2, kBK / 2, kBM,
-                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !make_map_2d(&b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws.x_perm, d.d, S, (uint64_t)d.d * 2, kBK, kBBoxRows,
+  CUtensorMap b;
+  if (!make_map_2d(&b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws.x_perm, d.d, S, (uint64_t)d.d * 2, kBK, kBBoxRows,
                    CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   TcParams P{};
+  P.w = w13;
   P.scales = w13s;
   P.tiles = ws.tc_tiles;
   P.counts = ws.counts;
@@ -495,19 +510,18 @@ cudaError_t launch_tc_w13(const moe_fp4_dims& d, const uint8_t* w13, const uint8
   P.acc1_offset = d.I;
   P.I = d.I;
   P.d = d.d;
-  return launch_tc<true>(raw, b, P, ws.max_tc_tiles, st);
+  return launch_tc<true>(b, P, ws.max_tc_tiles, st);
 }
 
 cudaError_t launch_tc_w2(const moe_fp4_dims& d, const uint8_t* w2, const uint8_t* w2s, const Workspace& ws,
                          cudaStream_t st) {
   const size_t S = (size_t)d.T * d.k;
-  CUtensorMap raw, b;
-  if (!make_map_2d(&raw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w2, d.I / 2, (uint64_t)d.E * d.d, d.I / 2, kBK / 2, kBM,
-                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      !make_map_2d(&b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ws.h, d.I, S, (uint64_t)d.I * 2, kBK, kBBoxRows,
+  CUtensorMap b;
+  if (!make_map_2d(&b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ws.h, d.I, S, (uint64_t)d.I * 2, kBK, kBBoxRows,
                    CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   TcParams P{};
+  P.w = w2;
   P.scales = w2s;
   P.tiles = ws.tc_tiles;
   P.counts = ws.counts;
@@ -520,7 +534,7 @@ cudaError_t launch_tc_w2(const moe_fp4_dims& d, const uint8_t* w2, const uint8_t
   P.acc1_offset = kBM;
   P.I = d.I;
   P.d = d.d;
-  return launch_tc<false>(raw, b, P, ws.max_tc_tiles, st);
+  return launch_tc<false>(b, P, ws.max_tc_tiles, st);
 }
 
 }  // namespace moe_fp4
