@@ -54,7 +54,10 @@ constexpr int kBN = kTcTileN;            // token rows per tile (<= 192: TMEM ho
 #endif
 constexpr int kStagesA = MOE_TC_STAGES_A;      // dequantised weight tiles (dequant -> MMA)
 constexpr int kStagesB = MOE_TC_STAGES_B;      // token tiles (TMA -> MMA)
-constexpr int kPrefetch = 4;                  // K steps of packed weights each dequantiser keeps in flight
+#ifndef MOE_TC_PREFETCH
+#define MOE_TC_PREFETCH 4
+#endif
+constexpr int kPrefetch = MOE_TC_PREFETCH;    // K steps of packed weights each dequantiser keeps in flight
 constexpr int kDqWarps = 8;
 constexpr int kMmaWarp = 0;                      // TMEM allocator and MMA issuer
 constexpr int kFirstDqWarp = 1;                  // dequantisers 1..8, then the epilogue
@@ -418,13 +421,15 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const TcParams P) {
         }
       }
     }
-    // epilogue column scales, fetched before the accumulators are ready
-    const int c_begin = (dq >> 2) * (kBN / 2);  // this warp's half of the columns
-    float xs_pre[kBN / 64] = {};
+    // epilogue: the two warps of a lane quadrant take alternate 32-column
+    // chunks; their column scales are fetched before the accumulators are ready
+    constexpr int kChunks = (kBN + 63) / 64;
+    const int half = dq >> 2;
+    float xs_pre[kChunks] = {};
     if (F16) {
 #pragma unroll
-      for (int i = 0; i < kBN / 64; ++i) {
-        const int col = c_begin + 32 * i + lane;
+      for (int i = 0; i < kChunks; ++i) {
+        const int col = 32 * (2 * i + half) + lane;
         if (col < n) xs_pre[i] = P.x_scale[row0 + col];
       }
     }
@@ -435,8 +440,8 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const TcParams P) {
       const int rr = r;                          // weight row of this thread's TMEM lane
       const float rs0 = F16 ? rowscale[rr] : 1.f, rs1 = F16 ? rowscale[128 + rr] : 1.f;
 #pragma unroll
-      for (int ci = 0; ci < kBN / 64; ++ci) {
-        const int c0 = c_begin + 32 * ci;
+      for (int ci = 0; ci < kChunks; ++ci) {
+        const int c0 = 32 * (2 * ci + half);
         if (c0 >= n_mma) break;
         float a0[32], a1[32];
         tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + c0, a0);
