@@ -62,7 +62,9 @@ constexpr int kDqWarps = 8;
 constexpr int kMmaWarp = 0;                      // TMEM allocator and MMA issuer
 constexpr int kFirstDqWarp = 1;                  // dequantisers 1..8, then the epilogue
 constexpr int kBWarp = kFirstDqWarp + kDqWarps;  // token-tile TMA producer
-constexpr int kTcThreads = (kBWarp + 1) * 32;
+constexpr int kRawWarp = kBWarp + 1;             // packed-weight TMA producer (RAW_TMA only)
+__host__ __device__ constexpr int tc_threads(bool raw_tma) { return (raw_tma ? kRawWarp + 1 : kBWarp + 1) * 32; }
+constexpr int kStagesRaw = 6;                    // packed-weight ring depth (RAW_TMA only)
 // TMEM columns: accumulator 0 at [0, kBN), accumulator 1 at [kBN, 2 kBN),
 // dequantised weight tiles (A operands) at [2 kBN, ...): per (stage, acc) a
 // 128-lane x 32-column slot holding 64 K values of each row as f16/bf16 pairs.
@@ -74,12 +76,15 @@ static_assert(kACol0 + kStagesA * 2 * kASlotCols <= kTmemCols, "TMEM columns exc
 
 constexpr int kBBoxRows = 64;                     // token rows per TMA box
 constexpr int kBBoxBytes = kBBoxRows * kBK * 2;   // 8 KB
-constexpr int kBTileBytes = kBN * kBK * 2;        // token tile slot
+constexpr int kBTileBytes = (kBN + kBBoxRows - 1) / kBBoxRows * kBBoxBytes;  // whole 64-row boxes
+constexpr int kRawTileBytes = kBM * kBK / 2;      // 4 KB packed (128 rows x 32 bytes)
 constexpr int kOffB = 0;                                       // [stage]
-constexpr int kOffRowScale = kOffB + kStagesB * kBTileBytes;
-constexpr int kOffBar = kOffRowScale + 2 * kBM * 4;
-constexpr int kSmemTc = kOffBar + 256 + 1024;                  // + barriers, slack for 1 KB alignment
-static_assert(kSmemTc <= 227 * 1024, "shared memory of the tensor-core kernel exceeds 227 KB");
+constexpr int kOffRaw = kOffB + kStagesB * kBTileBytes;        // [stage][acc] (RAW_TMA only)
+__host__ __device__ constexpr int off_rowscale(bool raw_tma) { return kOffRaw + (raw_tma ? kStagesRaw * 2 * kRawTileBytes : 0); }
+__host__ __device__ constexpr int off_bar(bool raw_tma) { return off_rowscale(raw_tma) + 2 * kBM * 4; }
+__host__ __device__ constexpr int smem_tc(bool raw_tma) { return off_bar(raw_tma) + 512 + 1024; }  // + barriers, 1 KB alignment slack
+static_assert(smem_tc(true) <= 227 * 1024, "shared memory of the tensor-core kernel exceeds 227 KB");
+static_assert(kBTileBytes % 1024 == 0, "token slots must stay 1 KB aligned for the 128-byte swizzle");
 
 struct TcParams {
   const uint8_t* w;        // packed E2M1 weights [rows][K/2]
@@ -237,13 +242,15 @@ __device__ __forceinline__ uint4 dequant8_f16(uint32_t packed, int e) {
 // by the per-row power of two of the gather; both undone in the epilogue (per
 // TMEM lane and column), then SwiGLU.  Otherwise (W2): operands bf16
 // (weights exactly 2^(s-127) * code, h as written), epilogue writes fp32 y.
-template <bool F16>
-__global__ void __launch_bounds__(kTcThreads, 1)
-tc_kernel(const __grid_constant__ CUtensorMap map_b, const TcParams P) {
+template <bool F16, bool RAW_TMA>
+__global__ void __launch_bounds__(tc_threads(RAW_TMA), 1)
+tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_raw, const TcParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* rowscale = reinterpret_cast<float*>(smem + kOffRowScale);  // [2][128]
-  uint64_t* b_full = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  float* rowscale = reinterpret_cast<float*>(smem + off_rowscale(RAW_TMA));  // [2][128]
+  uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem + off_bar(RAW_TMA));
+  uint64_t* raw_empty = raw_full + kStagesRaw;
+  uint64_t* b_full = raw_empty + kStagesRaw;
   uint64_t* b_empty = b_full + kStagesB;
   uint64_t* a_full = b_empty + kStagesB;
   uint64_t* a_empty = a_full + kStagesA;
@@ -261,6 +268,12 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const TcParams P) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
+    if (RAW_TMA) {
+      for (int s = 0; s < kStagesRaw; ++s) {
+        mbar_init(&raw_full[s], 1);
+        mbar_init(&raw_empty[s], kDqWarps);
+      }
+    }
     for (int s = 0; s < kStagesB; ++s) {
       mbar_init(&b_full[s], 1);
       mbar_init(&b_empty[s], 1);
@@ -283,7 +296,20 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const TcParams P) {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == kBWarp) {
+  if (RAW_TMA && warp == kRawWarp) {
+    // ---------------- TMA producer: packed weights ----------------
+    if (lane == 0) {
+      for (int ks = 0; ks < nk; ++ks) {
+        const int s = ks % kStagesRaw;
+        const uint32_t ph = (ks / kStagesRaw) & 1;
+        if (!mbar_wait(&raw_empty[s], ph ^ 1u, abort_flag, P.err, kErrWaitTimeout)) break;
+        mbar_expect_tx(&raw_full[s], 2 * kRawTileBytes);
+        uint8_t* raw = smem + kOffRaw + s * 2 * kRawTileBytes;
+        tma_load_2d(raw, &map_raw, ks * (kBK / 2), wrow0, &raw_full[s]);
+        tma_load_2d(raw + kRawTileBytes, &map_raw, ks * (kBK / 2), wrow0 + P.acc1_offset, &raw_full[s]);
+      }
+    }
+  } else if (warp == kBWarp) {
     // ---------------- TMA producer: token tiles ----------------
     if (lane == 0) {
       const int boxes = (n_mma + kBBoxRows - 1) / kBBoxRows;
@@ -338,7 +364,7 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const TcParams P) {
     uint4 pfl[kPrefetch], pfh[kPrefetch];
 #pragma unroll
     for (int j = 0; j < kPrefetch; ++j) {
-      if (j < nk) {
+      if (!RAW_TMA && j < nk) {
         pfl[j] = ldg_stream(wrow_p + 32 * j, pol);
         pfh[j] = ldg_stream(wrow_p + 32 * j + 16, pol);
       }
@@ -379,10 +405,29 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const TcParams P) {
         const int ks = ks0 + j;
         if (ks < nk && ok) {
           const int sa = ks % kStagesA;
-          const uint4 lo = pfl[j], hi = pfh[j];
-          if (ks + kPrefetch < nk) {
-            pfl[j] = ldg_stream(wrow_p + 32 * (ks + kPrefetch), pol);
-            pfh[j] = ldg_stream(wrow_p + 32 * (ks + kPrefetch) + 16, pol);
+          uint4 lo, hi;
+          if (RAW_TMA) {
+            const int s = ks % kStagesRaw;
+            if (!mbar_wait(&raw_full[s], (ks / kStagesRaw) & 1, abort_flag, P.err, kErrWaitTimeout)) {
+              ok = false;
+              continue;
+            }
+            // conflict-free order of the two 16-byte halves of the 32-byte row
+            const int c_first = (lane >> 2) & 1;
+            const uint8_t* raw = smem + kOffRaw + (s * 2 + acc) * kRawTileBytes + r * 32;
+            const uint4 h0 = *reinterpret_cast<const uint4*>(raw + 16 * c_first);
+            const uint4 h1 = *reinterpret_cast<const uint4*>(raw + 16 * (c_first ^ 1));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&raw_empty[s]);  // the packed bytes are in registers now
+            lo = c_first ? h1 : h0;
+            hi = c_first ? h0 : h1;
+          } else {
+            lo = pfl[j];
+            hi = pfh[j];
+            if (ks + kPrefetch < nk) {
+              pfl[j] = ldg_stream(wrow_p + 32 * (ks + kPrefetch), pol);
+              pfh[j] = ldg_stream(wrow_p + 32 * (ks + kPrefetch) + 16, pol);
+            }
           }
           uint32_t sc;
           if (vec_scales) {
@@ -478,16 +523,16 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const TcParams P) {
   }
 }
 
-template <bool F16>
-cudaError_t launch_tc(const CUtensorMap& b, const TcParams& P, int max_tiles, cudaStream_t st) {
+template <bool F16, bool RAW_TMA>
+cudaError_t launch_tc(const CUtensorMap& b, const CUtensorMap& raw, const TcParams& P, int max_tiles, cudaStream_t st) {
   static bool configured = false;
   if (!configured) {
-    cudaFuncSetAttribute(tc_kernel<F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTc);
+    cudaFuncSetAttribute(tc_kernel<F16, RAW_TMA>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_tc(RAW_TMA));
     configured = true;
   }
   const long long grid = (long long)max_tiles * P.mblocks;
   if (grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-  tc_kernel<F16><<<(unsigned)grid, kTcThreads, kSmemTc, st>>>(b, P);
+  tc_kernel<F16, RAW_TMA><<<(unsigned)grid, tc_threads(RAW_TMA), smem_tc(RAW_TMA), st>>>(b, raw, P);
   return cudaGetLastError();
 }
 
@@ -496,8 +541,10 @@ cudaError_t launch_tc(const CUtensorMap& b, const TcParams& P, int max_tiles, cu
 cudaError_t launch_tc_w13(const moe_fp4_dims& d, const uint8_t* w13, const uint8_t* w13s, const Workspace& ws,
                           cudaStream_t st) {
   const size_t S = (size_t)d.T * d.k;
-  CUtensorMap b;
-  if (!make_map_2d(&b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws.x_perm, d.d, S, (uint64_t)d.d * 2, kBK, kBBoxRows,
+  CUtensorMap b, raw;
+  if (!make_map_2d(&raw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w13, d.d / 2, (uint64_t)d.E * 2 * d.I, d.d / 2, kBK / 2, kBM,
+                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      !make_map_2d(&b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws.x_perm, d.d, S, (uint64_t)d.d * 2, kBK, kBBoxRows,
                    CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   TcParams P{};
@@ -515,7 +562,7 @@ cudaError_t launch_tc_w13(const moe_fp4_dims& d, const uint8_t* w13, const uint8
   P.acc1_offset = d.I;
   P.I = d.I;
   P.d = d.d;
-  return launch_tc<true>(b, P, ws.max_tc_tiles, st);
+  return launch_tc<true, true>(b, raw, P, ws.max_tc_tiles, st);
 }
 
 cudaError_t launch_tc_w2(const moe_fp4_dims& d, const uint8_t* w2, const uint8_t* w2s, const Workspace& ws,
@@ -539,7 +586,7 @@ cudaError_t launch_tc_w2(const moe_fp4_dims& d, const uint8_t* w2, const uint8_t
   P.acc1_offset = kBM;
   P.I = d.I;
   P.d = d.d;
-  return launch_tc<false>(b, P, ws.max_tc_tiles, st);
+  return launch_tc<false, false>(b, b, P, ws.max_tc_tiles, st);  // the packed weights are read without TMA
 }
 
 }  // namespace moe_fp4
