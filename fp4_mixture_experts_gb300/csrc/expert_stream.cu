@@ -33,8 +33,15 @@
 namespace moe_fp4 {
 namespace {
 
-constexpr int kConsWarps = 8;
+#ifndef MOE_STREAM_KSPLIT
+#define MOE_STREAM_KSPLIT 2
+#endif
+constexpr int kTiles = 8;                        // 16-row tiles per 128-row stage
+constexpr int kKSplit = MOE_STREAM_KSPLIT;       // warps sharing a tile, each taking 16/kKSplit blocks per stage
+constexpr int kBlkPerWarp = 16 / kKSplit;
+constexpr int kConsWarps = kTiles * kKSplit;
 constexpr int kThreads = (kConsWarps + 1) * 32;
+constexpr int kRedBytes = 2 * kTiles * (kKSplit - 1) * 32 * 16;  // double-buffered partial sums of the split
 constexpr int kRowsPerBlock = 128;     // weight rows per item (W13: 64 gate + 64 up)
 constexpr int kKStage = 512;           // K elements per stage
 constexpr int kStageA = kRowsPerBlock * kKStage / 2;  // 32 KB packed
@@ -109,7 +116,8 @@ stream_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
   uint8_t* xs_buf = ring + (size_t)P.stages * kStageBytes;          // [8 tokens][x_pitch] f16
-  float* tok_scale = reinterpret_cast<float*>(xs_buf + (size_t)kMaxTok * P.x_pitch);  // [8]
+  float4* red = reinterpret_cast<float4*>(xs_buf + (size_t)kMaxTok * P.x_pitch);  // [2][kKSplit-1][8 tiles][32]
+  float* tok_scale = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(red) + kRedBytes);  // [8]
   uint64_t* full = reinterpret_cast<uint64_t*>(tok_scale + kMaxTok);
   uint64_t* empty = full + P.stages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + P.stages);
@@ -155,9 +163,10 @@ stream_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__
 
   // ---------------- consumer warps ----------------
   const int g = lane >> 2, t = lane & 3;
+  const int tile = warp % kTiles, kpart = warp / kTiles;  // 16-row tile, share of the stage's blocks
   // rows of this thread inside the stage's 128 rows (A-fragment rows g and g+8)
-  const int rowA = W13 ? warp * 8 + g : warp * 16 + g;         // gate row / first W2 row
-  const int rowB = W13 ? 64 + warp * 8 + g : warp * 16 + g + 8; // up row / second W2 row
+  const int rowA = W13 ? tile * 8 + g : tile * 16 + g;         // gate row / first W2 row
+  const int rowB = W13 ? 64 + tile * 8 + g : tile * 16 + g + 8; // up row / second W2 row
   // swizzled byte offsets of this thread's 4 packed bytes, per 16-byte chunk
   const int box_stride = W13 ? 8192 : 16384;
   const int ra = W13 ? rowA & 63 : rowA, rbw = W13 ? rowB & 63 : rowB;
@@ -165,7 +174,7 @@ stream_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__
   const int baseB = (W13 ? (rowB >> 6) * 16384 : 0) + rbw * 128 + 4 * t;
   const int swA_ = ra & 7, swB_ = rbw & 7;
   int cur = -1, row0 = 0, mt = 0;
-  int slot = 0;
+  int slot = 0, rbuf = 0;
   uint32_t phase = 0;
   for (long long it = it0; it < it1; ++it) {
     const int c = (int)(it / P.n_rb), rb = (int)(it % P.n_rb);
@@ -176,7 +185,9 @@ stream_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__
       row0 = ch.y;
       mt = ch.z;
       uint8_t* xrow = xs_buf + (size_t)warp * P.x_pitch;
-      if (warp < mt) {
+      if (warp >= kMaxTok) {
+        // no token row for this warp
+      } else if (warp < mt) {
         const int src_row = W13 ? P.sorted_slot[row0 + warp] / P.k : row0 + warp;
         const uint4* src = reinterpret_cast<const uint4*>(P.act + (size_t)src_row * P.K);
         uint32_t emax = 1;
@@ -219,16 +230,21 @@ stream_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__
         // packed rows: two 128-byte-swizzled boxes (K 0..255, 256..511) of 128 (or 2 x 64) rows
         const uint8_t* pa = st + baseA;
         const uint8_t* pb = st + baseB;
-        const uint4 sA = *reinterpret_cast<const uint4*>(st + kStageA + rowA * 16);
-        const uint4 sB = *reinterpret_cast<const uint4*>(st + kStageA + rowB * 16);
-        const uint32_t swA[4] = {sA.x, sA.y, sA.z, sA.w}, swB[4] = {sB.x, sB.y, sB.z, sB.w};
-        const uint8_t* xk = xg + (size_t)ks * kKStage * 2;
+        // this warp's blocks [kpart * kBlkPerWarp, +kBlkPerWarp) of the stage's 16
+        uint32_t swA[kBlkPerWarp / 4], swB[kBlkPerWarp / 4];
 #pragma unroll
-        for (int blk = 0; blk < 16; ++blk) {
+        for (int i = 0; i < kBlkPerWarp / 4; ++i) {
+          swA[i] = *reinterpret_cast<const uint32_t*>(st + kStageA + rowA * 16 + kpart * kBlkPerWarp + 4 * i);
+          swB[i] = *reinterpret_cast<const uint32_t*>(st + kStageA + rowB * 16 + kpart * kBlkPerWarp + 4 * i);
+        }
+        const uint8_t* xk = xg + (size_t)ks * kKStage * 2 + kpart * kBlkPerWarp * 64;
+#pragma unroll
+        for (int bi = 0; bi < kBlkPerWarp; ++bi) {
+          const int blk = kpart * kBlkPerWarp + bi;  // uniform over the warp
           const int half = blk >> 3, chunk = blk & 7;
           const uint32_t wa = *reinterpret_cast<const uint32_t*>(pa + half * box_stride + ((chunk ^ swA_) << 4));
           const uint32_t wb = *reinterpret_cast<const uint32_t*>(pb + half * box_stride + ((chunk ^ swB_) << 4));
-          const uint4 xf = *reinterpret_cast<const uint4*>(xk + blk * 64);
+          const uint4 xf = *reinterpret_cast<const uint4*>(xk + bi * 64);
           const float zero[4] = {0.f, 0.f, 0.f, 0.f};
           float cb[4];
           // the conversion reads the low byte of its operand (no mask needed)
@@ -239,7 +255,7 @@ stream_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__
           a[2] = e2m1x2_h2(wa >> 24);
           a[3] = e2m1x2_h2(wb >> 24);
           mma_16816(cb, a, xf.z, xf.w, cb);
-          const float fa = scale2_of(swA[blk >> 2], blk & 3), fb = scale2_of(swB[blk >> 2], blk & 3);
+          const float fa = scale2_of(swA[bi >> 2], bi & 3), fb = scale2_of(swB[bi >> 2], bi & 3);
           acc[0] = fmaf(cb[0], fa, acc[0]);
           acc[1] = fmaf(cb[1], fa, acc[1]);
           acc[2] = fmaf(cb[2], fb, acc[2]);
@@ -253,16 +269,41 @@ stream_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__
         phase ^= 1u;
       }
     }
-    if (*abort_flag) continue;  // keep meeting the chunk barriers, no output
+    // the warps sharing a tile add their partial sums; the exit decision on an
+    // abort is taken jointly (barrier with an OR vote) so no barrier is left waiting
+    bool aborted = *abort_flag;
+    if (kKSplit > 1) {
+      if (kpart > 0)
+        red[((rbuf * (kKSplit - 1) + kpart - 1) * kTiles + tile) * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      uint32_t any;
+      asm volatile(
+          "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n}"
+          : "=r"(any)
+          : "r"((uint32_t)aborted), "r"(2 + tile), "r"(32 * kKSplit)
+          : "memory");
+      aborted = any != 0;
+      if (kpart == 0) {
+#pragma unroll
+        for (int p = 0; p < kKSplit - 1; ++p) {
+          const float4 o = red[((rbuf * (kKSplit - 1) + p) * kTiles + tile) * 32 + lane];
+          acc[0] += o.x;
+          acc[1] += o.y;
+          acc[2] += o.z;
+          acc[3] += o.w;
+        }
+      }
+      rbuf ^= 1;
+    }
+    if (aborted || kpart > 0) continue;  // keep meeting the chunk barriers, no output
     // epilogue: acc[0..1] = row A x tokens 2t, 2t+1; acc[2..3] = row B
     const int t0 = 2 * t, t1 = 2 * t + 1;
     const float s0 = tok_scale[t0], s1 = tok_scale[t1];
     if (W13) {
-      const int i = rb * 64 + warp * 8 + g;
+      const int i = rb * 64 + tile * 8 + g;
       if (t0 < mt) P.h_out[(size_t)(row0 + t0) * P.I + i] = f32_to_bf16_rn(swiglu(acc[0] * s0, acc[2] * s0));
       if (t1 < mt) P.h_out[(size_t)(row0 + t1) * P.I + i] = f32_to_bf16_rn(swiglu(acc[1] * s1, acc[3] * s1));
     } else {
-      const int n = rb * 128 + warp * 16 + g;
+      const int n = rb * 128 + tile * 16 + g;
       if (t0 < mt) {
         P.y_out[(size_t)(row0 + t0) * P.d + n] = acc[0] * s0;
         P.y_out[(size_t)(row0 + t0) * P.d + n + 8] = acc[2] * s0;
@@ -276,7 +317,7 @@ stream_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__
 }
 
 size_t smem_needed(int stages, int x_pitch) {
-  return 1024 /* alignment slack */ + (size_t)stages * kStageBytes + (size_t)kMaxTok * x_pitch +
+  return 1024 /* alignment slack */ + (size_t)stages * kStageBytes + (size_t)kMaxTok * x_pitch + kRedBytes +
          kMaxTok * sizeof(float) + 2 * stages * sizeof(uint64_t) + 16;
 }
 
