@@ -7,7 +7,8 @@
 
 namespace moe_fp4 {
 
-constexpr uint32_t kWaitLimit = 1u << 22;  // try_wait rounds before a wait gives up (~seconds)
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a wait gives up after 2 s
+constexpr uint32_t kSuspendHintNs = 20000;        // a waiting thread sleeps (up to 20 us) instead of spinning
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -29,13 +30,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait on phase `parity`.  Returns false on timeout (after raising the
-// CTA's abort flag and the device error word) or once another thread aborted.
+// try_wait with a suspend-time hint: the thread is parked until the phase
+// completes or the hint elapses, so waiting warps do not steal issue slots
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait on phase `parity`.  Returns false on timeout (2 s of the global
+// timer; after raising the CTA's abort flag and the device error word) or once
+// another thread aborted.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int32_t* err,
                                           int err_code) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63) == 63 && *abort_flag) return false;
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) break;
   }
   *abort_flag = 1;
   atomicOr(err, err_code);
