@@ -226,10 +226,9 @@ __device__ __forceinline__ uint32_t f16x2_pow2(int e) {
   return b | (b << 16);
 }
 
-// 4 packed bytes (8 E2M1 codes, K ascending) -> 8 exact f16 values times 2^e
-// (e = s - s_ref of the row; exact while e >= -23)
-__device__ __forceinline__ uint4 dequant8_f16(uint32_t packed, int e) {
-  const uint32_t m = f16x2_pow2(e);
+// 4 packed bytes (8 E2M1 codes, K ascending) -> 8 exact f16 values times the
+// factor pair m = f16x2_pow2(s - s_ref) (exact while s - s_ref >= -23)
+__device__ __forceinline__ uint4 dequant8_f16(uint32_t packed, uint32_t m) {
   uint32_t o[4];
 #pragma unroll
   for (int b = 0; b < 4; ++b) o[b] = f16x2_mul(e2m1x2_to_f16x2(packed >> (8 * b)), m);
@@ -412,15 +411,15 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
               ok = false;
               continue;
             }
-            // conflict-free order of the two 16-byte halves of the 32-byte row
-            const int c_first = (lane >> 2) & 1;
+            // the tile arrives with the 32-byte swizzle: the two 16-byte halves of
+            // row r are swapped when bit 2 of r is set, which keeps both reads
+            // of a warp free of bank conflicts
+            const int sw = ((r >> 2) & 1) << 4;
             const uint8_t* raw = smem + kOffRaw + (s * 2 + acc) * kRawTileBytes + r * 32;
-            const uint4 h0 = *reinterpret_cast<const uint4*>(raw + 16 * c_first);
-            const uint4 h1 = *reinterpret_cast<const uint4*>(raw + 16 * (c_first ^ 1));
+            lo = *reinterpret_cast<const uint4*>(raw + sw);
+            hi = *reinterpret_cast<const uint4*>(raw + (16 ^ sw));
             __syncwarp();
             if (lane == 0) mbar_arrive(&raw_empty[s]);  // the packed bytes are in registers now
-            lo = c_first ? h1 : h0;
-            hi = c_first ? h0 : h1;
           } else {
             lo = pfl[j];
             hi = pfh[j];
@@ -447,11 +446,12 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
             ok = false;
           } else {
             const uint32_t s0 = sc & 0xFFu, s1 = (sc >> 8) & 0xFFu;
+            const uint32_t m0 = F16 ? f16x2_pow2((int)s0 - s_ref) : 0u, m1 = F16 ? f16x2_pow2((int)s1 - s_ref) : 0u;
             uint32_t av[32];  // column j = K elements (2j, 2j+1) of this row
 #pragma unroll
             for (int c = 0; c < 8; ++c) {
               const uint32_t sb = c < 4 ? s0 : s1;
-              const uint4 v = F16 ? dequant8_f16(w[c], (int)sb - s_ref) : dequant8(w[c], sb);
+              const uint4 v = F16 ? dequant8_f16(w[c], c < 4 ? m0 : m1) : dequant8(w[c], sb);
               av[4 * c + 0] = v.x;
               av[4 * c + 1] = v.y;
               av[4 * c + 2] = v.z;
@@ -543,7 +543,7 @@ cudaError_t launch_tc_w13(const moe_fp4_dims& d, const uint8_t* w13, const uint8
   const size_t S = (size_t)d.T * d.k;
   CUtensorMap b, raw;
   if (!make_map_2d(&raw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w13, d.d / 2, (uint64_t)d.E * 2 * d.I, d.d / 2, kBK / 2, kBM,
-                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
+                   CU_TENSOR_MAP_SWIZZLE_32B) ||
       !make_map_2d(&b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws.x_perm, d.d, S, (uint64_t)d.d * 2, kBK, kBBoxRows,
                    CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
