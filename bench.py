@@ -147,21 +147,32 @@ def dist_setup(n_gpus):
     return rank, world, local, dist
 
 
-def barrier(dist):
+def barrier(dist, device="cuda"):
     import torch
-    torch.cuda.synchronize()
+    if device == "cuda":
+        torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
-        torch.cuda.synchronize()
+        if device == "cuda":
+            torch.cuda.synchronize()
 
 
-def max_over_ranks(dist, v):
+def _reduce(dist, v, op, device):
     import torch
     if dist is None:
         return v
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    t = torch.tensor([v], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=op)
     return float(t.item())
+
+
+def max_over_ranks(dist, v, device="cuda"):
+    """the slowest rank's time (the whole job waits for it)"""
+    return v if dist is None else _reduce(dist, v, dist.ReduceOp.MAX, device)
+
+
+def sum_over_ranks(dist, v, device="cuda"):
+    return v if dist is None else _reduce(dist, v, dist.ReduceOp.SUM, device)
 
 
 def measure_workload(name, steps, warmup, dist, local, sampler=None):

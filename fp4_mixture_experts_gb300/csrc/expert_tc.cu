@@ -568,8 +568,14 @@ cudaError_t launch_tc_w13(const moe_fp4_dims& d, const uint8_t* w13, const uint8
 cudaError_t launch_tc_w2(const moe_fp4_dims& d, const uint8_t* w2, const uint8_t* w2s, const Workspace& ws,
                          cudaStream_t st) {
   const size_t S = (size_t)d.T * d.k;
-  CUtensorMap b;
-  if (!make_map_2d(&b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ws.h, d.I, S, (uint64_t)d.I * 2, kBK, kBBoxRows,
+#ifndef MOE_TC_W2_RAW_TMA
+#define MOE_TC_W2_RAW_TMA 0
+#endif
+  CUtensorMap b, raw;
+  if ((MOE_TC_W2_RAW_TMA &&
+       !make_map_2d(&raw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w2, d.I / 2, (uint64_t)d.E * d.d, d.I / 2, kBK / 2, kBM,
+                    CU_TENSOR_MAP_SWIZZLE_32B)) ||
+      !make_map_2d(&b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ws.h, d.I, S, (uint64_t)d.I * 2, kBK, kBBoxRows,
                    CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   TcParams P{};
@@ -586,6 +592,7 @@ cudaError_t launch_tc_w2(const moe_fp4_dims& d, const uint8_t* w2, const uint8_t
   P.acc1_offset = kBM;
   P.I = d.I;
   P.d = d.d;
+  if (MOE_TC_W2_RAW_TMA) return launch_tc<false, true>(b, raw, P, ws.max_tc_tiles, st);
   return launch_tc<false, false>(b, b, P, ws.max_tc_tiles, st);  // the packed weights are read without TMA
 }
 

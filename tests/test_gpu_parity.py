@@ -218,3 +218,14 @@ def test_full_size_routing_exact_and_sampled_out(moe, name, n_tok):
     got = r["out"][torch.from_numpy(toks).cuda()].cpu().numpy()
     m = assert_out_close(got, want, name)
     print(name, m)
+
+
+def test_d7168_streaming_path(moe):
+    """the decode (streaming) path at the large layer's d = 7168 (3-deep ring)"""
+    full_check(moe, make_layer(T=12, d=7168, I=2048, E=12, k=2, exp_lo=-8, exp_hi=-6, seed=31), GEMV)
+
+
+def test_routing_block_boundary(moe):
+    """T = 32 runs the single-block routing kernel, T = 33 the three-kernel one"""
+    for T in (32, 33):
+        full_check(moe, make_layer(T=T, d=1024, I=1024, E=64, k=8, seed=32 + T))
