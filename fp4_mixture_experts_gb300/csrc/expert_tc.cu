@@ -2,38 +2,45 @@
 //
 // A grouped GEMM per expert, swap-AB: the expert's weight rows are the UMMA M
 // operand (128 rows per accumulator) and the expert's token rows the N
-// operand (up to 128 per tile), so an expert with few rows wastes little of
+// operand (up to 192 per tile), so an expert with few rows wastes little of
 // the MMA ("low-M utilisation" is a limit the DeepSeek-V4-Flash-on-gfx90a
 // paper names).  One CTA computes two 128 x N accumulators that share the
 // token tile: gate and up rows of W13 (so SwiGLU fuses into the epilogue), or
 // two adjacent 128-row blocks of W2.
 //
-// Warp roles (320 threads), per 64-wide K step:
-//   warp 9      TMA producer of the token tile (up to 192 rows, 128-byte
-//               swizzle, 3-deep ring: mostly L2 hits, shared by the CTAs of
-//               one expert)
-//   warp 0      TMEM allocator (512 columns: two accumulators of up to 192
-//               columns and the A ring) and MMA issuer: 2 x 4
-//               tcgen05.mma.kind::f16 (M=128, N=tile, K=16) per K step, fp32
-//               accumulators in TMEM; tcgen05.commit frees the token and
-//               weight slots
-//   warps 1..8  dequantisers (2-deep ring of dequantised tiles, kept in TMEM so
-//               that the MMA reads its A operand from tensor memory and shared
-//               memory only carries the token tiles); each thread streams its
-//               row's 32 packed bytes per K step (one 32-byte sector) straight
-//               into registers, 4 steps ahead: one thread per weight row; E2M1 pairs decoded by
+// Warp roles, per 64-wide K step (one stage of a 2- to 4-deep ring):
+//   warp 9      TMA producer of the token tile (up to 192 rows in 64-row
+//               boxes, 128-byte swizzle; mostly L2 hits, shared by the CTAs
+//               of one expert)
+//   warp 10     (W13) TMA producer of the packed weights, 6-deep ring of
+//               128 rows x 32 bytes per accumulator, 32-byte swizzle
+//   warp 0 and the last warp
+//               MMA issuers, one per accumulator: 4 tcgen05.mma.kind::f16
+//               (M=128, N=tile, K=16) per K step each, fp32 accumulators in
+//               TMEM.  An MMA instruction costs the issuing thread about as
+//               long as it runs, and so do its barrier wait and commit; with
+//               two issuers one of them is always feeding the tensor pipe
+//               while the other synchronises.  Warp 0 also owns TMEM
+//               (512 columns: both accumulators, then the A ring).
+//   warps 1..8  dequantisers, one thread per weight row: the row's 32 packed
+//               bytes per K step come from the TMA ring (W13) or straight from
+//               global memory 4 steps ahead (W2); E2M1 pairs are decoded by
 //               cvt.rn.f16x2.e2m1x2 and scaled exactly by a power of two
 //               (mul.f16x2 for W13, mul.bf16x2 after a bf16 re-encoding for
-//               W2), written to TMEM with tcgen05.st (lane = weight row); then
-//               the epilogue (tcgen05.ld, SwiGLU + bf16 rounding of h, or y)
+//               W2) and written to the stage's A slot in TMEM with tcgen05.st
+//               (lane = weight row), so that the MMA reads its A operand from
+//               tensor memory; then the epilogue (tcgen05.ld, SwiGLU + bf16
+//               rounding of h, or y)
+// A stage is full once the token tile has landed and all 8 dequantisers have
+// written their A slots (one mbarrier), and empty once both issuers' MMAs on
+// it have completed (one mbarrier, two tcgen05.commit arrivals).
 // Weights are dequantised exactly (an E2M1 value times a power of two has
 // 2 significant bits), so the MMA multiplies exact products and accumulates
 // them in fp32.  W13 runs on f16 operands: the weight row is scaled by
 // 2^(s - s_ref) (exact within 36 binades of the row's largest scale) and the
 // activation row by the gather's power of two; both factors come back in the
-// epilogue.  Every mbarrier wait is
-// bounded; a timeout sets the error word and an abort flag that releases the
-// other roles, and TMEM is always freed.
+// epilogue.  Every mbarrier wait is bounded; a timeout sets the error word
+// and an abort flag that releases the other roles, and TMEM is always freed.
 #include <cuda.h>
 #include <cuda_fp16.h>
 
@@ -46,43 +53,45 @@ namespace {
 constexpr int kBM = 128;                 // weight rows per accumulator
 constexpr int kBK = 64;                  // K elements per stage
 constexpr int kBN = kTcTileN;            // token rows per tile (<= 192: TMEM holds 2 accumulators + A)
-#ifndef MOE_TC_STAGES_A
-#define MOE_TC_STAGES_A 2
+#ifndef MOE_TC_STAGES
+#define MOE_TC_STAGES 4
 #endif
-#ifndef MOE_TC_STAGES_B
-#define MOE_TC_STAGES_B 4
-#endif
-constexpr int kStagesA = MOE_TC_STAGES_A;      // dequantised weight tiles (dequant -> MMA)
-constexpr int kStagesB = MOE_TC_STAGES_B;      // token tiles (TMA -> MMA)
+constexpr int kStages = MOE_TC_STAGES;   // most ring stages (token tile + A slots); TMEM may allow fewer
 #ifndef MOE_TC_PREFETCH
 #define MOE_TC_PREFETCH 4
 #endif
-constexpr int kPrefetch = MOE_TC_PREFETCH;    // K steps of packed weights each dequantiser keeps in flight
+constexpr int kPrefetch = MOE_TC_PREFETCH;    // K steps of packed weights each dequantiser keeps in flight (W2)
 constexpr int kDqWarps = 8;
-constexpr int kMmaWarp = 0;                      // TMEM allocator and MMA issuer
+constexpr int kMmaWarp = 0;                      // TMEM allocator, MMA issuer of accumulator 0
 constexpr int kFirstDqWarp = 1;                  // dequantisers 1..8, then the epilogue
 constexpr int kBWarp = kFirstDqWarp + kDqWarps;  // token-tile TMA producer
 constexpr int kRawWarp = kBWarp + 1;             // packed-weight TMA producer (RAW_TMA only)
-__host__ __device__ constexpr int tc_threads(bool raw_tma) { return (raw_tma ? kRawWarp + 1 : kBWarp + 1) * 32; }
-constexpr int kStagesRaw = 6;                    // packed-weight ring depth (RAW_TMA only)
-// TMEM columns: accumulator 0 at [0, kBN), accumulator 1 at [kBN, 2 kBN),
-// dequantised weight tiles (A operands) at [2 kBN, ...): per (stage, acc) a
-// 128-lane x 32-column slot holding 64 K values of each row as f16/bf16 pairs.
+__host__ __device__ constexpr int mma1_warp(bool raw_tma) { return raw_tma ? kRawWarp + 1 : kBWarp + 1; }
+__host__ __device__ constexpr int tc_threads(bool raw_tma) { return (mma1_warp(raw_tma) + 1) * 32; }
+#ifndef MOE_TC_STAGES_RAW
+#define MOE_TC_STAGES_RAW 6
+#endif
+constexpr int kStagesRaw = MOE_TC_STAGES_RAW;    // packed-weight ring depth (RAW_TMA only)
+// TMEM columns, per tile of n token rows (n_acc = n rounded up to 32):
+// accumulator 0 at [0, n_acc), accumulator 1 at [n_acc, 2 n_acc), and the
+// A slots in the rest: per (stage, acc) a 128-lane x 32-column slot holding
+// 64 K values of each row as f16/bf16 pairs.  Narrower tiles leave room for
+// more stages (2 at n = 192, 3 at 160, 4 at 128).
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccCols = kBN;
-constexpr uint32_t kACol0 = 2 * kBN;
 constexpr uint32_t kASlotCols = kBK / 2;
-static_assert(kACol0 + kStagesA * 2 * kASlotCols <= kTmemCols, "TMEM columns exceeded");
+static_assert(2 * ((kBN + 31) / 32 * 32) + 2 * 2 * kASlotCols <= kTmemCols, "TMEM columns exceeded at the widest tile");
+static_assert(kStages >= 2 && kStages <= 4, "ring of 2 to 4 stages");
 
 constexpr int kBBoxRows = 64;                     // token rows per TMA box
 constexpr int kBBoxBytes = kBBoxRows * kBK * 2;   // 8 KB
 constexpr int kBTileBytes = (kBN + kBBoxRows - 1) / kBBoxRows * kBBoxBytes;  // whole 64-row boxes
 constexpr int kRawTileBytes = kBM * kBK / 2;      // 4 KB packed (128 rows x 32 bytes)
 constexpr int kOffB = 0;                                       // [stage]
-constexpr int kOffRaw = kOffB + kStagesB * kBTileBytes;        // [stage][acc] (RAW_TMA only)
+constexpr int kOffRaw = kOffB + kStages * kBTileBytes;         // [stage][acc] (RAW_TMA only)
 __host__ __device__ constexpr int off_rowscale(bool raw_tma) { return kOffRaw + (raw_tma ? kStagesRaw * 2 * kRawTileBytes : 0); }
 __host__ __device__ constexpr int off_bar(bool raw_tma) { return off_rowscale(raw_tma) + 2 * kBM * 4; }
 __host__ __device__ constexpr int smem_tc(bool raw_tma) { return off_bar(raw_tma) + 512 + 1024; }  // + barriers, 1 KB alignment slack
+static_assert((2 * kStagesRaw + 2 * kStages + 1) * 8 + 8 <= 512, "barrier area exceeded");
 static_assert(smem_tc(true) <= 227 * 1024, "shared memory of the tensor-core kernel exceeds 227 KB");
 static_assert(kBTileBytes % 1024 == 0, "token slots must stay 1 KB aligned for the 128-byte swizzle");
 
@@ -121,14 +130,6 @@ __device__ __forceinline__ uint32_t idesc_f16kind(int M, int N, uint32_t ab_type
          | (ab_type << 7) | (ab_type << 10)       // A, B format
          | ((uint32_t)(N >> 3) << 17)             // N
          | ((uint32_t)(M >> 4) << 24);            // M
-}
-
-__device__ __forceinline__ void umma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(tmem_d),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc)
-      : "memory");
 }
 
 // D[tmem] (+)= A[tmem] * B[smem]: the A operand is read from tensor memory
@@ -235,7 +236,7 @@ __device__ __forceinline__ uint4 dequant8_f16(uint32_t packed, uint32_t m) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// Tile of one CTA: token rows [row0, row0 + n) of one expert (n <= 256) times
+// Tile of one CTA: token rows [row0, row0 + n) of one expert (n <= 192) times
 // two 128-row weight blocks.  F16 (W13): operands f16, weight rows scaled by
 // 2^(s - s_ref(row)) with s_ref = (largest E8M0 of the row) - 13, activations
 // by the per-row power of two of the gather; both undone in the epilogue (per
@@ -249,11 +250,9 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
   float* rowscale = reinterpret_cast<float*>(smem + off_rowscale(RAW_TMA));  // [2][128]
   uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem + off_bar(RAW_TMA));
   uint64_t* raw_empty = raw_full + kStagesRaw;
-  uint64_t* b_full = raw_empty + kStagesRaw;
-  uint64_t* b_empty = b_full + kStagesB;
-  uint64_t* a_full = b_empty + kStagesB;
-  uint64_t* a_empty = a_full + kStagesA;
-  uint64_t* acc_full = a_empty + kStagesA;
+  uint64_t* full = raw_empty + kStagesRaw;    // [stage]: token tile landed and both A slots written
+  uint64_t* empty = full + kStages;           // [stage]: the MMAs of both accumulators on it completed
+  uint64_t* acc_full = empty + kStages;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -262,6 +261,9 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
   const int4 tl = P.tiles[tile];
   const int row0 = tl.y, n = tl.z;
   const int n_mma = (n + 15) & ~15;
+  const uint32_t acc_cols = (uint32_t)(n_mma + 31) & ~31u;   // accumulator 1 starts here
+  const uint32_t a_col0 = 2 * acc_cols;                        // first A slot
+  const int nS = min(kStages, (int)((kTmemCols - a_col0) / (2 * kASlotCols)));
   const int wrow0 = tl.x * P.rows_per_expert + mb * P.block_rows;
   const int nk = P.K / kBK;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -273,18 +275,15 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
         mbar_init(&raw_empty[s], kDqWarps);
       }
     }
-    for (int s = 0; s < kStagesB; ++s) {
-      mbar_init(&b_full[s], 1);
-      mbar_init(&b_empty[s], 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], kDqWarps + 1);  // the dequantisers and the token producer's expect_tx
+      mbar_init(&empty[s], 2);            // one commit per MMA issuer
     }
-    for (int s = 0; s < kStagesA; ++s) {
-      mbar_init(&a_full[s], kDqWarps);
-      mbar_init(&a_empty[s], 1);
-    }
-    mbar_init(acc_full, 1);
+    mbar_init(acc_full, 2);
     *abort_flag = 0;
     mbar_fence_init();
   }
+  __syncwarp();  // warp 0 reconverges before the warp-wide TMEM allocation
   if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                  "r"(kTmemCols));
@@ -298,14 +297,15 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
   if (RAW_TMA && warp == kRawWarp) {
     // ---------------- TMA producer: packed weights ----------------
     if (lane == 0) {
+      const uint64_t pol = l2_evict_first_policy();  // weights are read once: keep the token tiles in L2
       for (int ks = 0; ks < nk; ++ks) {
         const int s = ks % kStagesRaw;
         const uint32_t ph = (ks / kStagesRaw) & 1;
         if (!mbar_wait(&raw_empty[s], ph ^ 1u, abort_flag, P.err, kErrWaitTimeout)) break;
         mbar_expect_tx(&raw_full[s], 2 * kRawTileBytes);
         uint8_t* raw = smem + kOffRaw + s * 2 * kRawTileBytes;
-        tma_load_2d(raw, &map_raw, ks * (kBK / 2), wrow0, &raw_full[s]);
-        tma_load_2d(raw + kRawTileBytes, &map_raw, ks * (kBK / 2), wrow0 + P.acc1_offset, &raw_full[s]);
+        tma_load_2d_hint(raw, &map_raw, ks * (kBK / 2), wrow0, &raw_full[s], pol);
+        tma_load_2d_hint(raw + kRawTileBytes, &map_raw, ks * (kBK / 2), wrow0 + P.acc1_offset, &raw_full[s], pol);
       }
     }
   } else if (warp == kBWarp) {
@@ -313,35 +313,30 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
     if (lane == 0) {
       const int boxes = (n_mma + kBBoxRows - 1) / kBBoxRows;
       for (int ks = 0; ks < nk; ++ks) {
-        const int s = ks % kStagesB;
-        const uint32_t ph = (ks / kStagesB) & 1;
-        if (!mbar_wait(&b_empty[s], ph ^ 1u, abort_flag, P.err, kErrWaitTimeout)) break;
-        mbar_expect_tx(&b_full[s], boxes * kBBoxBytes);
+        const int s = ks % nS;
+        const uint32_t ph = (ks / nS) & 1;
+        if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, P.err, kErrWaitTimeout)) break;
+        mbar_expect_tx(&full[s], boxes * kBBoxBytes);
         uint8_t* b = smem + kOffB + s * kBTileBytes;
-        for (int i = 0; i < boxes; ++i) tma_load_2d(b + i * kBBoxBytes, &map_b, ks * kBK, row0 + i * kBBoxRows, &b_full[s]);
+        for (int i = 0; i < boxes; ++i) tma_load_2d(b + i * kBBoxBytes, &map_b, ks * kBK, row0 + i * kBBoxRows, &full[s]);
       }
     }
-  } else if (warp == kMmaWarp) {
-    // ---------------- MMA issuer ----------------
+  } else if (warp == kMmaWarp || warp == mma1_warp(RAW_TMA)) {
+    // ---------------- MMA issuers, one per accumulator ----------------
     if (lane == 0) {
+      const int acc = warp == kMmaWarp ? 0 : 1;
       const uint32_t idesc = idesc_f16kind(kBM, n_mma, F16 ? 0u : 1u);
+      const uint32_t d_tmem = tmem + acc * acc_cols;
       for (int ks = 0; ks < nk; ++ks) {
-        const int sa = ks % kStagesA, sb = ks % kStagesB;
-        if (!mbar_wait(&b_full[sb], (ks / kStagesB) & 1, abort_flag, P.err, kErrWaitTimeout) ||
-            !mbar_wait(&a_full[sa], (ks / kStagesA) & 1, abort_flag, P.err, kErrWaitTimeout))
-          break;
+        const int s = ks % nS;
+        if (!mbar_wait(&full[s], (ks / nS) & 1, abort_flag, P.err, kErrWaitTimeout)) break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const uint32_t b_addr = smem_u32(smem + kOffB + sb * kBTileBytes);
+        const uint32_t b_addr = smem_u32(smem + kOffB + s * kBTileBytes);
+        const uint32_t a_tmem = tmem + a_col0 + (s * 2 + acc) * kASlotCols;
 #pragma unroll
-        for (int acc = 0; acc < 2; ++acc) {
-          const uint32_t a_tmem = tmem + kACol0 + (sa * 2 + acc) * kASlotCols;
-#pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
-            umma_tmem_a(tmem + acc * kAccCols, a_tmem + kk * 8, desc_sw128(b_addr + kk * 32), idesc,
-                        (ks > 0 || kk > 0) ? 1u : 0u);
-        }
-        umma_commit(&b_empty[sb]);
-        umma_commit(&a_empty[sa]);
+        for (int kk = 0; kk < kBK / 16; ++kk)
+          umma_tmem_a(d_tmem, a_tmem + kk * 8, desc_sw128(b_addr + kk * 32), idesc, (ks > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(&empty[s]);
       }
       umma_commit(acc_full);
       // the accumulators must be final before TMEM can be freed, also on an abort
@@ -403,7 +398,7 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
       for (int j = 0; j < kPrefetch; ++j) {
         const int ks = ks0 + j;
         if (ks < nk && ok) {
-          const int sa = ks % kStagesA;
+          const int sa = ks % nS;
           uint4 lo, hi;
           if (RAW_TMA) {
             const int s = ks % kStagesRaw;
@@ -442,7 +437,7 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
             if (ks + 1 < nk) sc_next = *reinterpret_cast<const uint16_t*>(srow + 2 * (ks + 1));
           }
           const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-          if (!mbar_wait(&a_empty[sa], ((ks / kStagesA) & 1) ^ 1u, abort_flag, P.err, kErrWaitTimeout)) {
+          if (!mbar_wait(&empty[sa], ((ks / nS) & 1) ^ 1u, abort_flag, P.err, kErrWaitTimeout)) {
             ok = false;
           } else {
             const uint32_t s0 = sc & 0xFFu, s1 = (sc >> 8) & 0xFFu;
@@ -457,11 +452,11 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
               av[4 * c + 2] = v.z;
               av[4 * c + 3] = v.w;
             }
-            tmem_st32(tmem + ((uint32_t)(q * 32) << 16) + kACol0 + (sa * 2 + acc) * kASlotCols, av);
+            tmem_st32(tmem + ((uint32_t)(q * 32) << 16) + a_col0 + (sa * 2 + acc) * kASlotCols, av);
             asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             __syncwarp();
-            if (lane == 0) mbar_arrive(&a_full[sa]);
+            if (lane == 0) mbar_arrive(&full[sa]);
           }
         }
       }
@@ -490,7 +485,7 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
         if (c0 >= n_mma) break;
         float a0[32], a1[32];
         tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + c0, a0);
-        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + kAccCols + c0, a1);
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + acc_cols + c0, a1);
         if (F16) {
           const float xs_l = xs_pre[ci];
           const int i = mb * kBM + rr;
@@ -515,6 +510,11 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
       }
     }
   }
+  // every warp reconverges first: lanes that skipped a lane-0 role must not
+  // arrive at the CTA barrier ahead of their lane 0 (an aligned barrier counts
+  // a warp as arrived when any of its lanes gets there), so that TMEM is freed
+  // only after all epilogue reads
+  __syncwarp();
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
   __syncthreads();
   if (warp == kMmaWarp) {
