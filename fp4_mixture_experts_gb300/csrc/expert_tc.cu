@@ -42,6 +42,8 @@
 // epilogue.  Every mbarrier wait is bounded; a timeout sets the error word
 // and an abort flag that releases the other roles, and TMEM is always freed.
 #include <cuda.h>
+
+#include <algorithm>
 #include <cuda_fp16.h>
 
 #include "moe_fp4_internal.cuh"
@@ -69,9 +71,15 @@ constexpr int kRawWarp = kBWarp + 1;             // packed-weight TMA producer (
 __host__ __device__ constexpr int mma1_warp(bool raw_tma) { return raw_tma ? kRawWarp + 1 : kBWarp + 1; }
 __host__ __device__ constexpr int tc_threads(bool raw_tma) { return (mma1_warp(raw_tma) + 1) * 32; }
 #ifndef MOE_TC_STAGES_RAW
-#define MOE_TC_STAGES_RAW 6
+#define MOE_TC_STAGES_RAW 2
 #endif
 constexpr int kStagesRaw = MOE_TC_STAGES_RAW;    // packed-weight ring depth (RAW_TMA only)
+#ifndef MOE_TC_RAW_STEPS
+#define MOE_TC_RAW_STEPS 4
+#endif
+constexpr int kRawSteps = MOE_TC_RAW_STEPS;      // K steps per packed-weight stage: 1 (32-byte rows) or 4 (128-byte rows)
+static_assert(kRawSteps == 1 || kRawSteps == 4, "packed-weight stages of 1 or 4 K steps");
+constexpr int kRawRowBytes = kRawSteps * kBK / 2;
 // TMEM columns, per tile of n token rows (n_acc = n rounded up to 32):
 // accumulator 0 at [0, n_acc), accumulator 1 at [n_acc, 2 n_acc), and the
 // A slots in the rest: per (stage, acc) a 128-lane x 32-column slot holding
@@ -85,13 +93,13 @@ static_assert(kStages >= 2 && kStages <= 4, "ring of 2 to 4 stages");
 constexpr int kBBoxRows = 64;                     // token rows per TMA box
 constexpr int kBBoxBytes = kBBoxRows * kBK * 2;   // 8 KB
 constexpr int kBTileBytes = (kBN + kBBoxRows - 1) / kBBoxRows * kBBoxBytes;  // whole 64-row boxes
-constexpr int kRawTileBytes = kBM * kBK / 2;      // 4 KB packed (128 rows x 32 bytes)
+constexpr int kRawTileBytes = kBM * kRawRowBytes;  // packed tile of one accumulator's 128 rows
 constexpr int kOffB = 0;                                       // [stage]
 constexpr int kOffRaw = kOffB + kStages * kBTileBytes;         // [stage][acc] (RAW_TMA only)
 __host__ __device__ constexpr int off_rowscale(bool raw_tma) { return kOffRaw + (raw_tma ? kStagesRaw * 2 * kRawTileBytes : 0); }
 __host__ __device__ constexpr int off_bar(bool raw_tma) { return off_rowscale(raw_tma) + 2 * kBM * 4; }
 __host__ __device__ constexpr int smem_tc(bool raw_tma) { return off_bar(raw_tma) + 512 + 1024; }  // + barriers, 1 KB alignment slack
-static_assert((2 * kStagesRaw + 2 * kStages + 1) * 8 + 8 <= 512, "barrier area exceeded");
+static_assert((2 * kStagesRaw + 2 * kStages + 2) * 8 + 8 <= 512, "barrier area exceeded");
 static_assert(smem_tc(true) <= 227 * 1024, "shared memory of the tensor-core kernel exceeds 227 KB");
 static_assert(kBTileBytes % 1024 == 0, "token slots must stay 1 KB aligned for the 128-byte swizzle");
 
@@ -236,8 +244,35 @@ __device__ __forceinline__ uint4 dequant8_f16(uint32_t packed, uint32_t m) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
-// Tile of one CTA: token rows [row0, row0 + n) of one expert (n <= 192) times
-// two 128-row weight blocks.  F16 (W13): operands f16, weight rows scaled by
+// Geometry of one work item: token rows [row0, row0 + n) of one expert (n <=
+// 192) times two 128-row weight blocks (m-block mb).  TMEM holds the ring of
+// A slots first ([0, 64 nS) columns) and the two accumulators after it, each
+// n rounded up to 32 columns wide; narrower tiles leave room for more stages.
+struct TcItem {
+  int row0, n, n_mma, nS, wrow0, mb;
+  uint32_t acc_cols, acc0;
+};
+
+__device__ __forceinline__ TcItem tc_item(const TcParams& P, int item) {
+  TcItem t;
+  const int tile = item / P.mblocks;
+  t.mb = item % P.mblocks;
+  const int4 tl = P.tiles[tile];
+  t.row0 = tl.y;
+  t.n = tl.z;
+  t.n_mma = (t.n + 15) & ~15;
+  t.acc_cols = (uint32_t)(t.n_mma + 31) & ~31u;
+  t.nS = min(kStages, (int)((kTmemCols - 2 * t.acc_cols) / (2 * kASlotCols)));
+  t.acc0 = (uint32_t)t.nS * 2 * kASlotCols;
+  t.wrow0 = tl.x * P.rows_per_expert + t.mb * P.block_rows;
+  return t;
+}
+
+// Persistent: each CTA takes the work items blockIdx.x, blockIdx.x + gridDim.x,
+// ... (items are (tile, m-block) pairs, tile-major, so neighbouring CTAs share
+// token tiles in L2).  The rings run on across items, so the producers load
+// the next item's weights and token rows while the current one is finishing;
+// TMEM is allocated once.  F16 (W13): operands f16, weight rows scaled by
 // 2^(s - s_ref(row)) with s_ref = (largest E8M0 of the row) - 13, activations
 // by the per-row power of two of the gather; both undone in the epilogue (per
 // TMEM lane and column), then SwiGLU.  Otherwise (W2): operands bf16
@@ -252,20 +287,15 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
   uint64_t* raw_empty = raw_full + kStagesRaw;
   uint64_t* full = raw_empty + kStagesRaw;    // [stage]: token tile landed and both A slots written
   uint64_t* empty = full + kStages;           // [stage]: the MMAs of both accumulators on it completed
-  uint64_t* acc_full = empty + kStages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_full + 1);
+  uint64_t* acc_full = empty + kStages;       // per item: both accumulators final
+  uint64_t* acc_empty = acc_full + 1;         // per item: the epilogue has read the accumulators
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
-  const int tile = blockIdx.x / P.mblocks, mb = blockIdx.x % P.mblocks;
-  if (tile >= P.counts[2]) return;
-  const int4 tl = P.tiles[tile];
-  const int row0 = tl.y, n = tl.z;
-  const int n_mma = (n + 15) & ~15;
-  const uint32_t acc_cols = (uint32_t)(n_mma + 31) & ~31u;   // accumulator 1 starts here
-  const uint32_t a_col0 = 2 * acc_cols;                        // first A slot
-  const int nS = min(kStages, (int)((kTmemCols - a_col0) / (2 * kASlotCols)));
-  const int wrow0 = tl.x * P.rows_per_expert + mb * P.block_rows;
+  const int items = P.counts[2] * P.mblocks;
+  if ((int)blockIdx.x >= items) return;
   const int nk = P.K / kBK;
+  const int nrs = (nk + kRawSteps - 1) / kRawSteps;  // packed-weight stages per item (a last partial one reads zeros)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -280,6 +310,7 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
       mbar_init(&empty[s], 2);            // one commit per MMA issuer
     }
     mbar_init(acc_full, 2);
+    mbar_init(acc_empty, kDqWarps);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -293,54 +324,84 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem = *tmem_slot;
+  // Ring bookkeeping: every role walks the same sequence of (item, K step), so
+  // per-slot phase bits (bit s = parity of slot s's next use) agree across roles.
 
   if (RAW_TMA && warp == kRawWarp) {
     // ---------------- TMA producer: packed weights ----------------
     if (lane == 0) {
       const uint64_t pol = l2_evict_first_policy();  // weights are read once: keep the token tiles in L2
-      for (int ks = 0; ks < nk; ++ks) {
-        const int s = ks % kStagesRaw;
-        const uint32_t ph = (ks / kStagesRaw) & 1;
-        if (!mbar_wait(&raw_empty[s], ph ^ 1u, abort_flag, P.err, kErrWaitTimeout)) break;
-        mbar_expect_tx(&raw_full[s], 2 * kRawTileBytes);
-        uint8_t* raw = smem + kOffRaw + s * 2 * kRawTileBytes;
-        tma_load_2d_hint(raw, &map_raw, ks * (kBK / 2), wrow0, &raw_full[s], pol);
-        tma_load_2d_hint(raw + kRawTileBytes, &map_raw, ks * (kBK / 2), wrow0 + P.acc1_offset, &raw_full[s], pol);
+      uint32_t g = 0;                                // packed-weight stages issued so far
+      bool ok = true;
+      for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
+        const TcItem t = tc_item(P, it);
+        for (int rs = 0; rs < nrs; ++rs, ++g) {
+          const int s = g % kStagesRaw;
+          if (!mbar_wait(&raw_empty[s], ((g / kStagesRaw) & 1) ^ 1u, abort_flag, P.err, kErrWaitTimeout)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(&raw_full[s], 2 * kRawTileBytes);
+          uint8_t* raw = smem + kOffRaw + s * 2 * kRawTileBytes;
+          tma_load_2d_hint(raw, &map_raw, rs * kRawRowBytes, t.wrow0, &raw_full[s], pol);
+          tma_load_2d_hint(raw + kRawTileBytes, &map_raw, rs * kRawRowBytes, t.wrow0 + P.acc1_offset, &raw_full[s], pol);
+        }
       }
     }
   } else if (warp == kBWarp) {
     // ---------------- TMA producer: token tiles ----------------
     if (lane == 0) {
-      const int boxes = (n_mma + kBBoxRows - 1) / kBBoxRows;
-      for (int ks = 0; ks < nk; ++ks) {
-        const int s = ks % nS;
-        const uint32_t ph = (ks / nS) & 1;
-        if (!mbar_wait(&empty[s], ph ^ 1u, abort_flag, P.err, kErrWaitTimeout)) break;
-        mbar_expect_tx(&full[s], boxes * kBBoxBytes);
-        uint8_t* b = smem + kOffB + s * kBTileBytes;
-        for (int i = 0; i < boxes; ++i) tma_load_2d(b + i * kBBoxBytes, &map_b, ks * kBK, row0 + i * kBBoxRows, &full[s]);
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
+        const TcItem t = tc_item(P, it);
+        const int boxes = (t.n_mma + kBBoxRows - 1) / kBBoxRows;
+        for (int ks = 0; ks < nk; ++ks) {
+          const int s = ks % t.nS;
+          if (!mbar_wait(&empty[s], ((ph >> s) & 1) ^ 1u, abort_flag, P.err, kErrWaitTimeout)) {
+            ok = false;
+            break;
+          }
+          ph ^= 1u << s;
+          mbar_expect_tx(&full[s], boxes * kBBoxBytes);
+          uint8_t* b = smem + kOffB + s * kBTileBytes;
+          for (int i = 0; i < boxes; ++i)
+            tma_load_2d(b + i * kBBoxBytes, &map_b, ks * kBK, t.row0 + i * kBBoxRows, &full[s]);
+        }
       }
     }
   } else if (warp == kMmaWarp || warp == mma1_warp(RAW_TMA)) {
     // ---------------- MMA issuers, one per accumulator ----------------
     if (lane == 0) {
       const int acc = warp == kMmaWarp ? 0 : 1;
-      const uint32_t idesc = idesc_f16kind(kBM, n_mma, F16 ? 0u : 1u);
-      const uint32_t d_tmem = tmem + acc * acc_cols;
-      for (int ks = 0; ks < nk; ++ks) {
-        const int s = ks % nS;
-        if (!mbar_wait(&full[s], (ks / nS) & 1, abort_flag, P.err, kErrWaitTimeout)) break;
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const uint32_t b_addr = smem_u32(smem + kOffB + s * kBTileBytes);
-        const uint32_t a_tmem = tmem + a_col0 + (s * 2 + acc) * kASlotCols;
+      uint32_t ph = 0;
+      int li = 0;  // items done by this CTA
+      bool ok = true;
+      for (int it = blockIdx.x; it < items && ok; it += gridDim.x, ++li) {
+        const TcItem t = tc_item(P, it);
+        // the epilogue of the previous item must have read the accumulators
+        if (li > 0 && !mbar_wait(acc_empty, (li - 1) & 1, abort_flag, P.err, kErrWaitTimeout)) break;
+        const uint32_t idesc = idesc_f16kind(kBM, t.n_mma, F16 ? 0u : 1u);
+        const uint32_t d_tmem = tmem + t.acc0 + acc * t.acc_cols;
+        for (int ks = 0; ks < nk; ++ks) {
+          const int s = ks % t.nS;
+          if (!mbar_wait(&full[s], (ph >> s) & 1, abort_flag, P.err, kErrWaitTimeout)) {
+            ok = false;
+            break;
+          }
+          ph ^= 1u << s;
+          asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+          const uint32_t b_addr = smem_u32(smem + kOffB + s * kBTileBytes);
+          const uint32_t a_tmem = tmem + (s * 2 + acc) * kASlotCols;
 #pragma unroll
-        for (int kk = 0; kk < kBK / 16; ++kk)
-          umma_tmem_a(d_tmem, a_tmem + kk * 8, desc_sw128(b_addr + kk * 32), idesc, (ks > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(&empty[s]);
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            umma_tmem_a(d_tmem, a_tmem + kk * 8, desc_sw128(b_addr + kk * 32), idesc, (ks > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(&empty[s]);
+        }
+        umma_commit(acc_full);
       }
-      umma_commit(acc_full);
-      // the accumulators must be final before TMEM can be freed, also on an abort
-      mbar_wait(acc_full, 0, abort_flag, P.err, kErrWaitTimeout);
+      // the last accumulators must be final before TMEM can be freed, also on an abort
+      if (li > 0) mbar_wait(acc_full, (li - 1) & 1, abort_flag, P.err, kErrWaitTimeout);
     }
   } else {
     // ---------------- dequantisers (one weight row each), then the epilogue ----------------
@@ -348,166 +409,205 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
     const int acc = dq >> 2;                 // 0: first block (gate), 1: second block (up)
     const int q = warp & 3;                  // TMEM lane quadrant this warp may access
     const int r = q * 32 + lane;             // row within the 128-row block = TMEM lane
-    const int wrow = wrow0 + acc * P.acc1_offset + r;
+    const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
     const int kpr = P.K / 32;                // scale bytes per row
-    const uint8_t* srow = P.scales + (size_t)wrow * kpr;
-    // packed bytes of this row: 32 per K step, one full 32-byte sector, read
-    // straight into registers kPrefetch steps ahead (no shared-memory staging)
-    const uint8_t* wrow_p = P.w + (size_t)wrow * (P.K / 2);
     const uint64_t pol = l2_evict_first_policy();
-    uint4 pfl[kPrefetch], pfh[kPrefetch];
-#pragma unroll
-    for (int j = 0; j < kPrefetch; ++j) {
-      if (!RAW_TMA && j < nk) {
-        pfl[j] = ldg_stream(wrow_p + 32 * j, pol);
-        pfh[j] = ldg_stream(wrow_p + 32 * j + 16, pol);
-      }
-    }
-    int s_ref = 0;
-    if (F16) {
-      uint32_t smax = 0;
-      auto max4 = [](uint32_t m, uint32_t w4) {
-        return max(m, max(max(w4 & 0xFFu, (w4 >> 8) & 0xFFu), max((w4 >> 16) & 0xFFu, w4 >> 24)));
-      };
-      if ((kpr & 15) == 0 && kpr <= 256) {
-        uint4 sv[16];  // all loads in flight at once
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          if (16 * i < kpr) sv[i] = *reinterpret_cast<const uint4*>(srow + 16 * i);
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          if (16 * i < kpr) smax = max4(max4(max4(max4(smax, sv[i].x), sv[i].y), sv[i].z), sv[i].w);
-      } else {
-        for (int i = 0; i < kpr; i += 4) smax = max4(smax, *reinterpret_cast<const uint32_t*>(srow + i));
-      }
-      s_ref = (int)smax - 13;
-      rowscale[acc * 128 + r] = pow2f(s_ref - 127);
-    }
-    // scale bytes: 16 at a time (8 K steps) when rows are 16-byte aligned, else 2 per step
-    const bool vec_scales = (kpr & 15) == 0;
-    uint4 sg_cur = make_uint4(0, 0, 0, 0), sg_next = make_uint4(0, 0, 0, 0);
-    uint32_t sc_next = 0;
-    if (vec_scales) {
-      sg_next = *reinterpret_cast<const uint4*>(srow);
-    } else {
-      sc_next = *reinterpret_cast<const uint16_t*>(srow);
-    }
+    uint32_t ph = 0;                         // A-slot phase bits
+    uint32_t g = 0;                          // packed-weight stages consumed so far (all items)
+    int li = 0;
     bool ok = true;
-    for (int ks0 = 0; ks0 < nk && ok; ks0 += kPrefetch) {
+    for (int it = blockIdx.x; it < items && ok; it += gridDim.x, ++li) {
+      const TcItem t = tc_item(P, it);
+      // a W2 tile whose second block runs past the expert's d rows (d % 256 ==
+      // 128) reads a valid row there instead (its results are not written),
+      // so that no read leaves the weight and scale tensors
+      const bool row_in = t.mb * P.block_rows + acc * P.acc1_offset + r < P.rows_per_expert;
+      const int wrow = row_in ? t.wrow0 + acc * P.acc1_offset + r : t.wrow0 + r;
+      const uint8_t* srow = P.scales + (size_t)wrow * kpr;
+      // packed bytes of this row: 32 per K step, one full 32-byte sector (W2:
+      // read straight into registers kPrefetch steps ahead)
+      const uint8_t* wrow_p = P.w + (size_t)wrow * (P.K / 2);
+      uint4 pfl[kPrefetch], pfh[kPrefetch];
 #pragma unroll
       for (int j = 0; j < kPrefetch; ++j) {
-        const int ks = ks0 + j;
-        if (ks < nk && ok) {
-          const int sa = ks % nS;
-          uint4 lo, hi;
-          if (RAW_TMA) {
-            const int s = ks % kStagesRaw;
-            if (!mbar_wait(&raw_full[s], (ks / kStagesRaw) & 1, abort_flag, P.err, kErrWaitTimeout)) {
-              ok = false;
-              continue;
-            }
-            // the tile arrives with the 32-byte swizzle: the two 16-byte halves of
-            // row r are swapped when bit 2 of r is set, which keeps both reads
-            // of a warp free of bank conflicts
-            const int sw = ((r >> 2) & 1) << 4;
-            const uint8_t* raw = smem + kOffRaw + (s * 2 + acc) * kRawTileBytes + r * 32;
-            lo = *reinterpret_cast<const uint4*>(raw + sw);
-            hi = *reinterpret_cast<const uint4*>(raw + (16 ^ sw));
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&raw_empty[s]);  // the packed bytes are in registers now
-          } else {
-            lo = pfl[j];
-            hi = pfh[j];
-            if (ks + kPrefetch < nk) {
-              pfl[j] = ldg_stream(wrow_p + 32 * (ks + kPrefetch), pol);
-              pfh[j] = ldg_stream(wrow_p + 32 * (ks + kPrefetch) + 16, pol);
-            }
-          }
-          uint32_t sc;
-          if (vec_scales) {
-            if ((ks & 7) == 0) {
-              sg_cur = sg_next;
-              if (ks + 8 < nk) sg_next = *reinterpret_cast<const uint4*>(srow + 2 * (ks + 8));
-            }
-            const uint32_t wsel = ((ks & 7) >> 1) == 0 ? sg_cur.x : ((ks & 7) >> 1) == 1 ? sg_cur.y
-                                : ((ks & 7) >> 1) == 2 ? sg_cur.z : sg_cur.w;
-            sc = (ks & 1) ? wsel >> 16 : wsel & 0xFFFFu;
-          } else {
-            sc = sc_next;
-            if (ks + 1 < nk) sc_next = *reinterpret_cast<const uint16_t*>(srow + 2 * (ks + 1));
-          }
-          const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-          if (!mbar_wait(&empty[sa], ((ks / nS) & 1) ^ 1u, abort_flag, P.err, kErrWaitTimeout)) {
-            ok = false;
-          } else {
-            const uint32_t s0 = sc & 0xFFu, s1 = (sc >> 8) & 0xFFu;
-            const uint32_t m0 = F16 ? f16x2_pow2((int)s0 - s_ref) : 0u, m1 = F16 ? f16x2_pow2((int)s1 - s_ref) : 0u;
-            uint32_t av[32];  // column j = K elements (2j, 2j+1) of this row
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              const uint32_t sb = c < 4 ? s0 : s1;
-              const uint4 v = F16 ? dequant8_f16(w[c], c < 4 ? m0 : m1) : dequant8(w[c], sb);
-              av[4 * c + 0] = v.x;
-              av[4 * c + 1] = v.y;
-              av[4 * c + 2] = v.z;
-              av[4 * c + 3] = v.w;
-            }
-            tmem_st32(tmem + ((uint32_t)(q * 32) << 16) + a_col0 + (sa * 2 + acc) * kASlotCols, av);
-            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&full[sa]);
-          }
+        if (!RAW_TMA && j < nk) {
+          pfl[j] = ldg_stream(wrow_p + 32 * j, pol);
+          pfh[j] = ldg_stream(wrow_p + 32 * j + 16, pol);
         }
       }
-    }
-    // epilogue: the two warps of a lane quadrant take alternate 32-column
-    // chunks; their column scales are fetched before the accumulators are ready
-    constexpr int kChunks = (kBN + 63) / 64;
-    const int half = dq >> 2;
-    float xs_pre[kChunks] = {};
-    if (F16) {
+      int s_ref = 0;
+      if (F16) {
+        uint32_t smax = 0;
+        auto max4 = [](uint32_t m, uint32_t w4) {
+          return max(m, max(max(w4 & 0xFFu, (w4 >> 8) & 0xFFu), max((w4 >> 16) & 0xFFu, w4 >> 24)));
+        };
+        if ((kpr & 15) == 0 && kpr <= 256) {
+          uint4 sv[16];  // all loads in flight at once
 #pragma unroll
-      for (int i = 0; i < kChunks; ++i) {
-        const int col = 32 * (2 * i + half) + lane;
-        if (col < n) xs_pre[i] = P.x_scale[row0 + col];
-      }
-    }
-    // the row scales written above must be visible to every epilogue warp
-    asm volatile("bar.sync 1, %0;" ::"r"(kDqWarps * 32) : "memory");
-    if (ok && mbar_wait(acc_full, 0, abort_flag, P.err, kErrWaitTimeout)) {
-      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      const int rr = r;                          // weight row of this thread's TMEM lane
-      const float rs0 = F16 ? rowscale[rr] : 1.f, rs1 = F16 ? rowscale[128 + rr] : 1.f;
+          for (int i = 0; i < 16; ++i)
+            if (16 * i < kpr) sv[i] = *reinterpret_cast<const uint4*>(srow + 16 * i);
 #pragma unroll
-      for (int ci = 0; ci < kChunks; ++ci) {
-        const int c0 = 32 * (2 * ci + half);
-        if (c0 >= n_mma) break;
-        float a0[32], a1[32];
-        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + c0, a0);
-        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + acc_cols + c0, a1);
-        if (F16) {
-          const float xs_l = xs_pre[ci];
-          const int i = mb * kBM + rr;
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float xs = __shfl_sync(0xFFFFFFFFu, xs_l, j);
-            if (c0 + j < n)
-              P.h_out[(size_t)(row0 + c0 + j) * P.I + i] =
-                  f32_to_bf16_rn(swiglu(a0[j] * rs0 * xs, a1[j] * rs1 * xs));
-          }
+          for (int i = 0; i < 16; ++i)
+            if (16 * i < kpr) smax = max4(max4(max4(max4(smax, sv[i].x), sv[i].y), sv[i].z), sv[i].w);
         } else {
-          const int nrow = mb * P.block_rows + rr;
+          for (int i = 0; i < kpr; i += 4) smax = max4(smax, *reinterpret_cast<const uint32_t*>(srow + i));
+        }
+        s_ref = (int)smax - 13;
+        rowscale[acc * 128 + r] = pow2f(s_ref - 127);
+      }
+      // scale bytes: 16 at a time (8 K steps) when rows are 16-byte aligned, else 2 per step
+      const bool vec_scales = (kpr & 15) == 0;
+      uint4 sg_cur = make_uint4(0, 0, 0, 0), sg_next = make_uint4(0, 0, 0, 0);
+      uint32_t sc_next = 0;
+      if (vec_scales) {
+        sg_next = *reinterpret_cast<const uint4*>(srow);
+      } else {
+        sc_next = *reinterpret_cast<const uint16_t*>(srow);
+      }
+      for (int ks0 = 0; ks0 < nk && ok; ks0 += kPrefetch) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (c0 + j < n) {
-              float* yrow = P.y_out + (size_t)(row0 + c0 + j) * P.d;
-              yrow[nrow] = a0[j];
-              if (nrow + P.acc1_offset < P.d) yrow[nrow + P.acc1_offset] = a1[j];  // last block may hold 128 rows
+        for (int j = 0; j < kPrefetch; ++j) {
+          const int ks = ks0 + j;
+          if (ks < nk && ok) {
+            const int sa = ks % t.nS;
+            uint4 lo, hi;
+            if (RAW_TMA) {
+              const int sub = ks % kRawSteps;
+              const uint32_t gs = g + ks / kRawSteps;
+              const int s = gs % kStagesRaw;
+              if (sub == 0 && !mbar_wait(&raw_full[s], (gs / kStagesRaw) & 1, abort_flag, P.err, kErrWaitTimeout)) {
+                ok = false;
+                continue;
+              }
+              const uint8_t* raw = smem + kOffRaw + (s * 2 + acc) * kRawTileBytes + r * kRawRowBytes;
+              if (kRawSteps == 1) {
+                // 32-byte swizzle: the two 16-byte halves of row r are swapped when
+                // bit 2 of r is set, which keeps both reads of a warp free of bank conflicts
+                const int sw = ((r >> 2) & 1) << 4;
+                lo = *reinterpret_cast<const uint4*>(raw + sw);
+                hi = *reinterpret_cast<const uint4*>(raw + (16 ^ sw));
+              } else {
+                // 128-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ (r mod 8)
+                lo = *reinterpret_cast<const uint4*>(raw + (((2 * sub) ^ (r & 7)) << 4));
+                hi = *reinterpret_cast<const uint4*>(raw + (((2 * sub + 1) ^ (r & 7)) << 4));
+              }
+              if (sub == kRawSteps - 1 || ks == nk - 1) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&raw_empty[s]);  // the stage's packed bytes are all in registers now
+              }
+            } else {
+              lo = pfl[j];
+              hi = pfh[j];
+              if (ks + kPrefetch < nk) {
+                pfl[j] = ldg_stream(wrow_p + 32 * (ks + kPrefetch), pol);
+                pfh[j] = ldg_stream(wrow_p + 32 * (ks + kPrefetch) + 16, pol);
+              }
+            }
+            uint32_t sc;
+            if (vec_scales) {
+              if ((ks & 7) == 0) {
+                sg_cur = sg_next;
+                if (ks + 8 < nk) sg_next = *reinterpret_cast<const uint4*>(srow + 2 * (ks + 8));
+              }
+              const uint32_t wsel = ((ks & 7) >> 1) == 0 ? sg_cur.x : ((ks & 7) >> 1) == 1 ? sg_cur.y
+                                  : ((ks & 7) >> 1) == 2 ? sg_cur.z : sg_cur.w;
+              sc = (ks & 1) ? wsel >> 16 : wsel & 0xFFFFu;
+            } else {
+              sc = sc_next;
+              if (ks + 1 < nk) sc_next = *reinterpret_cast<const uint16_t*>(srow + 2 * (ks + 1));
+            }
+            const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+            if (!mbar_wait(&empty[sa], ((ph >> sa) & 1) ^ 1u, abort_flag, P.err, kErrWaitTimeout)) {
+              ok = false;
+            } else {
+              ph ^= 1u << sa;
+              const uint32_t s0 = sc & 0xFFu, s1 = (sc >> 8) & 0xFFu;
+              const uint32_t m0 = F16 ? f16x2_pow2((int)s0 - s_ref) : 0u, m1 = F16 ? f16x2_pow2((int)s1 - s_ref) : 0u;
+              uint32_t av[32];  // column j = K elements (2j, 2j+1) of this row
+#pragma unroll
+              for (int c = 0; c < 8; ++c) {
+                const uint32_t sb = c < 4 ? s0 : s1;
+                const uint4 v = F16 ? dequant8_f16(w[c], c < 4 ? m0 : m1) : dequant8(w[c], sb);
+                av[4 * c + 0] = v.x;
+                av[4 * c + 1] = v.y;
+                av[4 * c + 2] = v.z;
+                av[4 * c + 3] = v.w;
+              }
+              tmem_st32(lane_base + (sa * 2 + acc) * kASlotCols, av);
+              asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+              asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&full[sa]);
             }
           }
         }
       }
+      g += nrs;
+      // epilogue: the two warps of a lane quadrant take alternate 32-column
+      // chunks; their column scales are fetched before the accumulators are ready
+      constexpr int kChunks = (kBN + 63) / 64;
+      const int half = dq >> 2;
+      float xs_pre[kChunks] = {};
+      if (F16) {
+#pragma unroll
+        for (int i = 0; i < kChunks; ++i) {
+          const int col = 32 * (2 * i + half) + lane;
+          if (col < t.n) xs_pre[i] = P.x_scale[t.row0 + col];
+        }
+      }
+      // the row scales written above must be visible to every epilogue warp
+      asm volatile("bar.sync 1, %0;" ::"r"(kDqWarps * 32) : "memory");
+      if (ok && mbar_wait(acc_full, li & 1, abort_flag, P.err, kErrWaitTimeout)) {
+        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        const float rs0 = F16 ? rowscale[r] : 1.f, rs1 = F16 ? rowscale[128 + r] : 1.f;
+#pragma unroll
+        for (int ci = 0; ci < kChunks; ++ci) {
+          const int c0 = 32 * (2 * ci + half);
+          if (c0 >= t.n_mma) break;
+          float a0[32], a1[32];
+          tmem_ld32(lane_base + t.acc0 + c0, a0);
+          tmem_ld32(lane_base + t.acc0 + t.acc_cols + c0, a1);
+          if (F16) {
+            const float xs_l = xs_pre[ci];
+            const int i = t.mb * kBM + r;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float xs = __shfl_sync(0xFFFFFFFFu, xs_l, j);
+              if (c0 + j < t.n)
+                P.h_out[(size_t)(t.row0 + c0 + j) * P.I + i] =
+                    f32_to_bf16_rn(swiglu(a0[j] * rs0 * xs, a1[j] * rs1 * xs));
+            }
+          } else {
+            const int nrow = t.mb * P.block_rows + r;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              if (c0 + j < t.n) {
+                float* yrow = P.y_out + (size_t)(t.row0 + c0 + j) * P.d;
+                yrow[nrow] = a0[j];
+                if (nrow + P.acc1_offset < P.d) yrow[nrow + P.acc1_offset] = a1[j];  // last block may hold 128 rows
+              }
+            }
+          }
+        }
+        // the accumulators are in registers: the next item's MMAs may overwrite them
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acc_empty);
+      } else {
+        ok = false;
+      }
+      // every dequantiser is done with this item's accumulators and row scales
+      // before any of them writes the next item's A slots (which may cover
+      // them); a failure seen by any of them stops all of them together, so
+      // that they keep meeting at the same named barriers
+      uint32_t stop;
+      asm volatile(
+          "{\n\t.reg .pred pin, pout;\n\tsetp.ne.u32 pin, %1, 0;\n\tbar.red.or.pred pout, 1, %2, pin;\n\t"
+          "selp.u32 %0, 1, 0, pout;\n}"
+          : "=r"(stop)
+          : "r"((!ok || *abort_flag) ? 1u : 0u), "r"(kDqWarps * 32)
+          : "memory");
+      if (stop) ok = false;
     }
   }
   // every warp reconverges first: lanes that skipped a lane-0 role must not
@@ -530,9 +630,12 @@ cudaError_t launch_tc(const CUtensorMap& b, const CUtensorMap& raw, const TcPara
     cudaFuncSetAttribute(tc_kernel<F16, RAW_TMA>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_tc(RAW_TMA));
     configured = true;
   }
-  const long long grid = (long long)max_tiles * P.mblocks;
-  if (grid > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-  tc_kernel<F16, RAW_TMA><<<(unsigned)grid, tc_threads(RAW_TMA), smem_tc(RAW_TMA), st>>>(b, raw, P);
+  // one CTA per SM, each looping over work items; no more CTAs than items
+  const long long most = (long long)max_tiles * P.mblocks;
+  if (most > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+  const int grid = (int)std::min<long long>(most, num_sms());
+  if (grid <= 0) return cudaSuccess;
+  tc_kernel<F16, RAW_TMA><<<grid, tc_threads(RAW_TMA), smem_tc(RAW_TMA), st>>>(b, raw, P);
   return cudaGetLastError();
 }
 
@@ -542,8 +645,8 @@ cudaError_t launch_tc_w13(const moe_fp4_dims& d, const uint8_t* w13, const uint8
                           cudaStream_t st) {
   const size_t S = (size_t)d.T * d.k;
   CUtensorMap b, raw;
-  if (!make_map_2d(&raw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w13, d.d / 2, (uint64_t)d.E * 2 * d.I, d.d / 2, kBK / 2, kBM,
-                   CU_TENSOR_MAP_SWIZZLE_32B) ||
+  if (!make_map_2d(&raw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w13, d.d / 2, (uint64_t)d.E * 2 * d.I, d.d / 2, kRawRowBytes, kBM,
+                   kRawSteps == 1 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map_2d(&b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws.x_perm, d.d, S, (uint64_t)d.d * 2, kBK, kBBoxRows,
                    CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
@@ -573,8 +676,8 @@ cudaError_t launch_tc_w2(const moe_fp4_dims& d, const uint8_t* w2, const uint8_t
 #endif
   CUtensorMap b, raw;
   if ((MOE_TC_W2_RAW_TMA &&
-       !make_map_2d(&raw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w2, d.I / 2, (uint64_t)d.E * d.d, d.I / 2, kBK / 2, kBM,
-                    CU_TENSOR_MAP_SWIZZLE_32B)) ||
+       !make_map_2d(&raw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w2, d.I / 2, (uint64_t)d.E * d.d, d.I / 2, kRawRowBytes, kBM,
+                    kRawSteps == 1 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_128B)) ||
       !make_map_2d(&b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ws.h, d.I, S, (uint64_t)d.I * 2, kBK, kBBoxRows,
                    CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
