@@ -53,8 +53,10 @@ bool layout_workspace(const moe_fp4_dims& d, void* base, bool with_staging, Work
   ws->slot_pos = (int32_t*)take(S * sizeof(int32_t));
   ws->gemv_chunks = (int4*)take((size_t)ws->max_gemv_chunks * sizeof(int4));
   ws->tc_tiles = (int4*)take((size_t)ws->max_tc_tiles * sizeof(int4));
-  ws->x_perm = (uint16_t*)take(S * d.d * sizeof(uint16_t));
+  ws->x_perm = (uint16_t*)take(S * (size_t)(d.d > d.I ? d.d : d.I) * sizeof(uint16_t));
   ws->x_scale = (float*)take(S * sizeof(float));
+  ws->h16 = ws->x_perm;
+  ws->h_scale = ws->x_scale;
   ws->h = (uint16_t*)take(S * d.I * sizeof(uint16_t));
   ws->y = (float*)take(S * d.d * sizeof(float));
   if (with_staging) {
@@ -109,6 +111,7 @@ int run_forward(const moe_fp4_dims& d, const void* x, const float* logits, const
     mark(2);
     if (e == cudaSuccess) e = launch_tc_w13(d, w13, w13s, ws, st);
     mark(3);
+    if (e == cudaSuccess) e = launch_h_f16(d, ws, st);  // counted in the W2 stage
     if (e == cudaSuccess) e = launch_tc_w2(d, w2, w2s, ws, st);
   }
   mark(4);

@@ -145,11 +145,12 @@ w2_rows_kernel(const uint16_t* __restrict__ h, const uint8_t* __restrict__ w2,
 __global__ void __launch_bounds__(256)
 gather_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ sorted_slot, int S, int k, int d,
               uint16_t* __restrict__ x_perm, float* __restrict__ x_scale) {
+  // sorted_slot == nullptr: row r of x itself (the f16 copy of h for the tensor-core W2)
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   const int nwarps = (gridDim.x * blockDim.x) >> 5;
   const int vec = d / 8;
   for (int r = warp; r < S; r += nwarps) {
-    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(sorted_slot[r] / k) * d);
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(sorted_slot ? sorted_slot[r] / k : r) * d);
     uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)r * d);
     uint32_t emax = 1;
     for (int v = lane; v < vec; v += 32) {
@@ -221,6 +222,13 @@ cudaError_t launch_gather(const moe_fp4_dims& d, const uint16_t* x, const Worksp
   int blocks = (S + 7) / 8;
   if (blocks > num_sms() * 16) blocks = num_sms() * 16;
   gather_kernel<<<blocks, 256, 0, st>>>(x, ws.sorted_slot, S, d.k, d.d, ws.x_perm, ws.x_scale);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_h_f16(const moe_fp4_dims& d, const Workspace& ws, cudaStream_t st) {
+  const int S = d.T * d.k;
+  const int blocks = (S + 7) / 8 < num_sms() * 16 ? (S + 7) / 8 : num_sms() * 16;
+  gather_kernel<<<blocks, 256, 0, st>>>(ws.h, nullptr, S, 1, d.I, ws.h16, ws.h_scale);
   return cudaGetLastError();
 }
 

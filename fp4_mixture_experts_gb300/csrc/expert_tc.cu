@@ -4,16 +4,18 @@
 // operand (128 rows per accumulator) and the expert's token rows the N
 // operand (up to 192 per tile), so an expert with few rows wastes little of
 // the MMA ("low-M utilisation" is a limit the DeepSeek-V4-Flash-on-gfx90a
-// paper names).  One CTA computes two 128 x N accumulators that share the
+// paper names).  A work item computes two 128 x N accumulators that share the
 // token tile: gate and up rows of W13 (so SwiGLU fuses into the epilogue), or
-// two adjacent 128-row blocks of W2.
+// two adjacent 128-row blocks of W2.  The kernel is persistent: one CTA per
+// SM loops over the items.
 //
 // Warp roles, per 64-wide K step (one stage of a 2- to 4-deep ring):
 //   warp 9      TMA producer of the token tile (up to 192 rows in 64-row
 //               boxes, 128-byte swizzle; mostly L2 hits, shared by the CTAs
 //               of one expert)
-//   warp 10     (W13) TMA producer of the packed weights, 6-deep ring of
-//               128 rows x 32 bytes per accumulator, 32-byte swizzle
+//   warp 10     TMA producer of the packed weights, 2-deep ring of
+//               128 rows x 128 bytes (4 K steps) per accumulator, 128-byte
+//               swizzle
 //   warp 0 and the last warp
 //               MMA issuers, one per accumulator: 4 tcgen05.mma.kind::f16
 //               (M=128, N=tile, K=16) per K step each, fp32 accumulators in
@@ -21,26 +23,25 @@
 //               long as it runs, and so do its barrier wait and commit; with
 //               two issuers one of them is always feeding the tensor pipe
 //               while the other synchronises.  Warp 0 also owns TMEM
-//               (512 columns: both accumulators, then the A ring).
+//               (512 columns: the A ring, then both accumulators).
 //   warps 1..8  dequantisers, one thread per weight row: the row's 32 packed
-//               bytes per K step come from the TMA ring (W13) or straight from
-//               global memory 4 steps ahead (W2); E2M1 pairs are decoded by
-//               cvt.rn.f16x2.e2m1x2 and scaled exactly by a power of two
-//               (mul.f16x2 for W13, mul.bf16x2 after a bf16 re-encoding for
-//               W2) and written to the stage's A slot in TMEM with tcgen05.st
-//               (lane = weight row), so that the MMA reads its A operand from
-//               tensor memory; then the epilogue (tcgen05.ld, SwiGLU + bf16
-//               rounding of h, or y)
+//               bytes per K step come from the TMA ring; E2M1 pairs are decoded by
+//               cvt.rn.f16x2.e2m1x2, scaled exactly by a power of two
+//               (mul.f16x2) and written to the stage's A slot in TMEM with
+//               tcgen05.st (lane = weight row), so that the MMA reads its A
+//               operand from tensor memory; then the epilogue (tcgen05.ld,
+//               SwiGLU + bf16 rounding of h, or y)
 // A stage is full once the token tile has landed and all 8 dequantisers have
 // written their A slots (one mbarrier), and empty once both issuers' MMAs on
 // it have completed (one mbarrier, two tcgen05.commit arrivals).
 // Weights are dequantised exactly (an E2M1 value times a power of two has
 // 2 significant bits), so the MMA multiplies exact products and accumulates
-// them in fp32.  W13 runs on f16 operands: the weight row is scaled by
-// 2^(s - s_ref) (exact within 36 binades of the row's largest scale) and the
-// activation row by the gather's power of two; both factors come back in the
-// epilogue.  Every mbarrier wait is bounded; a timeout sets the error word
-// and an abort flag that releases the other roles, and TMEM is always freed.
+// them in fp32.  Operands are f16: the weight row is scaled by 2^(s - s_ref)
+// (exact within 36 binades of the row's largest scale) and each token row
+// (x for W13; the f16 copy of h for W2) by a power of two of its own; both
+// factors come back in the epilogue.  Every mbarrier wait is bounded; a
+// timeout sets the error word and an abort flag that releases the other
+// roles, and TMEM is always freed.
 #include <cuda.h>
 
 #include <algorithm>
@@ -59,21 +60,21 @@ constexpr int kBN = kTcTileN;            // token rows per tile (<= 192: TMEM ho
 #define MOE_TC_STAGES 4
 #endif
 constexpr int kStages = MOE_TC_STAGES;   // most ring stages (token tile + A slots); TMEM may allow fewer
-#ifndef MOE_TC_PREFETCH
-#define MOE_TC_PREFETCH 4
-#endif
-constexpr int kPrefetch = MOE_TC_PREFETCH;    // K steps of packed weights each dequantiser keeps in flight (W2)
 constexpr int kDqWarps = 8;
+#ifndef MOE_TC_DQ_UNROLL
+#define MOE_TC_DQ_UNROLL 4
+#endif
+constexpr int kDqUnroll = MOE_TC_DQ_UNROLL;     // K steps of the dequantiser loop unrolled together
 constexpr int kMmaWarp = 0;                      // TMEM allocator, MMA issuer of accumulator 0
 constexpr int kFirstDqWarp = 1;                  // dequantisers 1..8, then the epilogue
 constexpr int kBWarp = kFirstDqWarp + kDqWarps;  // token-tile TMA producer
-constexpr int kRawWarp = kBWarp + 1;             // packed-weight TMA producer (RAW_TMA only)
-__host__ __device__ constexpr int mma1_warp(bool raw_tma) { return raw_tma ? kRawWarp + 1 : kBWarp + 1; }
-__host__ __device__ constexpr int tc_threads(bool raw_tma) { return (mma1_warp(raw_tma) + 1) * 32; }
+constexpr int kRawWarp = kBWarp + 1;             // packed-weight TMA producer
+constexpr int kMma1Warp = kRawWarp + 1;          // MMA issuer of accumulator 1
+constexpr int kTcThreads = (kMma1Warp + 1) * 32;
 #ifndef MOE_TC_STAGES_RAW
 #define MOE_TC_STAGES_RAW 2
 #endif
-constexpr int kStagesRaw = MOE_TC_STAGES_RAW;    // packed-weight ring depth (RAW_TMA only)
+constexpr int kStagesRaw = MOE_TC_STAGES_RAW;    // packed-weight ring depth
 #ifndef MOE_TC_RAW_STEPS
 #define MOE_TC_RAW_STEPS 4
 #endif
@@ -83,7 +84,7 @@ constexpr int kRawRowBytes = kRawSteps * kBK / 2;
 // TMEM columns, per tile of n token rows (n_acc = n rounded up to 32):
 // accumulator 0 at [0, n_acc), accumulator 1 at [n_acc, 2 n_acc), and the
 // A slots in the rest: per (stage, acc) a 128-lane x 32-column slot holding
-// 64 K values of each row as f16/bf16 pairs.  Narrower tiles leave room for
+// 64 K values of each row as f16 pairs.  Narrower tiles leave room for
 // more stages (2 at n = 192, 3 at 160, 4 at 128).
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kASlotCols = kBK / 2;
@@ -95,12 +96,12 @@ constexpr int kBBoxBytes = kBBoxRows * kBK * 2;   // 8 KB
 constexpr int kBTileBytes = (kBN + kBBoxRows - 1) / kBBoxRows * kBBoxBytes;  // whole 64-row boxes
 constexpr int kRawTileBytes = kBM * kRawRowBytes;  // packed tile of one accumulator's 128 rows
 constexpr int kOffB = 0;                                       // [stage]
-constexpr int kOffRaw = kOffB + kStages * kBTileBytes;         // [stage][acc] (RAW_TMA only)
-__host__ __device__ constexpr int off_rowscale(bool raw_tma) { return kOffRaw + (raw_tma ? kStagesRaw * 2 * kRawTileBytes : 0); }
-__host__ __device__ constexpr int off_bar(bool raw_tma) { return off_rowscale(raw_tma) + 2 * kBM * 4; }
-__host__ __device__ constexpr int smem_tc(bool raw_tma) { return off_bar(raw_tma) + 512 + 1024; }  // + barriers, 1 KB alignment slack
+constexpr int kOffRaw = kOffB + kStages * kBTileBytes;         // [stage][acc]
+constexpr int kOffRowscale = kOffRaw + kStagesRaw * 2 * kRawTileBytes;
+constexpr int kOffBar = kOffRowscale + 2 * kBM * 4;
+constexpr int kSmemTc = kOffBar + 512 + 1024;  // + barriers, 1 KB alignment slack
 static_assert((2 * kStagesRaw + 2 * kStages + 2) * 8 + 8 <= 512, "barrier area exceeded");
-static_assert(smem_tc(true) <= 227 * 1024, "shared memory of the tensor-core kernel exceeds 227 KB");
+static_assert(kSmemTc <= 227 * 1024, "shared memory of the tensor-core kernel exceeds 227 KB");
 static_assert(kBTileBytes % 1024 == 0, "token slots must stay 1 KB aligned for the 128-byte swizzle");
 
 struct TcParams {
@@ -193,47 +194,6 @@ __device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, float (&va
   }
 }
 
-// E8M0 byte s -> the bf16x2 factor (m, m) that turns the shifted bf16 pattern
-// of an E2M1 value (its value times 2^-112) into value * 2^(s-127): m = 2^(s-15)
-// for s <= 142; larger s take two factors (2^112, then 2^(s-127)).
-__device__ __forceinline__ uint32_t bf16x2_pow2(int e_unbiased) {
-  const uint32_t b = (uint32_t)(e_unbiased + 127) << 7;
-  return b | (b << 16);
-}
-
-__device__ __forceinline__ uint32_t bf16x2_mul(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-
-// 4 packed bytes (8 E2M1 codes, K ascending) -> 8 exact bf16 values scaled by 2^(s-127)
-__device__ __forceinline__ uint4 dequant8(uint32_t packed, uint32_t s) {
-  uint32_t o[4];
-  const bool big = s > 142;
-  const uint32_t m1 = big ? bf16x2_pow2(112) : bf16x2_pow2((int)s - 15);
-  const uint32_t m2 = bf16x2_pow2((int)s - 127);
-#pragma unroll
-  for (int b = 0; b < 4; ++b) {
-    const uint32_t h2 = e2m1x2_to_f16x2((packed >> (8 * b)) & 0xFFu);
-    // f16 -> bf16 bit pattern of value * 2^-112 (exponent and mantissa shift, sign kept)
-    uint32_t v = ((h2 >> 3) & 0x0FFF0FFFu) | (h2 & 0x80008000u);
-    v = bf16x2_mul(v, m1);
-    if (big) v = bf16x2_mul(v, m2);
-    o[b] = v;
-  }
-  return make_uint4(o[0], o[1], o[2], o[3]);
-}
-
-// 16-byte streaming load: read once, no L1 allocation, evict-first in L2
-__device__ __forceinline__ uint4 ldg_stream(const uint8_t* p, uint64_t pol) {
-  uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p), "l"(pol));
-  return r;
-}
-
 __device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
@@ -284,18 +244,18 @@ __device__ __forceinline__ TcItem tc_item(const TcParams& P, int item) {
 // ... (items are (tile, m-block) pairs, tile-major, so neighbouring CTAs share
 // token tiles in L2).  The rings run on across items, so the producers load
 // the next item's weights and token rows while the current one is finishing;
-// TMEM is allocated once.  F16 (W13): operands f16, weight rows scaled by
-// 2^(s - s_ref(row)) with s_ref = (largest E8M0 of the row) - 13, activations
-// by the per-row power of two of the gather; both undone in the epilogue (per
-// TMEM lane and column), then SwiGLU.  Otherwise (W2): operands bf16
-// (weights exactly 2^(s-127) * code, h as written), epilogue writes fp32 y.
-template <bool F16, bool RAW_TMA>
-__global__ void __launch_bounds__(tc_threads(RAW_TMA), 1)
+// TMEM is allocated once.  Operands are f16: weight rows scaled by
+// 2^(s - s_ref(row)) with s_ref = (largest E8M0 of the row) - 13, token rows
+// (x for W13, h for W2) by a per-row power of two; both are undone in the
+// epilogue (per TMEM lane and column), then SwiGLU and bf16 h (W13) or fp32 y
+// (W2).
+template <bool W13>
+__global__ void __launch_bounds__(kTcThreads, 1)
 tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_raw, const TcParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* rowscale = reinterpret_cast<float*>(smem + off_rowscale(RAW_TMA));  // [2][128]
-  uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem + off_bar(RAW_TMA));
+  float* rowscale = reinterpret_cast<float*>(smem + kOffRowscale);  // [2][128]
+  uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint64_t* raw_empty = raw_full + kStagesRaw;
   uint64_t* full = raw_empty + kStagesRaw;    // [stage]: token tile landed and both A slots written
   uint64_t* empty = full + kStages;           // [stage]: the MMAs of both accumulators on it completed
@@ -311,11 +271,9 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    if (RAW_TMA) {
-      for (int s = 0; s < kStagesRaw; ++s) {
-        mbar_init(&raw_full[s], 1);
-        mbar_init(&raw_empty[s], kDqWarps);
-      }
+    for (int s = 0; s < kStagesRaw; ++s) {
+      mbar_init(&raw_full[s], 1);
+      mbar_init(&raw_empty[s], kDqWarps);
     }
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], kDqWarps + 1);  // the dequantisers and the token producer's expect_tx
@@ -339,7 +297,7 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
   // Ring bookkeeping: every role walks the same sequence of (item, K step), so
   // per-slot phase bits (bit s = parity of slot s's next use) agree across roles.
 
-  if (RAW_TMA && warp == kRawWarp) {
+  if (warp == kRawWarp) {
     // ---------------- TMA producer: packed weights ----------------
     if (lane == 0) {
       const uint64_t pol = l2_evict_first_policy();  // weights are read once: keep the token tiles in L2
@@ -382,7 +340,7 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
         }
       }
     }
-  } else if (warp == kMmaWarp || warp == mma1_warp(RAW_TMA)) {
+  } else if (warp == kMmaWarp || warp == kMma1Warp) {
     // ---------------- MMA issuers, one per accumulator ----------------
     if (lane == 0) {
       const int acc = warp == kMmaWarp ? 0 : 1;
@@ -393,7 +351,7 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
         const TcItem t = tc_item(P, it);
         // the epilogue of the previous item must have read the accumulators
         if (li > 0 && !mbar_wait(acc_empty, (li - 1) & 1, abort_flag, P.err, kErrWaitTimeout)) break;
-        const uint32_t idesc = idesc_f16kind(kBM, t.n_mma, F16 ? 0u : 1u);
+        const uint32_t idesc = idesc_f16kind(kBM, t.n_mma, 0u);
         const uint32_t d_tmem = tmem + t.acc0 + acc * t.acc_cols;
         for (int ks = 0; ks < nk; ++ks) {
           const int s = ks % t.nS;
@@ -423,7 +381,6 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
     const int r = q * 32 + lane;             // row within the 128-row block = TMEM lane
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
     const int kpr = P.K / 32;                // scale bytes per row
-    const uint64_t pol = l2_evict_first_policy();
     uint32_t ph = 0;                         // A-slot phase bits
     uint32_t g = 0;                          // packed-weight stages consumed so far (all items)
     int li = 0;
@@ -436,31 +393,23 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
       const bool row_in = t.mb * P.block_rows + acc * P.acc1_offset + r < P.rows_per_expert;
       const int wrow = row_in ? t.wrow0 + acc * P.acc1_offset + r : t.wrow0 + r;
       const uint8_t* srow = P.scales + (size_t)wrow * kpr;
-      // packed bytes of this row: 32 per K step, one full 32-byte sector (W2:
-      // read straight into registers kPrefetch steps ahead)
-      const uint8_t* wrow_p = P.w + (size_t)wrow * (P.K / 2);
-      uint4 pfl[kPrefetch], pfh[kPrefetch];
-#pragma unroll
-      for (int j = 0; j < kPrefetch; ++j) {
-        if (!RAW_TMA && j < nk) {
-          pfl[j] = ldg_stream(wrow_p + 32 * j, pol);
-          pfh[j] = ldg_stream(wrow_p + 32 * j + 16, pol);
-        }
-      }
       int s_ref = 0;
-      if (F16) {
+      {
         uint32_t smax = 0;
         auto max4 = [](uint32_t m, uint32_t w4) {
           return max(m, max(max(w4 & 0xFFu, (w4 >> 8) & 0xFFu), max((w4 >> 16) & 0xFFu, w4 >> 24)));
         };
-        if ((kpr & 15) == 0 && kpr <= 256) {
-          uint4 sv[16];  // all loads in flight at once
+        if ((kpr & 15) == 0) {
+          constexpr int kSv = 16;  // 16-byte loads in flight at a time
+          for (int i0 = 0; i0 < kpr; i0 += 16 * kSv) {
+            uint4 sv[kSv];
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if (16 * i < kpr) sv[i] = *reinterpret_cast<const uint4*>(srow + 16 * i);
+            for (int i = 0; i < kSv; ++i)
+              if (i0 + 16 * i < kpr) sv[i] = *reinterpret_cast<const uint4*>(srow + i0 + 16 * i);
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if (16 * i < kpr) smax = max4(max4(max4(max4(smax, sv[i].x), sv[i].y), sv[i].z), sv[i].w);
+            for (int i = 0; i < kSv; ++i)
+              if (i0 + 16 * i < kpr) smax = max4(max4(max4(max4(smax, sv[i].x), sv[i].y), sv[i].z), sv[i].w);
+          }
         } else {
           for (int i = 0; i < kpr; i += 4) smax = max4(smax, *reinterpret_cast<const uint32_t*>(srow + i));
         }
@@ -476,82 +425,69 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
       } else {
         sc_next = *reinterpret_cast<const uint16_t*>(srow);
       }
-      for (int ks0 = 0; ks0 < nk && ok; ks0 += kPrefetch) {
-#pragma unroll
-        for (int j = 0; j < kPrefetch; ++j) {
-          const int ks = ks0 + j;
-          if (ks < nk && ok) {
-            const int sa = ks % t.nS;
-            uint4 lo, hi;
-            if (RAW_TMA) {
-              const int sub = ks % kRawSteps;
-              const uint32_t gs = g + ks / kRawSteps;
-              const int s = gs % kStagesRaw;
-              if (sub == 0 && !mbar_wait(&raw_full[s], (gs / kStagesRaw) & 1, abort_flag, P.err, kErrWaitTimeout)) {
-                ok = false;
-                continue;
-              }
-              const uint8_t* raw = smem + kOffRaw + (s * 2 + acc) * kRawTileBytes + r * kRawRowBytes;
-              if (kRawSteps == 1) {
-                // 32-byte swizzle: the two 16-byte halves of row r are swapped when
-                // bit 2 of r is set, which keeps both reads of a warp free of bank conflicts
-                const int sw = ((r >> 2) & 1) << 4;
-                lo = *reinterpret_cast<const uint4*>(raw + sw);
-                hi = *reinterpret_cast<const uint4*>(raw + (16 ^ sw));
-              } else {
-                // 128-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ (r mod 8)
-                lo = *reinterpret_cast<const uint4*>(raw + (((2 * sub) ^ (r & 7)) << 4));
-                hi = *reinterpret_cast<const uint4*>(raw + (((2 * sub + 1) ^ (r & 7)) << 4));
-              }
-              if (sub == kRawSteps - 1 || ks == nk - 1) {
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&raw_empty[s]);  // the stage's packed bytes are all in registers now
-              }
-            } else {
-              lo = pfl[j];
-              hi = pfh[j];
-              if (ks + kPrefetch < nk) {
-                pfl[j] = ldg_stream(wrow_p + 32 * (ks + kPrefetch), pol);
-                pfh[j] = ldg_stream(wrow_p + 32 * (ks + kPrefetch) + 16, pol);
-              }
-            }
-            uint32_t sc;
-            if (vec_scales) {
-              if ((ks & 7) == 0) {
-                sg_cur = sg_next;
-                if (ks + 8 < nk) sg_next = *reinterpret_cast<const uint4*>(srow + 2 * (ks + 8));
-              }
-              const uint32_t wsel = ((ks & 7) >> 1) == 0 ? sg_cur.x : ((ks & 7) >> 1) == 1 ? sg_cur.y
-                                  : ((ks & 7) >> 1) == 2 ? sg_cur.z : sg_cur.w;
-              sc = (ks & 1) ? wsel >> 16 : wsel & 0xFFFFu;
-            } else {
-              sc = sc_next;
-              if (ks + 1 < nk) sc_next = *reinterpret_cast<const uint16_t*>(srow + 2 * (ks + 1));
-            }
-            const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-            if (!mbar_wait(&empty[sa], ((ph >> sa) & 1) ^ 1u, abort_flag, P.err, kErrWaitTimeout)) {
-              ok = false;
-            } else {
-              ph ^= 1u << sa;
-              const uint32_t s0 = sc & 0xFFu, s1 = (sc >> 8) & 0xFFu;
-              const uint32_t m0 = F16 ? f16x2_pow2((int)s0 - s_ref) : 0u, m1 = F16 ? f16x2_pow2((int)s1 - s_ref) : 0u;
-              uint32_t av[32];  // column j = K elements (2j, 2j+1) of this row
-#pragma unroll
-              for (int c = 0; c < 8; ++c) {
-                const uint32_t sb = c < 4 ? s0 : s1;
-                const uint4 v = F16 ? dequant8_f16(w[c], c < 4 ? m0 : m1) : dequant8(w[c], sb);
-                av[4 * c + 0] = v.x;
-                av[4 * c + 1] = v.y;
-                av[4 * c + 2] = v.z;
-                av[4 * c + 3] = v.w;
-              }
-              tmem_st32(lane_base + (sa * 2 + acc) * kASlotCols, av);
-              asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-              asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-              __syncwarp();
-              if (lane == 0) mbar_arrive(&full[sa]);
-            }
+#pragma unroll kDqUnroll
+      for (int ks = 0; ks < nk && ok; ++ks) {
+        const int sa = ks % t.nS;
+        uint4 lo, hi;
+        {
+          const int sub = ks % kRawSteps;
+          const uint32_t gs = g + ks / kRawSteps;
+          const int s = gs % kStagesRaw;
+          if (sub == 0 && !mbar_wait(&raw_full[s], (gs / kStagesRaw) & 1, abort_flag, P.err, kErrWaitTimeout)) {
+            ok = false;
+            break;
           }
+          const uint8_t* raw = smem + kOffRaw + (s * 2 + acc) * kRawTileBytes + r * kRawRowBytes;
+          if (kRawSteps == 1) {
+            // 32-byte swizzle: the two 16-byte halves of row r are swapped when
+            // bit 2 of r is set, which keeps both reads of a warp free of bank conflicts
+            const int sw = ((r >> 2) & 1) << 4;
+            lo = *reinterpret_cast<const uint4*>(raw + sw);
+            hi = *reinterpret_cast<const uint4*>(raw + (16 ^ sw));
+          } else {
+            // 128-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ (r mod 8)
+            lo = *reinterpret_cast<const uint4*>(raw + (((2 * sub) ^ (r & 7)) << 4));
+            hi = *reinterpret_cast<const uint4*>(raw + (((2 * sub + 1) ^ (r & 7)) << 4));
+          }
+          if (sub == kRawSteps - 1 || ks == nk - 1) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&raw_empty[s]);  // the stage's packed bytes are all in registers now
+          }
+        }
+        uint32_t sc;
+        if (vec_scales) {
+          if ((ks & 7) == 0) {
+            sg_cur = sg_next;
+            if (ks + 8 < nk) sg_next = *reinterpret_cast<const uint4*>(srow + 2 * (ks + 8));
+          }
+          const uint32_t wsel = ((ks & 7) >> 1) == 0 ? sg_cur.x : ((ks & 7) >> 1) == 1 ? sg_cur.y
+                              : ((ks & 7) >> 1) == 2 ? sg_cur.z : sg_cur.w;
+          sc = (ks & 1) ? wsel >> 16 : wsel & 0xFFFFu;
+        } else {
+          sc = sc_next;
+          if (ks + 1 < nk) sc_next = *reinterpret_cast<const uint16_t*>(srow + 2 * (ks + 1));
+        }
+        const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+        if (!mbar_wait(&empty[sa], ((ph >> sa) & 1) ^ 1u, abort_flag, P.err, kErrWaitTimeout)) {
+          ok = false;
+        } else {
+          ph ^= 1u << sa;
+          const uint32_t s0 = sc & 0xFFu, s1 = (sc >> 8) & 0xFFu;
+          const uint32_t m0 = f16x2_pow2((int)s0 - s_ref), m1 = f16x2_pow2((int)s1 - s_ref);
+          uint32_t av[32];  // column j = K elements (2j, 2j+1) of this row
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 v = dequant8_f16(w[c], c < 4 ? m0 : m1);
+            av[4 * c + 0] = v.x;
+            av[4 * c + 1] = v.y;
+            av[4 * c + 2] = v.z;
+            av[4 * c + 3] = v.w;
+          }
+          tmem_st32(lane_base + (sa * 2 + acc) * kASlotCols, av);
+          asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+          asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&full[sa]);
         }
       }
       g += nrs;
@@ -560,7 +496,7 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
       constexpr int kChunks = (kBN + 63) / 64;
       const int half = dq >> 2;
       float xs_pre[kChunks] = {};
-      if (F16) {
+      {
 #pragma unroll
         for (int i = 0; i < kChunks; ++i) {
           const int col = 32 * (2 * i + half) + lane;
@@ -571,15 +507,15 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
       asm volatile("bar.sync 1, %0;" ::"r"(kDqWarps * 32) : "memory");
       if (ok && mbar_wait(acc_full, li & 1, abort_flag, P.err, kErrWaitTimeout)) {
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const float rs0 = F16 ? rowscale[r] : 1.f, rs1 = F16 ? rowscale[128 + r] : 1.f;
+        const float rs0 = rowscale[r], rs1 = rowscale[128 + r];
 #pragma unroll
         for (int ci = 0; ci < kChunks; ++ci) {
           const int c0 = 32 * (2 * ci + half);
           if (c0 >= t.n_mma) break;
           float a0[32], a1[32];
           tmem_ld32x2(lane_base + t.acc0 + c0, lane_base + t.acc0 + t.acc_cols + c0, a0, a1);
-          if (F16) {
-            const float xs_l = xs_pre[ci];
+          const float xs_l = xs_pre[ci];
+          if (W13) {
             const int i = t.mb * kBM + r;
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
@@ -592,10 +528,11 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
             const int nrow = t.mb * P.block_rows + r;
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
+              const float xs = __shfl_sync(0xFFFFFFFFu, xs_l, j);
               if (c0 + j < t.n) {
                 float* yrow = P.y_out + (size_t)(t.row0 + c0 + j) * P.d;
-                yrow[nrow] = a0[j];
-                if (nrow + P.acc1_offset < P.d) yrow[nrow + P.acc1_offset] = a1[j];  // last block may hold 128 rows
+                yrow[nrow] = a0[j] * rs0 * xs;
+                if (nrow + P.acc1_offset < P.d) yrow[nrow + P.acc1_offset] = a1[j] * rs1 * xs;  // last block may hold 128 rows
               }
             }
           }
@@ -634,11 +571,11 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
   }
 }
 
-template <bool F16, bool RAW_TMA>
+template <bool W13>
 cudaError_t launch_tc(const CUtensorMap& b, const CUtensorMap& raw, const TcParams& P, int max_tiles, cudaStream_t st) {
   static bool configured = false;
   if (!configured) {
-    cudaFuncSetAttribute(tc_kernel<F16, RAW_TMA>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_tc(RAW_TMA));
+    cudaFuncSetAttribute(tc_kernel<W13>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTc);
     configured = true;
   }
   // one CTA per SM, each looping over work items; no more CTAs than items
@@ -646,7 +583,7 @@ cudaError_t launch_tc(const CUtensorMap& b, const CUtensorMap& raw, const TcPara
   if (most > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   const int grid = (int)std::min<long long>(most, num_sms());
   if (grid <= 0) return cudaSuccess;
-  tc_kernel<F16, RAW_TMA><<<grid, tc_threads(RAW_TMA), smem_tc(RAW_TMA), st>>>(b, raw, P);
+  tc_kernel<W13><<<grid, kTcThreads, kSmemTc, st>>>(b, raw, P);
   return cudaGetLastError();
 }
 
@@ -676,20 +613,16 @@ cudaError_t launch_tc_w13(const moe_fp4_dims& d, const uint8_t* w13, const uint8
   P.acc1_offset = d.I;
   P.I = d.I;
   P.d = d.d;
-  return launch_tc<true, true>(b, raw, P, ws.max_tc_tiles, st);
+  return launch_tc<true>(b, raw, P, ws.max_tc_tiles, st);
 }
 
 cudaError_t launch_tc_w2(const moe_fp4_dims& d, const uint8_t* w2, const uint8_t* w2s, const Workspace& ws,
                          cudaStream_t st) {
   const size_t S = (size_t)d.T * d.k;
-#ifndef MOE_TC_W2_RAW_TMA
-#define MOE_TC_W2_RAW_TMA 0
-#endif
   CUtensorMap b, raw;
-  if ((MOE_TC_W2_RAW_TMA &&
-       !make_map_2d(&raw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w2, d.I / 2, (uint64_t)d.E * d.d, d.I / 2, kRawRowBytes, kBM,
-                    kRawSteps == 1 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_128B)) ||
-      !make_map_2d(&b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ws.h, d.I, S, (uint64_t)d.I * 2, kBK, kBBoxRows,
+  if (!make_map_2d(&raw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w2, d.I / 2, (uint64_t)d.E * d.d, d.I / 2, kRawRowBytes, kBM,
+                   kRawSteps == 1 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_map_2d(&b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws.h16, d.I, S, (uint64_t)d.I * 2, kBK, kBBoxRows,
                    CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   TcParams P{};
@@ -699,6 +632,7 @@ cudaError_t launch_tc_w2(const moe_fp4_dims& d, const uint8_t* w2, const uint8_t
   P.counts = ws.counts;
   P.err = ws.err;
   P.y_out = ws.y;
+  P.x_scale = ws.h_scale;
   P.K = d.I;
   P.rows_per_expert = d.d;
   P.mblocks = (d.d + 2 * kBM - 1) / (2 * kBM);  // d % 256 == 128 leaves a 128-row last block
@@ -706,8 +640,7 @@ cudaError_t launch_tc_w2(const moe_fp4_dims& d, const uint8_t* w2, const uint8_t
   P.acc1_offset = kBM;
   P.I = d.I;
   P.d = d.d;
-  if (MOE_TC_W2_RAW_TMA) return launch_tc<false, true>(b, raw, P, ws.max_tc_tiles, st);
-  return launch_tc<false, false>(b, b, P, ws.max_tc_tiles, st);  // the packed weights are read without TMA
+  return launch_tc<false>(b, raw, P, ws.max_tc_tiles, st);
 }
 
 }  // namespace moe_fp4

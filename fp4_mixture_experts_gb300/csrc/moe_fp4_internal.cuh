@@ -40,6 +40,9 @@ struct Workspace {
   uint16_t* x_perm;       // [S, d] f16, each row scaled by a power of two (tensor-core path)
   float* x_scale;         // [S]    the inverse of that power of two
   uint16_t* h;            // [S, I] bf16
+  uint16_t* h16;          // [S, I] f16 copy of h, each row scaled by a power of two (tensor-core W2);
+                          //        shares x_perm's region, which is dead once W13 has run
+  float* h_scale;         // [S]    the inverse of that power of two (shares x_scale's region)
   float* y;               // [S, d] fp32 expert outputs in sorted-row order
   // staging for the host-buffer entry point (only laid out when requested)
   uint16_t* stage_x;      // [T, d]
@@ -64,6 +67,7 @@ int num_sms();
 // ---- launchers (one per kernel family; each returns cudaGetLastError()) ----
 cudaError_t launch_route(const moe_fp4_dims& d, const float* logits, const Workspace& ws, cudaStream_t st);
 cudaError_t launch_gather(const moe_fp4_dims& d, const uint16_t* x, const Workspace& ws, cudaStream_t st);
+cudaError_t launch_h_f16(const moe_fp4_dims& d, const Workspace& ws, cudaStream_t st);
 cudaError_t launch_gemv_w13(const moe_fp4_dims& d, const uint16_t* x, const uint8_t* w13,
                             const uint8_t* w13s, const Workspace& ws, cudaStream_t st);
 cudaError_t launch_gemv_w2(const moe_fp4_dims& d, const uint8_t* w2, const uint8_t* w2s,
