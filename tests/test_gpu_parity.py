@@ -49,7 +49,7 @@ def check_routing(r, ref):
     np.testing.assert_allclose(r["topk_weights"].cpu().numpy(), ref["topk_w"], rtol=2e-6, atol=1e-7)
 
 
-def check_h(r, ref):
+def check_h(r, ref, max_flip_rate=2e-3):
     got = oracle.bf16_bits_to_f64(bf16_bits(r["h"]))
     want = ref["h"]
     mism = got != want
@@ -61,7 +61,7 @@ def check_h(r, ref):
         diff = np.abs(got[mism] - want[mism])
         ok = (diff <= ulp * 1.0001) | (diff <= 1e-5 * np.abs(want).max())
         assert ok.all(), f"h differs beyond tolerance: worst {diff[~ok].max()} at values {want[mism][~ok][:4]}"
-        assert mism.mean() < 2e-3, f"too many h flips: {mism.mean()}"
+        assert mism.mean() < max_flip_rate, f"too many h flips: {mism.mean()}"
 
 
 def full_check(moe, L, flags=0):
@@ -229,3 +229,33 @@ def test_routing_block_boundary(moe):
     """T = 32 runs the single-block routing kernel, T = 33 the three-kernel one"""
     for T in (32, 33):
         full_check(moe, make_layer(T=T, d=1024, I=1024, E=64, k=8, seed=32 + T))
+
+
+@pytest.mark.parametrize("flags", [GEMV, TC])
+def test_wide_dynamic_range(moe, flags):
+    # E8M0 exponents spread over 24 binades inside every weight row, token rows
+    # scaled by powers of two from 2^-16 to 2^16 and one all-zero token: every
+    # power-of-two rescaling on the path (weight rows against their largest
+    # block scale, x rows, h rows) must stay exact, so each token's output keeps
+    # the usual relative accuracy whatever its magnitude
+    L = make_layer(T=48, d=1024, I=1024, E=6, k=2, exp_lo=-20, exp_hi=3, seed=41)
+    rng = np.random.default_rng(41)
+    shift = rng.integers(-16, 17, size=L.T)
+    x32 = (L.x_bf16.astype(np.uint32) << 16).view(np.float32) * np.ldexp(1.0, shift)[:, None].astype(np.float32)
+    x32[5] = 0.0
+    L.x_bf16 = (x32.view(np.uint32) >> 16).astype(np.uint16)  # exact: power-of-two scaling of bf16 values
+    ref = oracle.forward(L.x_bf16, L.router_logits, L.w13, L.w13_scale, L.w2, L.w2_scale, L.k)
+    r = run_gpu(moe, L, flags)
+    check_routing(r, ref)
+    # blocks 2^23 apart in scale cancel more in the fp32 sums than the usual
+    # workloads do, so more h values sit within fp32 rounding of a bf16
+    # rounding boundary: still one ulp at most, on up to 1% of the elements
+    check_h(r, ref, max_flip_rate=1e-2)
+    got = r["out"].cpu().numpy().astype(np.float64)
+    want = ref["out"]
+    assert not got[5].any() and not want[5].any()
+    for t in range(L.T):
+        if t == 5:
+            continue
+        rel = np.linalg.norm(got[t] - want[t]) / np.linalg.norm(want[t])
+        assert rel <= 5e-3, f"token {t} (x scaled by 2^{shift[t]}): relative L2 {rel}"
