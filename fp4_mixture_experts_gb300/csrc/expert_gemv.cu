@@ -178,13 +178,16 @@ gather_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ sorted
   }
 }
 
+// out[t] = sum_j w_tj * y[slot_pos(t, j)]; block (t, c) covers columns
+// [1024 c, 1024 c + 1024) of token t, one float4 per thread, so that even a
+// decode batch of 32 tokens spreads over d / 1024 times as many blocks
 __global__ void __launch_bounds__(256)
 combine_kernel(const float* __restrict__ y, const float* __restrict__ topk_w,
                const int32_t* __restrict__ slot_pos, int T, int k, int d, float* __restrict__ out) {
   const int t = blockIdx.x;
   if (t >= T) return;
   const int vec = d / 4;
-  for (int v = threadIdx.x; v < vec; v += blockDim.x) {
+  for (int v = blockIdx.y * blockDim.x + threadIdx.x; v < vec; v += gridDim.y * blockDim.x) {
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j = 0; j < k; ++j) {
       const float w = topk_w[(size_t)t * k + j];
@@ -233,7 +236,8 @@ cudaError_t launch_h_f16(const moe_fp4_dims& d, const Workspace& ws, cudaStream_
 }
 
 cudaError_t launch_combine(const moe_fp4_dims& d, float* out, const Workspace& ws, cudaStream_t st) {
-  combine_kernel<<<d.T, 256, 0, st>>>(ws.y, ws.topk_w, ws.slot_pos, d.T, d.k, d.d, out);
+  const dim3 grid(d.T, (d.d / 4 + 255) / 256);
+  combine_kernel<<<grid, 256, 0, st>>>(ws.y, ws.topk_w, ws.slot_pos, d.T, d.k, d.d, out);
   return cudaGetLastError();
 }
 

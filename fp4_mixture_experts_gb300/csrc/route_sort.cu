@@ -9,7 +9,9 @@
 //
 // Three kernels:
 //   route_hist  one warp per token: k rounds of a warp-wide argmax over the
-//               token's E logits, softmax of the k picked, per-block counts
+//               token's E logits (two warp reductions per round: the largest
+//               key, then the lowest index holding it), softmax of the k
+//               picked, per-block counts
 //   sort_scan   one block: per-expert totals, offsets, per-block bases, the
 //               list of non-empty experts and the work lists of the expert
 //               kernels (so the host never reads a count)
@@ -37,21 +39,50 @@ __device__ __forceinline__ void topk_softmax_warp(const float* row, int E, int k
   uint32_t taken = 0;            // bit i: entry lane + 32 i already picked
   int my_id = 0;
   float my_val = 0.f;
-  for (int r = 0; r < k; ++r) {
-    unsigned long long best = 0;
+  if (E <= 256) {
+    // up to 8 entries per lane, kept in registers as unique 64-bit keys
+    // (ordered value, then the inverted index: equal values rank the lower
+    // index first); a picked or absent entry is 0
+    unsigned long long kk[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = lane + 32 * i;
+      kk[i] = e < E ? ((unsigned long long)ordered_key(row[e]) << 32) | (0xFFFFFFFFu - (uint32_t)e) : 0ull;
+    }
+    for (int r = 0; r < k; ++r) {
+      unsigned long long b = kk[0];
+#pragma unroll
+      for (int i = 1; i < 8; ++i) b = kk[i] > b ? kk[i] : b;
+      const uint32_t hi = (uint32_t)(b >> 32);
+      const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, hi);
+      const uint32_t l = __reduce_max_sync(0xFFFFFFFFu, hi == m ? (uint32_t)b : 0u);
+      const int e_star = (int)(0xFFFFFFFFu - l);
+      const int won = (e_star & 31) == lane ? (e_star >> 5) : -1;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) kk[i] = i == won ? 0ull : kk[i];
+      if (lane == r) {
+        my_id = e_star;
+        my_val = row[e_star];
+      }
+    }
+  } else for (int r = 0; r < k; ++r) {
+    // this lane's best remaining entry (the first of equal keys: lowest index)
+    uint32_t best = 0;
+    int best_e = -1;
     for (int i = 0; i < nv; ++i) {
       const int e = lane + 32 * i;
       if (e < E && !((taken >> i) & 1u)) {
-        unsigned long long key = ((unsigned long long)ordered_key(row[e]) << 32) | (0xFFFFFFFFu - (uint32_t)e);
-        best = key > best ? key : best;
+        const uint32_t key = ordered_key(row[e]);
+        if (best_e < 0 || key > best) {
+          best = key;
+          best_e = e;
+        }
       }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, best, o);
-      best = other > best ? other : best;
-    }
-    const int e_star = (int)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFu));
+    // warp-wide: the largest key, then the lowest index holding it
+    const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, best_e < 0 ? 0u : best);
+    const uint32_t cand = (best_e >= 0 && best == m) ? (uint32_t)best_e : 0xFFFFFFFFu;
+    const int e_star = (int)__reduce_min_sync(0xFFFFFFFFu, cand);
     if ((e_star & 31) == lane) taken |= 1u << (e_star >> 5);
     if (lane == r) {
       my_id = e_star;
