@@ -259,3 +259,31 @@ def test_wide_dynamic_range(moe, flags):
             continue
         rel = np.linalg.norm(got[t] - want[t]) / np.linalg.norm(want[t])
         assert rel <= 5e-3, f"token {t} (x scaled by 2^{shift[t]}): relative L2 {rel}"
+
+
+@pytest.mark.parametrize("flags", [GEMV, TC])
+def test_cuda_graph_capture_replays_bit_identical(moe, flags):
+    # the layer call allocates nothing and never waits on the host, so it can
+    # be captured in a CUDA graph; replays recompute everything from the inputs
+    L = make_layer(T=40, d=1024, I=1024, E=16, k=4, seed=42)
+    D = to_device(L)
+    ws = torch.empty(moe.workspace_bytes(L.T, L.d, L.I, L.E, L.k), dtype=torch.uint8, device="cuda")
+    out = torch.empty(L.T, L.d, dtype=torch.float32, device="cuda")
+    args = (D["x"], D["logits"], D["w13"], D["w13_scale"], D["w2"], D["w2_scale"], L.k)
+    moe.forward(*args, out=out, workspace=ws, flags=flags)
+    torch.cuda.synchronize()
+    eager = out.clone()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        moe.forward(*args, out=out, workspace=ws, flags=flags)
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        moe.forward(*args, out=out, workspace=ws, flags=flags)
+    out.zero_()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    moe.check(ws)
+    assert torch.equal(out, eager)
