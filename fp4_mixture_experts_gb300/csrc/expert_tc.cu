@@ -75,12 +75,8 @@ constexpr int kTcThreads = (kMma1Warp + 1) * 32;
 #define MOE_TC_STAGES_RAW 2
 #endif
 constexpr int kStagesRaw = MOE_TC_STAGES_RAW;    // packed-weight ring depth
-#ifndef MOE_TC_RAW_STEPS
-#define MOE_TC_RAW_STEPS 4
-#endif
-constexpr int kRawSteps = MOE_TC_RAW_STEPS;      // K steps per packed-weight stage: 1 (32-byte rows) or 4 (128-byte rows)
-static_assert(kRawSteps == 1 || kRawSteps == 4, "packed-weight stages of 1 or 4 K steps");
-constexpr int kRawRowBytes = kRawSteps * kBK / 2;
+constexpr int kRawSteps = 4;                     // K steps per packed-weight stage
+constexpr int kRawRowBytes = kRawSteps * kBK / 2; // 128 bytes of each weight row per stage (128-byte swizzle)
 // TMEM columns, per tile of n token rows (n_acc = n rounded up to 32):
 // accumulator 0 at [0, n_acc), accumulator 1 at [n_acc, 2 n_acc), and the
 // A slots in the rest: per (stage, acc) a 128-lane x 32-column slot holding
@@ -438,17 +434,10 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
             break;
           }
           const uint8_t* raw = smem + kOffRaw + (s * 2 + acc) * kRawTileBytes + r * kRawRowBytes;
-          if (kRawSteps == 1) {
-            // 32-byte swizzle: the two 16-byte halves of row r are swapped when
-            // bit 2 of r is set, which keeps both reads of a warp free of bank conflicts
-            const int sw = ((r >> 2) & 1) << 4;
-            lo = *reinterpret_cast<const uint4*>(raw + sw);
-            hi = *reinterpret_cast<const uint4*>(raw + (16 ^ sw));
-          } else {
-            // 128-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ (r mod 8)
-            lo = *reinterpret_cast<const uint4*>(raw + (((2 * sub) ^ (r & 7)) << 4));
-            hi = *reinterpret_cast<const uint4*>(raw + (((2 * sub + 1) ^ (r & 7)) << 4));
-          }
+          // 128-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ (r mod 8),
+          // so the 8 rows of a warp's quarter hit 8 different bank groups
+          lo = *reinterpret_cast<const uint4*>(raw + (((2 * sub) ^ (r & 7)) << 4));
+          hi = *reinterpret_cast<const uint4*>(raw + (((2 * sub + 1) ^ (r & 7)) << 4));
           if (sub == kRawSteps - 1 || ks == nk - 1) {
             __syncwarp();
             if (lane == 0) mbar_arrive(&raw_empty[s]);  // the stage's packed bytes are all in registers now
@@ -594,7 +583,7 @@ cudaError_t launch_tc_w13(const moe_fp4_dims& d, const uint8_t* w13, const uint8
   const size_t S = (size_t)d.T * d.k;
   CUtensorMap b, raw;
   if (!make_map_2d(&raw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w13, d.d / 2, (uint64_t)d.E * 2 * d.I, d.d / 2, kRawRowBytes, kBM,
-                   kRawSteps == 1 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_128B) ||
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map_2d(&b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws.x_perm, d.d, S, (uint64_t)d.d * 2, kBK, kBBoxRows,
                    CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
@@ -621,7 +610,7 @@ cudaError_t launch_tc_w2(const moe_fp4_dims& d, const uint8_t* w2, const uint8_t
   const size_t S = (size_t)d.T * d.k;
   CUtensorMap b, raw;
   if (!make_map_2d(&raw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w2, d.I / 2, (uint64_t)d.E * d.d, d.I / 2, kRawRowBytes, kBM,
-                   kRawSteps == 1 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_128B) ||
+                   CU_TENSOR_MAP_SWIZZLE_128B) ||
       !make_map_2d(&b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws.h16, d.I, S, (uint64_t)d.I * 2, kBK, kBBoxRows,
                    CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
