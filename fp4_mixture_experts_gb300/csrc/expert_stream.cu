@@ -14,7 +14,8 @@
 //     scaled by a power of two per token (every bf16 value within 2^31 of the
 //     row maximum is exact, smaller ones round at 2^-39 of it);
 //   - per 32-element MX block a thread loads 4 packed bytes of each of its
-//     two rows; every cvt.rn.f16x2.e2m1x2 result is directly an A-fragment
+//     two rows (one byte per register, by a 4 x u8 vector load, so no shifts
+//     are spent on the ALU pipe); every cvt.rn.f16x2.e2m1x2 result is directly an A-fragment
 //     register of mma.sync.m16n8k16 (the K order inside the block is permuted
 //     so that each thread's bytes and activations are contiguous, identically
 //     for A and B); two MMAs give the block's exact sums (f16 x f16 products
@@ -65,6 +66,17 @@ struct StreamParams {
 };
 
 __device__ __forceinline__ uint32_t e2m1x2_h2(uint32_t byte) { return e2m1x2_to_f16x2(byte); }
+
+// 4 consecutive bytes of shared memory, one per register (zero-extended):
+// one load instead of a word load and three shifts on the busy ALU pipe.  Not
+// volatile, so loads of later blocks may be scheduled early; the memory clobber
+// keeps it after the wait on the stage's full barrier.
+__device__ __forceinline__ void lds_bytes4(const uint8_t* p, uint32_t (&b)[4]) {
+  asm("ld.shared.v4.u8 {%0,%1,%2,%3}, [%4];"
+      : "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3])
+      : "r"(smem_u32(p))
+      : "memory");
+}
 
 __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1,
                                           const float (&c)[4]) {
@@ -242,18 +254,18 @@ stream_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__
         for (int bi = 0; bi < kBlkPerWarp; ++bi) {
           const int blk = kpart * kBlkPerWarp + bi;  // uniform over the warp
           const int half = blk >> 3, chunk = blk & 7;
-          const uint32_t wa = *reinterpret_cast<const uint32_t*>(pa + half * box_stride + ((chunk ^ swA_) << 4));
-          const uint32_t wb = *reinterpret_cast<const uint32_t*>(pb + half * box_stride + ((chunk ^ swB_) << 4));
+          uint32_t ba[4], bb[4];  // this thread's 4 packed bytes of rows A and B (8 codes each)
+          lds_bytes4(pa + half * box_stride + ((chunk ^ swA_) << 4), ba);
+          lds_bytes4(pb + half * box_stride + ((chunk ^ swB_) << 4), bb);
           const uint4 xf = *reinterpret_cast<const uint4*>(xk + bi * 64);
           const float zero[4] = {0.f, 0.f, 0.f, 0.f};
           float cb[4];
-          // the conversion reads the low byte of its operand (no mask needed)
-          uint32_t a[4] = {e2m1x2_h2(wa), e2m1x2_h2(wb), e2m1x2_h2(wa >> 8), e2m1x2_h2(wb >> 8)};
+          uint32_t a[4] = {e2m1x2_h2(ba[0]), e2m1x2_h2(bb[0]), e2m1x2_h2(ba[1]), e2m1x2_h2(bb[1])};
           mma_16816(cb, a, xf.x, xf.y, zero);
-          a[0] = e2m1x2_h2(wa >> 16);
-          a[1] = e2m1x2_h2(wb >> 16);
-          a[2] = e2m1x2_h2(wa >> 24);
-          a[3] = e2m1x2_h2(wb >> 24);
+          a[0] = e2m1x2_h2(ba[2]);
+          a[1] = e2m1x2_h2(bb[2]);
+          a[2] = e2m1x2_h2(ba[3]);
+          a[3] = e2m1x2_h2(bb[3]);
           mma_16816(cb, a, xf.z, xf.w, cb);
           const float fa = scale2_of(swA[bi >> 2], bi & 3), fb = scale2_of(swB[bi >> 2], bi & 3);
           acc[0] = fmaf(cb[0], fa, acc[0]);
