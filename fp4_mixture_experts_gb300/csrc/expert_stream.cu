@@ -87,15 +87,10 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
 }
 
-// Byte i (0..3) of w, an E8M0 value s, as the fp32 factor 2^(s-126) = 2 * 2^(s-127):
-// (s + 1) << 23 is a normal fp32 for every s in [0, 253] (0 needs no special
-// case); the factor 2 is taken back in the token scale.  One byte permute
-// and one integer multiply-add.
-__device__ __forceinline__ float scale2_of(uint32_t w, int i) {
-  uint32_t b;
-  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(b) : "r"(w), "r"(0x4440u + i));
-  return __uint_as_float(b * (1u << 23) + (1u << 23));
-}
+// An E8M0 byte s as the fp32 factor 2^(s-126) = 2 * 2^(s-127): (s + 1) << 23
+// is a normal fp32 for every s in [0, 253] (0 needs no special case); the
+// factor 2 is taken back in the token scale.  One integer multiply-add.
+__device__ __forceinline__ float scale2_of(uint32_t s) { return __uint_as_float(s * (1u << 23) + (1u << 23)); }
 
 // Item geometry.  W13: rows [i0, i0+64) of gate and up; W2: rows [n0, n0+128).
 template <bool W13>
@@ -243,11 +238,18 @@ stream_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__
         const uint8_t* pa = st + baseA;
         const uint8_t* pb = st + baseB;
         // this warp's blocks [kpart * kBlkPerWarp, +kBlkPerWarp) of the stage's 16
-        uint32_t swA[kBlkPerWarp / 4], swB[kBlkPerWarp / 4];
+        // the E8M0 bytes of this warp's blocks, one per register
+        uint32_t sbA[kBlkPerWarp], sbB[kBlkPerWarp];
 #pragma unroll
         for (int i = 0; i < kBlkPerWarp / 4; ++i) {
-          swA[i] = *reinterpret_cast<const uint32_t*>(st + kStageA + rowA * 16 + kpart * kBlkPerWarp + 4 * i);
-          swB[i] = *reinterpret_cast<const uint32_t*>(st + kStageA + rowB * 16 + kpart * kBlkPerWarp + 4 * i);
+          uint32_t ta[4], tb[4];
+          lds_bytes4(st + kStageA + rowA * 16 + kpart * kBlkPerWarp + 4 * i, ta);
+          lds_bytes4(st + kStageA + rowB * 16 + kpart * kBlkPerWarp + 4 * i, tb);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            sbA[4 * i + j] = ta[j];
+            sbB[4 * i + j] = tb[j];
+          }
         }
         const uint8_t* xk = xg + (size_t)ks * kKStage * 2 + kpart * kBlkPerWarp * 64;
 #pragma unroll
@@ -267,7 +269,7 @@ stream_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__
           a[2] = e2m1x2_h2(ba[3]);
           a[3] = e2m1x2_h2(bb[3]);
           mma_16816(cb, a, xf.z, xf.w, cb);
-          const float fa = scale2_of(swA[bi >> 2], bi & 3), fb = scale2_of(swB[bi >> 2], bi & 3);
+          const float fa = scale2_of(sbA[bi]), fb = scale2_of(sbB[bi]);
           acc[0] = fmaf(cb[0], fa, acc[0]);
           acc[1] = fmaf(cb[1], fa, acc[1]);
           acc[2] = fmaf(cb[2], fb, acc[2]);
