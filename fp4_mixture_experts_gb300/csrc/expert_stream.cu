@@ -8,21 +8,24 @@
 //   - one producer warp streams 128-row x 512-K stages (32 KB of packed
 //     E2M1 codes, TMA 2-D boxes with the 128-byte swizzle, plus their E8M0
 //     scales) into a shared-memory ring guarded by full/empty mbarriers;
-//   - each of 8 consumer warps owns a 16-row tile (W13: 8 gate rows and the 8
-//     matching up rows, so SwiGLU stays in-thread; W2: 16 output rows) and
-//     the full K; a chunk's token rows (up to 8) sit in shared memory as f16
-//     scaled by a power of two per token (every bf16 value within 2^31 of the
-//     row maximum is exact, smaller ones round at 2^-39 of it);
+//   - 16 consumer warps: each 16-row tile (W13: 8 gate rows and the 8
+//     matching up rows, so SwiGLU stays in-thread; W2: 16 output rows) is
+//     shared by two warps, each taking half of the stage's MX blocks; the
+//     pair adds its partial sums once per item through shared memory.  A
+//     chunk's token rows (up to 8) sit in shared memory as f16 scaled by a
+//     power of two per token (every bf16 value within 2^31 of the row maximum
+//     is exact, smaller ones round at 2^-39 of it);
 //   - per 32-element MX block a thread loads 4 packed bytes of each of its
-//     two rows (one byte per register, by a 4 x u8 vector load, so no shifts
-//     are spent on the ALU pipe); every cvt.rn.f16x2.e2m1x2 result is directly an A-fragment
-//     register of mma.sync.m16n8k16 (the K order inside the block is permuted
-//     so that each thread's bytes and activations are contiguous, identically
-//     for A and B); two MMAs give the block's exact sums (f16 x f16 products
-//     are exact, accumulation fp32), which are scaled by 2^(s-127) in fp32 and
-//     accumulated, so every E8M0 value is handled exactly;
-//   - no cross-warp reduction: the W13 epilogue applies SwiGLU and rounds h
-//     to bf16, the W2 epilogue writes fp32 y.
+//     two rows, one byte per register (a 4 x u8 vector load, so no shifts are
+//     spent on the ALU pipe); every cvt.rn.f16x2.e2m1x2 result is directly an
+//     A-fragment register of mma.sync.m16n8k16 (the K order inside the block
+//     is permuted so that each thread's bytes and activations are contiguous,
+//     identically for A and B); two MMAs give the block's exact sums (f16 x
+//     f16 products are exact, accumulation fp32), which are scaled by
+//     2^(s-127) in fp32 and accumulated, so every E8M0 value is handled
+//     exactly;
+//   - the W13 epilogue applies SwiGLU and rounds h to bf16, the W2 epilogue
+//     writes fp32 y.
 // Waits are bounded; a timeout raises the CTA abort flag, after which every
 // warp runs the same loop without waiting or computing, so all barriers are
 // still met and the kernel exits.
