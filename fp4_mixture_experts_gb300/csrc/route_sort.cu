@@ -7,16 +7,21 @@
 // of the DeepSeek-V4-Flash-on-gfx90a paper's prefill path: a stable
 // counting sort, so the permutation is unique and reproducible.
 //
-// Three kernels:
+// Three kernels for any T:
 //   route_hist  one warp per token: k rounds of a warp-wide argmax over the
 //               token's E logits (two warp reductions per round: the largest
 //               key, then the lowest index holding it), softmax of the k
 //               picked, per-block counts
-//   sort_scan   one block: per-expert totals, offsets, per-block bases, the
-//               list of non-empty experts and the work lists of the expert
-//               kernels (so the host never reads a count)
+//   sort_scan   one block: per-expert totals (several threads per expert,
+//               each summing a contiguous range of routing blocks), offsets,
+//               per-block bases, the list of non-empty experts and the work
+//               lists of the expert kernels (so the host never reads a count)
 //   scatter     one block per routing block: stable ranks by warp match,
 //               writes sorted_slot and its inverse
+// and one for T <= 32 (the decode batch): route_small, a cluster of CTAs on
+// separate SMs, one token per warp, with the sort done in CTA 0.
+#include <cooperative_groups.h>
+
 #include "moe_fp4_internal.cuh"
 
 namespace moe_fp4 {
@@ -31,7 +36,14 @@ __device__ __forceinline__ uint32_t ordered_key(float v) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Top-k of one token's E logits (staged in `row`, shared memory) by (value
+// Larger key first.
+__device__ __forceinline__ void cmpx_desc(unsigned long long& a, unsigned long long& b) {
+  const unsigned long long hi = a > b ? a : b, lo = a > b ? b : a;
+  a = hi;
+  b = lo;
+}
+
+// Top-k of one token's E logits (`row`, shared or global memory) by (value
 // desc, index asc) and the softmax over the k picked, shifted by the slot-0
 // logit with the sum in slot order.  Lane j < k returns slot j.
 __device__ __forceinline__ void topk_softmax_warp(const float* row, int E, int k, int lane, int& id, float& w) {
@@ -42,24 +54,31 @@ __device__ __forceinline__ void topk_softmax_warp(const float* row, int E, int k
   if (E <= 256) {
     // up to 8 entries per lane, kept in registers as unique 64-bit keys
     // (ordered value, then the inverted index: equal values rank the lower
-    // index first); a picked or absent entry is 0
+    // index first; an absent entry is 0), sorted once in descending order:
+    // a round compares the lanes' first keys only and the winning lane
+    // drops its first key
     unsigned long long kk[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int e = lane + 32 * i;
       kk[i] = e < E ? ((unsigned long long)ordered_key(row[e]) << 32) | (0xFFFFFFFFu - (uint32_t)e) : 0ull;
     }
+    // Batcher's odd-even merge sort of 8 keys (19 compare-exchanges)
+    cmpx_desc(kk[0], kk[2]); cmpx_desc(kk[1], kk[3]); cmpx_desc(kk[4], kk[6]); cmpx_desc(kk[5], kk[7]);
+    cmpx_desc(kk[0], kk[4]); cmpx_desc(kk[1], kk[5]); cmpx_desc(kk[2], kk[6]); cmpx_desc(kk[3], kk[7]);
+    cmpx_desc(kk[0], kk[1]); cmpx_desc(kk[2], kk[3]); cmpx_desc(kk[4], kk[5]); cmpx_desc(kk[6], kk[7]);
+    cmpx_desc(kk[2], kk[4]); cmpx_desc(kk[3], kk[5]);
+    cmpx_desc(kk[1], kk[4]); cmpx_desc(kk[3], kk[6]);
+    cmpx_desc(kk[1], kk[2]); cmpx_desc(kk[3], kk[4]); cmpx_desc(kk[5], kk[6]);
     for (int r = 0; r < k; ++r) {
-      unsigned long long b = kk[0];
-#pragma unroll
-      for (int i = 1; i < 8; ++i) b = kk[i] > b ? kk[i] : b;
-      const uint32_t hi = (uint32_t)(b >> 32);
+      const uint32_t hi = (uint32_t)(kk[0] >> 32);
       const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, hi);
-      const uint32_t l = __reduce_max_sync(0xFFFFFFFFu, hi == m ? (uint32_t)b : 0u);
+      const uint32_t l = __reduce_max_sync(0xFFFFFFFFu, hi == m ? (uint32_t)kk[0] : 0u);
       const int e_star = (int)(0xFFFFFFFFu - l);
-      const int won = (e_star & 31) == lane ? (e_star >> 5) : -1;
+      const bool won = (e_star & 31) == lane;
 #pragma unroll
-      for (int i = 0; i < 8; ++i) kk[i] = i == won ? 0ull : kk[i];
+      for (int i = 0; i < 7; ++i) kk[i] = won ? kk[i + 1] : kk[i];
+      kk[7] = won ? 0ull : kk[7];
       if (lane == r) {
         my_id = e_star;
         my_val = row[e_star];
@@ -131,12 +150,13 @@ route_hist_kernel(const float* __restrict__ logits, int T, int E, int k,
 }
 
 // Exclusive scan over the block (blockDim.x <= 1024, a multiple of 32).
-__device__ int block_exclusive_scan(int v, int* scratch /* [32] */, int* total) {
+template <typename V>
+__device__ V block_exclusive_scan(V v, V* scratch /* [33] */, V* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int incl = v;
+  V incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    int n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    const V n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
     if (lane >= o) incl += n;
   }
   __syncthreads();
@@ -144,66 +164,90 @@ __device__ int block_exclusive_scan(int v, int* scratch /* [32] */, int* total) 
   __syncthreads();
   if (warp == 0) {
     const int nw = blockDim.x >> 5;
-    int w = lane < nw ? scratch[lane] : 0;
-    int wi = w;
+    const V w = lane < nw ? scratch[lane] : V(0);
+    V wi = w;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      int n = __shfl_up_sync(0xFFFFFFFFu, wi, o);
+      const V n = __shfl_up_sync(0xFFFFFFFFu, wi, o);
       if (lane >= o) wi += n;
     }
     scratch[lane] = wi - w;  // exclusive prefix of warp totals
     if (lane == 31) scratch[32] = wi;
   }
   __syncthreads();
-  const int res = scratch[warp] + incl - v;
+  const V res = scratch[warp] + incl - v;
   *total = scratch[32];
   __syncthreads();
   return res;
 }
 
-__global__ void __launch_bounds__(1024)
-sort_scan_kernel(int32_t* __restrict__ block_hist, int nb, int E, int32_t* __restrict__ offsets,
+// Two 32-bit counters in one 64-bit word (each total stays below 2^31, so
+// sums never carry from the low field into the high one).
+__device__ __forceinline__ unsigned long long pack2(int lo, int hi) {
+  return (unsigned long long)(uint32_t)lo | ((unsigned long long)(uint32_t)hi << 32);
+}
+
+// Threads e*G .. e*G+G-1 serve expert e (G a power of two <= 32, G*E <= 1024),
+// part p of G summing routing blocks [p*ceil(nb/G), ...) of that expert.
+__global__ void __launch_bounds__(1024, 1)
+sort_scan_kernel(int32_t* __restrict__ block_hist, int nb, int E, int G, int32_t* __restrict__ offsets,
                  int32_t* __restrict__ active, int32_t* __restrict__ counts,
                  int4* __restrict__ gemv_chunks, int4* __restrict__ tc_tiles) {
-  __shared__ int scratch[33];
-  const int e = threadIdx.x;
+  __shared__ unsigned long long scratch[33];
+  const int e = threadIdx.x / G, p = threadIdx.x & (G - 1);
   const bool ok = e < E;
-  int cnt = 0;
-  if (ok)
-    for (int b = 0; b < nb; ++b) cnt += block_hist[(size_t)b * E + e];
-  int total;
-  const int off = block_exclusive_scan(ok ? cnt : 0, scratch, &total);
+  const int per = (nb + G - 1) / G;
+  const int b0 = min(nb, p * per), b1 = min(nb, b0 + per);
+  int part = 0;
   if (ok) {
-    offsets[e] = off;
-    int run = off;
-    for (int b = 0; b < nb; ++b) {
+#pragma unroll 8
+    for (int b = b0; b < b1; ++b) part += block_hist[(size_t)b * E + e];
+  }
+  // prefix over the expert's G parts (consecutive lanes of one warp)
+  int pin = part;
+  for (int o = 1; o < G; o <<= 1) {
+    const int n = __shfl_up_sync(0xFFFFFFFFu, pin, o, G);
+    if (p >= o) pin += n;
+  }
+  const int cnt = __shfl_sync(0xFFFFFFFFu, pin, G - 1, G);
+  const bool lead = ok && p == 0;
+  // offsets and the non-empty-expert positions in one scan, the GEMV chunk
+  // and tensor-core tile positions in another
+  const int nch = ok ? (cnt + kGemvTokens - 1) / kGemvTokens : 0;
+  const int ntl = ok ? (cnt + kTcTileN - 1) / kTcTileN : 0;
+  unsigned long long tot1, tot2;
+  const unsigned long long x1 =
+      block_exclusive_scan(lead ? pack2(cnt, cnt > 0 ? 1 : 0) : 0ull, scratch, &tot1);
+  const unsigned long long x2 = block_exclusive_scan(lead ? pack2(nch, ntl) : 0ull, scratch, &tot2);
+  const unsigned long long y1 = __shfl_sync(0xFFFFFFFFu, x1, 0, G);
+  const unsigned long long y2 = __shfl_sync(0xFFFFFFFFu, x2, 0, G);
+  const int off = (int)(uint32_t)y1, apos = (int)(y1 >> 32);
+  const int cpos = (int)(uint32_t)y2, tpos = (int)(y2 >> 32);
+  if (ok) {
+    if (p == 0) {
+      offsets[e] = off;
+      if (cnt > 0) active[apos] = e;
+    }
+    int run = off + pin - part;  // rows of this expert in the routing blocks before b0
+#pragma unroll 8
+    for (int b = b0; b < b1; ++b) {
       const int c = block_hist[(size_t)b * E + e];
       block_hist[(size_t)b * E + e] = run;
       run += c;
     }
+    // GEMV chunks of up to kGemvTokens rows
+    for (int c = p; c < nch; c += G)
+      gemv_chunks[cpos + c] = make_int4(e, off + c * kGemvTokens, min(kGemvTokens, cnt - c * kGemvTokens), 0);
+    // tensor-core tiles: ceil(cnt / kTcTileN) tiles of equal size (rounded up to 16)
+    const int per_tile = ntl ? (((cnt + ntl - 1) / ntl + 15) & ~15) : 0;
+    for (int c = p; c < ntl; c += G)
+      tc_tiles[tpos + c] = make_int4(e, off + c * per_tile, min(per_tile, cnt - c * per_tile), 0);
   }
-  if (e == 0) offsets[E] = total;
-  // non-empty experts
-  int n_active;
-  const int apos = block_exclusive_scan(ok && cnt > 0 ? 1 : 0, scratch, &n_active);
-  if (ok && cnt > 0) active[apos] = e;
-  // GEMV chunks of up to kGemvTokens rows
-  const int nch = ok ? (cnt + kGemvTokens - 1) / kGemvTokens : 0;
-  int n_chunks;
-  const int cpos = block_exclusive_scan(nch, scratch, &n_chunks);
-  for (int c = 0; c < nch; ++c)
-    gemv_chunks[cpos + c] = make_int4(e, off + c * kGemvTokens, min(kGemvTokens, cnt - c * kGemvTokens), 0);
-  // tensor-core tiles of up to kTcTileN rows
-  // tensor-core tiles: ceil(cnt / kTcTileN) tiles of equal size (rounded up to 16)
-  const int ntl = ok ? (cnt + kTcTileN - 1) / kTcTileN : 0;
-  const int per = ntl ? (((cnt + ntl - 1) / ntl + 15) & ~15) : 0;
-  int n_tiles;
-  const int tpos = block_exclusive_scan(ntl, scratch, &n_tiles);
-  for (int c = 0; c < ntl; ++c) tc_tiles[tpos + c] = make_int4(e, off + c * per, min(per, cnt - c * per), 0);
-  if (e == 0) {
-    counts[0] = n_active;
-    counts[1] = n_chunks;
-    counts[2] = n_tiles;
+  if (threadIdx.x == 0) {
+    offsets[E] = (int)(uint32_t)tot1;
+    counts[0] = (int)(tot1 >> 32);
+    counts[1] = (int)(uint32_t)tot2;
+    counts[2] = (int)(tot2 >> 32);
     counts[3] = 0;
   }
 }
@@ -249,84 +293,110 @@ scatter_kernel(const int32_t* __restrict__ topk_ids, const int32_t* __restrict__
 }
 
 
-// One block does everything when all tokens fit one routing block (T <= 32,
-// the decode shape): routing by 32 warps, per-expert totals, offsets and work
-// lists, then the stable scatter by a single warp walking the slots in order.
-__global__ void __launch_bounds__(1024)
+// Routing and sort when all tokens fit one routing block (T <= 32, the decode
+// batch): a cluster of kSmallCtas CTAs on separate SMs, one token per warp
+// (32 warps of top-k on one SM are issue-bound), each warp also storing its
+// token's k expert ids into CTA 0's shared memory.  After the cluster barrier
+// CTA 0 alone builds, per expert, the mask of tokens that picked it, then the
+// offsets and work lists (one scan of packed counters) and the stable
+// scatter: a token picks an expert at most once, so the rank of slot (t, j)
+// among its expert's slots in ascending flat index is the number of tokens
+// before t in the expert's mask.
+constexpr int kSmallCtas = 8;
+constexpr int kSmallWarps = kRouteTokensPerBlock / kSmallCtas;  // tokens per CTA
+constexpr int kSmallThreads = kSmallWarps * 32;
+constexpr int kMaxExperts = 1024;
+static_assert(kSmallCtas * kSmallWarps == 32, "a token mask is one 32-bit word");
+
+// Per-expert counters packed in 16-bit fields: rows, non-empty, GEMV chunks,
+// tensor-core tiles.  Each total is at most T*k <= 1024 (or E <= 1024), so
+// fields never carry into one another.
+__device__ __forceinline__ unsigned long long pack4(int cnt) {
+  const unsigned long long nch = (cnt + kGemvTokens - 1) / kGemvTokens;
+  const unsigned long long ntl = (cnt + kTcTileN - 1) / kTcTileN;
+  return (unsigned long long)cnt | ((unsigned long long)(cnt > 0) << 16) | (nch << 32) | (ntl << 48);
+}
+
+__global__ void __cluster_dims__(kSmallCtas, 1, 1) __launch_bounds__(kSmallThreads)
 route_small_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ topk_ids,
                    float* __restrict__ topk_w, int32_t* __restrict__ offsets, int32_t* __restrict__ active,
                    int32_t* __restrict__ counts, int4* __restrict__ gemv_chunks, int4* __restrict__ tc_tiles,
                    int32_t* __restrict__ sorted_slot, int32_t* __restrict__ slot_pos, int32_t* __restrict__ err) {
-  extern __shared__ int smem_small[];
-  int* hist = smem_small;                            // [E] counts, then running positions
-  int* ids_s = hist + E;                             // [T*k]
-  float* rows = reinterpret_cast<float*>(ids_s + kRouteTokensPerBlock * 32);  // [32 warps][E]
-  __shared__ int scratch[33];
+  __shared__ int ids_s[kRouteTokensPerBlock * 32];  // [T*k] expert of each slot (CTA 0's copy)
+  __shared__ uint32_t mask_s[kMaxExperts];          // bit t: token t picked the expert
+  __shared__ int off_s[kMaxExperts];
+  __shared__ unsigned long long wsum[kSmallWarps];
+  cooperative_groups::cluster_group cluster = cooperative_groups::this_cluster();
+  const int cta = (int)cluster.block_rank();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x < 4) err[threadIdx.x] = 0;
-  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
-  __syncthreads();
-  if (warp < T) {
-    float* row = rows + warp * E;
-    const float* src = logits + (size_t)warp * E;
-    for (int e = lane; e < E; e += 32) row[e] = src[e];
-    __syncwarp();
+  if (cta == 0) {
+    if (threadIdx.x < 4) err[threadIdx.x] = 0;
+    for (int e = threadIdx.x; e < E; e += kSmallThreads) mask_s[e] = 0;
+  }
+  const int t = cta * kSmallWarps + warp;
+  if (t < T) {
     int id;
     float w;
-    topk_softmax_warp(row, E, k, lane, id, w);
+    topk_softmax_warp(logits + (size_t)t * E, E, k, lane, id, w);
     if (lane < k) {
-      topk_ids[warp * k + lane] = id;
-      topk_w[warp * k + lane] = w;
-      ids_s[warp * k + lane] = id;
-      atomicAdd(&hist[id], 1);
+      topk_ids[t * k + lane] = id;
+      topk_w[t * k + lane] = w;
+      cluster.map_shared_rank(ids_s, 0)[t * k + lane] = id;
     }
   }
+  cluster.sync();
+  if (cta != 0) return;
+  const int S = T * k;
+  for (int f = threadIdx.x; f < S; f += kSmallThreads) atomicOr(&mask_s[ids_s[f]], 1u << (f / k));
   __syncthreads();
-  const int e = threadIdx.x;
-  const bool ok = e < E;
-  const int cnt = ok ? hist[e] : 0;
-  int total;
-  const int off = block_exclusive_scan(cnt, scratch, &total);
-  if (ok) offsets[e] = off;
-  if (e == 0) offsets[E] = total;
-  int n_active;
-  const int apos = block_exclusive_scan(ok && cnt > 0 ? 1 : 0, scratch, &n_active);
-  if (ok && cnt > 0) active[apos] = e;
-  const int nch = ok ? (cnt + kGemvTokens - 1) / kGemvTokens : 0;
-  int n_chunks;
-  const int cpos = block_exclusive_scan(nch, scratch, &n_chunks);
-  for (int c = 0; c < nch; ++c)
-    gemv_chunks[cpos + c] = make_int4(e, off + c * kGemvTokens, min(kGemvTokens, cnt - c * kGemvTokens), 0);
-  // tensor-core tiles: ceil(cnt / kTcTileN) tiles of equal size (rounded up to 16)
-  const int ntl = ok ? (cnt + kTcTileN - 1) / kTcTileN : 0;
-  const int per = ntl ? (((cnt + ntl - 1) / ntl + 15) & ~15) : 0;
-  int n_tiles;
-  const int tpos = block_exclusive_scan(ntl, scratch, &n_tiles);
-  for (int c = 0; c < ntl; ++c) tc_tiles[tpos + c] = make_int4(e, off + c * per, min(per, cnt - c * per), 0);
-  if (e == 0) {
-    counts[0] = n_active;
-    counts[1] = n_chunks;
-    counts[2] = n_tiles;
+  // this thread's experts [e0, e1), in order
+  const int ept = (E + kSmallThreads - 1) / kSmallThreads;
+  const int e0 = min(E, (int)threadIdx.x * ept), e1 = min(E, e0 + ept);
+  unsigned long long mine = 0;
+  for (int e = e0; e < e1; ++e) mine += pack4(__popc(mask_s[e]));
+  unsigned long long incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned long long n = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  unsigned long long base = incl - mine, total = 0;
+#pragma unroll
+  for (int w = 0; w < kSmallWarps; ++w) {
+    if (w < warp) base += wsum[w];
+    total += wsum[w];
+  }
+  for (int e = e0; e < e1; ++e) {
+    const int cnt = __popc(mask_s[e]);
+    const int off = (int)(base & 0xFFFF), apos = (int)((base >> 16) & 0xFFFF);
+    const int cpos = (int)((base >> 32) & 0xFFFF), tpos = (int)(base >> 48);
+    offsets[e] = off;
+    off_s[e] = off;
+    if (cnt > 0) active[apos] = e;
+    const int nch = (cnt + kGemvTokens - 1) / kGemvTokens;
+    for (int c = 0; c < nch; ++c)
+      gemv_chunks[cpos + c] = make_int4(e, off + c * kGemvTokens, min(kGemvTokens, cnt - c * kGemvTokens), 0);
+    // tensor-core tiles: ceil(cnt / kTcTileN) tiles of equal size (rounded up to 16)
+    const int ntl = (cnt + kTcTileN - 1) / kTcTileN;
+    const int per = ntl ? (((cnt + ntl - 1) / ntl + 15) & ~15) : 0;
+    for (int c = 0; c < ntl; ++c) tc_tiles[tpos + c] = make_int4(e, off + c * per, min(per, cnt - c * per), 0);
+    base += pack4(cnt);
+  }
+  if (threadIdx.x == 0) {
+    offsets[E] = (int)(total & 0xFFFF);
+    counts[0] = (int)((total >> 16) & 0xFFFF);
+    counts[1] = (int)((total >> 32) & 0xFFFF);
+    counts[2] = (int)(total >> 48);
     counts[3] = 0;
   }
-  if (ok) hist[e] = off;  // running position of each expert
   __syncthreads();
-  if (warp == 0) {
-    const int S = T * k;
-    for (int f0 = 0; f0 < S; f0 += 32) {
-      const int f = f0 + lane;
-      const int ef = f < S ? ids_s[f] : -1;
-      const unsigned peers = __match_any_sync(0xFFFFFFFFu, ef);
-      const int rank = __popc(peers & ((1u << lane) - 1u));
-      if (ef >= 0) {
-        const int pos = hist[ef] + rank;
-        sorted_slot[pos] = f;
-        slot_pos[f] = pos;
-      }
-      __syncwarp();
-      if (ef >= 0 && rank == 0) hist[ef] += __popc(peers);
-      __syncwarp();
-    }
+  for (int f = threadIdx.x; f < S; f += kSmallThreads) {
+    const int e = ids_s[f];
+    const int pos = off_s[e] + __popc(mask_s[e] & ((1u << (f / k)) - 1u));
+    sorted_slot[pos] = f;
+    slot_pos[f] = pos;
   }
 }
 
@@ -335,22 +405,17 @@ route_small_kernel(const float* __restrict__ logits, int T, int E, int k, int32_
 cudaError_t launch_route(const moe_fp4_dims& d, const float* logits, const Workspace& ws, cudaStream_t st) {
   const int nb = ws.nb_route;
   if (nb == 1) {
-    const size_t smem = (size_t)d.E * sizeof(int) + kRouteTokensPerBlock * 32 * sizeof(int) +
-                        (size_t)32 * d.E * sizeof(float);
-    static bool configured = false;
-    if (!configured) {
-      cudaFuncSetAttribute(route_small_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024);
-      configured = true;
-    }
-    route_small_kernel<<<1, 1024, smem, st>>>(logits, d.T, d.E, d.k, ws.topk_ids, ws.topk_w, ws.offsets, ws.active,
-                                              ws.counts, ws.gemv_chunks, ws.tc_tiles, ws.sorted_slot, ws.slot_pos,
-                                              ws.err);
+    route_small_kernel<<<kSmallCtas, kSmallThreads, 0, st>>>(logits, d.T, d.E, d.k, ws.topk_ids, ws.topk_w,
+                                                           ws.offsets, ws.active, ws.counts, ws.gemv_chunks,
+                                                           ws.tc_tiles, ws.sorted_slot, ws.slot_pos, ws.err);
     return cudaGetLastError();
   }
   size_t smem1 = (size_t)(kWarps * d.E) * sizeof(float) + (size_t)d.E * sizeof(int);
   route_hist_kernel<<<nb, kRouteThreads, smem1, st>>>(logits, d.T, d.E, d.k, ws.topk_ids, ws.topk_w,
                                                      ws.block_hist, ws.err);
-  sort_scan_kernel<<<1, 1024, 0, st>>>(ws.block_hist, nb, d.E, ws.offsets, ws.active, ws.counts,
+  int G = 1;  // threads per expert in sort_scan
+  while (G < 32 && 2 * G * d.E <= 1024) G *= 2;
+  sort_scan_kernel<<<1, 1024, 0, st>>>(ws.block_hist, nb, d.E, G, ws.offsets, ws.active, ws.counts,
                                        ws.gemv_chunks, ws.tc_tiles);
   size_t smem3 = (size_t)(kWarps + 1) * d.E * sizeof(int);
   scatter_kernel<<<nb, kRouteThreads, smem3, st>>>(ws.topk_ids, ws.block_hist, d.T, d.E, d.k,

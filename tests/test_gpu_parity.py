@@ -178,6 +178,30 @@ def test_route_entry_point(moe):
     np.testing.assert_allclose(w.cpu().numpy(), ref_w, rtol=2e-6, atol=1e-7)
 
 
+@pytest.mark.parametrize("T,E,k", [(32, 1024, 32), (17, 300, 7), (1, 1000, 3), (32, 257, 8), (5, 8, 8),
+                                   (100, 1024, 32), (77, 8, 3), (70, 1000, 5), (64, 512, 8)])
+def test_route_wide_expert_counts(moe, T, E, k):
+    """both routing paths (T <= 32: one cluster; T > 32: three kernels) over
+    expert counts and k beyond the layer configs, with ties on every third token"""
+    L = make_layer(T=T, d=32, I=32, E=E, k=k, seed=T * 7 + E + k)
+    logits = L.router_logits.copy()
+    logits[::3] = np.round(logits[::3] * 2.0) / 2.0
+    ids, w, off, ss = moe.route(torch.from_numpy(logits).cuda(), k)
+    torch.cuda.synchronize()
+    ref_ids, ref_w = oracle.route(logits, k)
+    ref_off, ref_ss, _ = oracle.expert_sort(ref_ids, E)
+    np.testing.assert_array_equal(ids.cpu().numpy(), ref_ids)
+    np.testing.assert_array_equal(off.cpu().numpy(), ref_off)
+    np.testing.assert_array_equal(ss.cpu().numpy(), ref_ss)
+    np.testing.assert_allclose(w.cpu().numpy(), ref_w, rtol=2e-6, atol=1e-7)
+
+
+@pytest.mark.parametrize("flags", [GEMV, TC])
+def test_small_batch_many_experts_forward(moe, flags):
+    """T <= 32 routing with E > 256 (work lists for many sparse experts)"""
+    full_check(moe, make_layer(T=32, d=1024, I=1024, E=300, k=2, seed=51), flags)
+
+
 def test_forward_host_matches_forward(moe):
     L = make_layer(T=40, d=1024, I=1024, E=16, k=4, seed=16)
     D = to_device(L)
