@@ -184,6 +184,7 @@ gather_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ sorted
 __global__ void __launch_bounds__(256)
 combine_kernel(const float* __restrict__ y, const float* __restrict__ topk_w,
                const int32_t* __restrict__ slot_pos, int T, int k, int d, float* __restrict__ out) {
+  griddep_wait();  // y comes from the W2 kernel (launched early, see launch_combine)
   const int t = blockIdx.x;
   if (t >= T) return;
   const int vec = d / 4;
@@ -237,8 +238,11 @@ cudaError_t launch_h_f16(const moe_fp4_dims& d, const Workspace& ws, cudaStream_
 
 cudaError_t launch_combine(const moe_fp4_dims& d, float* out, const Workspace& ws, cudaStream_t st) {
   const dim3 grid(d.T, (d.d / 4 + 255) / 256);
-  combine_kernel<<<grid, 256, 0, st>>>(ws.y, ws.topk_w, ws.slot_pos, d.T, d.k, d.d, out);
-  return cudaGetLastError();
+  const float* y = ws.y;
+  const float* w = ws.topk_w;
+  const int32_t* pos = ws.slot_pos;
+  // launched early: blocks start as the W2 kernel's CTAs retire, then wait for it
+  return launch_early(combine_kernel, grid, dim3(256), 0, st, y, w, pos, d.T, d.k, d.d, out);
 }
 
 }  // namespace moe_fp4

@@ -133,11 +133,6 @@ stream_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + P.stages);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int n_chunks = P.counts[1];
-  const long long n_items = (long long)n_chunks * P.n_rb;
-  const long long it0 = n_items * blockIdx.x / gridDim.x;
-  const long long it1 = n_items * (blockIdx.x + 1) / gridDim.x;
-  const int nst = P.K / kKStage;
   if (tid == 0) {
     for (int i = 0; i < P.stages; ++i) {
       mbar_init(&full[i], 1);
@@ -147,6 +142,18 @@ stream_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__
     mbar_fence_init();
   }
   __syncthreads();
+  // Both kernels are launched early.  W13 waits here for the routing kernel
+  // (the work list); W2 was let start only after every W13 CTA had passed
+  // that wait, so the work list is complete, and it reads it through L2
+  // (ld.global.cg) so that its producer can stream weights while W13 ends;
+  // its consumers wait for W13 (h) below.
+  if (W13) griddep_wait();
+  griddep_launch_dependents();
+  const int n_chunks = __ldcg(P.counts + 1);
+  const long long n_items = (long long)n_chunks * P.n_rb;
+  const long long it0 = n_items * blockIdx.x / gridDim.x;
+  const long long it1 = n_items * (blockIdx.x + 1) / gridDim.x;
+  const int nst = P.K / kKStage;
 
   if (warp == kConsWarps) {
     // ---------------- producer warp ----------------
@@ -156,7 +163,7 @@ stream_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__
       uint32_t phase = 0;
       for (long long it = it0; it < it1; ++it) {
         const int c = (int)(it / P.n_rb), rb = (int)(it % P.n_rb);
-        const int e = P.chunks[c].x;
+        const int e = __ldcg(P.chunks + c).x;
         for (int ks = 0; ks < nst; ++ks) {
           if (!mbar_wait(&empty[slot], phase ^ 1u, abort_flag, P.err, kErrWaitTimeout)) break;
           issue_stage<W13>(&map_w, &map_s, P, e, rb, ks, ring + (size_t)slot * kStageBytes, &full[slot], pol);
@@ -172,6 +179,7 @@ stream_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__
   }
 
   // ---------------- consumer warps ----------------
+  if (!W13) griddep_wait();  // h comes from the W13 kernel
   const int g = lane >> 2, t = lane & 3;
   const int tile = warp % kTiles, kpart = warp / kTiles;  // 16-row tile, share of the stage's blocks
   // rows of this thread inside the stage's 128 rows (A-fragment rows g and g+8)
@@ -350,8 +358,7 @@ cudaError_t launch_stream(const CUtensorMap& mw, const CUtensorMap& ms, StreamPa
     cudaFuncSetAttribute(stream_kernel<W13>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     configured = true;
   }
-  stream_kernel<W13><<<num_sms(), kThreads, smem, st>>>(mw, ms, P);
-  return cudaGetLastError();
+  return launch_early(stream_kernel<W13>, dim3(num_sms()), dim3(kThreads), smem, st, mw, ms, P);
 }
 
 }  // namespace

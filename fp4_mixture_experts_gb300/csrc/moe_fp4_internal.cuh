@@ -113,6 +113,33 @@ __device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
 // few ulp of fp32, far below the bf16 rounding of h that follows)
 __device__ __forceinline__ float swiglu(float g, float u) { return __fdividef(g, 1.0f + __expf(-g)) * u; }
 
+// Programmatic dependent launch.  A kernel launched by launch_early() may start
+// while the previous kernel of the stream is still running: griddep_wait()
+// returns once that kernel has completed and its writes are visible (at once
+// for a kernel launched the ordinary way), and the early kernel may touch
+// nothing that kernel writes before it.  griddep_launch_dependents() lets the
+// next early kernel start before this one ends.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_early(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                         Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 #endif
 
 }  // namespace moe_fp4

@@ -326,6 +326,7 @@ route_small_kernel(const float* __restrict__ logits, int T, int E, int k, int32_
   __shared__ uint32_t mask_s[kMaxExperts];          // bit t: token t picked the expert
   __shared__ int off_s[kMaxExperts];
   __shared__ unsigned long long wsum[kSmallWarps];
+  griddep_launch_dependents();  // the W13 kernel may start its prologue (it waits for this kernel)
   cooperative_groups::cluster_group cluster = cooperative_groups::this_cluster();
   const int cta = (int)cluster.block_rank();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
