@@ -250,7 +250,7 @@ def test_d7168_streaming_path(moe):
 
 
 def test_routing_block_boundary(moe):
-    """T = 32 runs the single-block routing kernel, T = 33 the three-kernel one"""
+    """T = 32 runs the one-cluster routing kernel, T = 33 the three-kernel one"""
     for T in (32, 33):
         full_check(moe, make_layer(T=T, d=1024, I=1024, E=64, k=8, seed=32 + T))
 
