@@ -2,15 +2,15 @@
 
 A thin Python binding over the C-ABI library ``libmoe_fp4.so`` (declared in
 ``include/moe_fp4.h``).  It only marshals arguments: every step of the layer
-(routing, expert sort, gather, W13 + SwiGLU, W2, combine) runs in the
-library's CUDA kernels.  PyTorch supplies device memory and streams.
+(routing, expert sort, gather, W13 + SwiGLU, W2, combine), and the MXFP8
+activation quantiser, run in the library's CUDA kernels.  PyTorch supplies device memory and streams.
 Importing the package does not need a GPU; calling a compute function
 without the built library raises.
 """
 from ._binding import (EXPORTED_SYMBOLS, FLAG_FORCE_GEMV, FLAG_FORCE_TC, Dims, MoeFp4Error, check, forward,
-                       forward_host, forward_noalloc, host_workspace_bytes, lib_path, load_library, route, status_string,
-                       workspace_bytes)
+                       forward_host, forward_noalloc, host_workspace_bytes, lib_path, load_library, mxfp8_quantize, route,
+                       status_string, workspace_bytes)
 
 __all__ = ["EXPORTED_SYMBOLS", "FLAG_FORCE_GEMV", "FLAG_FORCE_TC", "Dims", "MoeFp4Error", "check", "forward",
-           "forward_host", "forward_noalloc", "host_workspace_bytes", "lib_path", "load_library", "route", "status_string",
-           "workspace_bytes"]
+           "forward_host", "forward_noalloc", "host_workspace_bytes", "lib_path", "load_library", "mxfp8_quantize",
+           "route", "status_string", "workspace_bytes"]

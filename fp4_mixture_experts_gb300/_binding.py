@@ -23,6 +23,7 @@ EXPORTED_SYMBOLS = (
     "moe_fp4_forward_profiled",
     "moe_fp4_forward_host",
     "moe_fp4_forward_noalloc",
+    "moe_fp4_mxfp8_quantize",
     "moe_fp4_check",
     "moe_fp4_status_string",
 )
@@ -72,6 +73,8 @@ def load_library():
     lib.moe_fp4_forward_host.restype = ctypes.c_int
     lib.moe_fp4_forward_noalloc.argtypes = [pd, P, P, P, P, P, P, P, ctypes.c_uint, P]
     lib.moe_fp4_forward_noalloc.restype = ctypes.c_int
+    lib.moe_fp4_mxfp8_quantize.argtypes = [P, ctypes.c_int64, ctypes.c_int32, P, P, P]
+    lib.moe_fp4_mxfp8_quantize.restype = ctypes.c_int
     lib.moe_fp4_check.argtypes = [P, P]
     lib.moe_fp4_check.restype = ctypes.c_int
     lib.moe_fp4_status_string.argtypes = [ctypes.c_int]
@@ -139,6 +142,25 @@ def route(router_logits, k: int, d: int = 128, I: int = 128, workspace=None, str
     if rc != 0:
         raise MoeFp4Error(rc, "moe_fp4_route")
     return ids, w, off, ss
+
+
+def mxfp8_quantize(x_bf16, codes=None, scales=None, stream=None):
+    """MXFP8 of bf16 rows x_bf16 [R, K] (K a multiple of 32) on the GPU.
+
+    Returns (codes uint8 [R, K] E4M3, scales uint8 [R, K/32] E8M0)."""
+    import torch
+    if x_bf16.dim() != 2 or x_bf16.dtype != torch.bfloat16 or not x_bf16.is_contiguous():
+        raise ValueError("x_bf16 must be a contiguous bf16 [R, K] tensor")
+    R, K = x_bf16.shape
+    dev = x_bf16.device
+    if codes is None:
+        codes = torch.empty(R, K, dtype=torch.uint8, device=dev)
+    if scales is None:
+        scales = torch.empty(R, K // 32, dtype=torch.uint8, device=dev)
+    rc = load_library().moe_fp4_mxfp8_quantize(_ptr(x_bf16), R, K, _ptr(codes), _ptr(scales), _stream(stream))
+    if rc != 0:
+        raise MoeFp4Error(rc, "moe_fp4_mxfp8_quantize")
+    return codes, scales
 
 
 def forward(x_bf16, router_logits, w13, w13_scale, w2, w2_scale, k: int, out=None, flags: int = 0,

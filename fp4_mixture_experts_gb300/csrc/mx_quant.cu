@@ -1,0 +1,82 @@
+// MXFP8 quantisation of bf16 rows, the activation operand of a block-scaled
+// tensor-core product (E4M3 elements, one E8M0 scale per 32 elements along
+// the row, OCP Microscaling v1.0 conversion).
+//
+// One thread per 32-element block: four 16-byte loads, the block's largest
+// magnitude from the bf16 bit patterns (with the sign bit cleared, bit order
+// is magnitude order), its exponent minus 8 (the largest E4M3 exponent) as
+// the scale, then every element times the exact power of two 2^-scale goes
+// through the CUDA fp8 conversion (round to nearest even, saturating at the
+// largest finite E4M3); two 16-byte stores of codes and one scale byte.  The
+// kernel is bound by HBM: 2 bytes read and 1 + 1/32 written per element.
+#include <cuda_fp8.h>
+
+#include "moe_fp4_internal.cuh"
+
+namespace moe_fp4 {
+namespace {
+
+// floor(log2(v)) of a nonzero bf16 magnitude given by its 15 low bits.
+__device__ __forceinline__ int bf16_floor_log2(uint32_t mag) {
+  const int e = (int)(mag >> 7);
+  if (e > 0) return e - 127;
+  return -133 + (31 - __clz(mag));  // subnormal: mag * 2^-133, mag in [1, 127]
+}
+
+__device__ __forceinline__ uint32_t e4m3_code(uint32_t bf16_bits, float inv_scale) {
+  const float v = __uint_as_float(bf16_bits << 16) * inv_scale;
+  return (uint32_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
+}
+
+__global__ void __launch_bounds__(256)
+mxfp8_quantize_kernel(const uint4* __restrict__ x, long long n_blocks, uint4* __restrict__ codes,
+                      uint8_t* __restrict__ scales) {
+  for (long long b = blockIdx.x * (long long)blockDim.x + threadIdx.x; b < n_blocks;
+       b += (long long)gridDim.x * blockDim.x) {
+    uint32_t w[16];  // 32 bf16, two per word, the even element in the low half
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 q = x[4 * b + i];
+      w[4 * i] = q.x;
+      w[4 * i + 1] = q.y;
+      w[4 * i + 2] = q.z;
+      w[4 * i + 3] = q.w;
+    }
+    uint32_t amax = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) amax = max(amax, max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu));
+    // scale exponent in [-127, 119]; 2^-s is then a normal fp32 (exponent field 127 - s in [8, 254])
+    const int s = amax == 0 ? -127 : max(bf16_floor_log2(amax) - 8, -127);
+    const float inv = __uint_as_float((uint32_t)(127 - s) << 23);
+    uint32_t out[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t a = w[2 * i], c = w[2 * i + 1];
+      out[i] = e4m3_code(a & 0xFFFFu, inv) | (e4m3_code(a >> 16, inv) << 8) | (e4m3_code(c & 0xFFFFu, inv) << 16) |
+               (e4m3_code(c >> 16, inv) << 24);
+    }
+    codes[2 * b] = make_uint4(out[0], out[1], out[2], out[3]);
+    codes[2 * b + 1] = make_uint4(out[4], out[5], out[6], out[7]);
+    scales[b] = (uint8_t)(s + 127);
+  }
+}
+
+}  // namespace
+}  // namespace moe_fp4
+
+extern "C" int moe_fp4_mxfp8_quantize(const void* x_bf16, int64_t rows, int32_t K, uint8_t* codes, uint8_t* scales,
+                                      void* cuda_stream) {
+  using namespace moe_fp4;
+  if (rows < 0 || K <= 0 || K % 32 != 0) return MOE_FP4_ERR_INVALID_ARG;
+  if (rows == 0) return MOE_FP4_OK;  // nothing to do; the pointers are not looked at
+  if (!x_bf16 || !codes || !scales) return MOE_FP4_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(x_bf16) & 15) || (reinterpret_cast<uintptr_t>(codes) & 15))
+    return MOE_FP4_ERR_INVALID_ARG;
+  const long long n_blocks = (long long)rows * (K / 32);
+  long long grid = (n_blocks + 255) / 256;
+  const long long cap = (long long)num_sms() * 16;
+  if (grid > cap) grid = cap;
+  mxfp8_quantize_kernel<<<(unsigned)grid, 256, 0, static_cast<cudaStream_t>(cuda_stream)>>>(
+      static_cast<const uint4*>(x_bf16), n_blocks, reinterpret_cast<uint4*>(codes), scales);
+  return cudaGetLastError() == cudaSuccess ? MOE_FP4_OK : MOE_FP4_ERR_CUDA;
+}

@@ -169,6 +169,30 @@ int moe_fp4_forward_noalloc(const moe_fp4_dims* dims, const void* x_bf16, const 
                             const uint8_t* w2, const uint8_t* w2_scale, float* out,
                             unsigned flags, void* cuda_stream);
 
+/* MXFP8 quantisation of bf16 rows: the activation operand of a block-scaled
+ * (MX) tensor-core product.  The paper quantises its decode activations
+ * (abstract: INT8 activation quantisation) and the MI250 blog names
+ * block-wise FP8 quantisation as the next gain; this is the MX form, with
+ * the blocks of the weights (OCP Microscaling v1.0 conversion, E4M3 element).
+ * For each 32 consecutive elements of a row, with amax their largest
+ * magnitude:
+ *   scale byte  s = floor(log2(amax)) - 8 + 127, at least 0; an all-zero
+ *               block gets 0 (the scale is 2^(s-127));
+ *   codes       E4M3 (OCP FP8 "FN": bias 7, no infinities, largest 448) of
+ *               x / 2^(s-127), rounded to nearest even, saturated at +-448;
+ *               a negative zero gives 0x80.
+ * Layouts (row-major, device memory):
+ *   x_bf16  bf16   [rows, K]      16-byte aligned; K a positive multiple of 32
+ *   codes   uint8  [rows, K]      16-byte aligned; fully overwritten
+ *   scales  uint8  [rows, K/32]   fully overwritten
+ * The caller owns the buffers and the stream.  One kernel is enqueued; for
+ * rows = 0 nothing is, and the pointers may be null.  The call never
+ * synchronises.  Returns MOE_FP4_ERR_INVALID_ARG, with nothing enqueued, for
+ * rows < 0, K not a positive multiple of 32, or (rows > 0) a null pointer or
+ * a misaligned x_bf16 / codes; MOE_FP4_ERR_CUDA if the launch fails. */
+int moe_fp4_mxfp8_quantize(const void* x_bf16, int64_t rows, int32_t K, uint8_t* codes, uint8_t* scales,
+                           void* cuda_stream);
+
 /* Synchronises the stream and reads the device error word of the workspace
  * (set by a kernel that met an index out of range, e.g. a corrupted expert
  * id); returns MOE_FP4_OK, MOE_FP4_ERR_DEVICE or MOE_FP4_ERR_CUDA, and clears

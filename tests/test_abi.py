@@ -85,3 +85,20 @@ def test_bad_arguments_are_rejected_on_the_host(lib):
     assert rc == -1
     rc = lib.moe_fp4_check(None, None)
     assert rc == -1
+
+
+def test_mxfp8_quantize_rejects_bad_arguments_on_the_host(lib):
+    P = ctypes.c_void_p
+    fake = 0x100000  # never dereferenced: every call below fails its host-side checks
+    q = lib.moe_fp4_mxfp8_quantize
+    assert q(None, 4, 64, P(fake), P(fake), None) == -1           # null x
+    assert q(P(fake), 4, 64, None, P(fake), None) == -1           # null codes
+    assert q(P(fake), 4, 64, P(fake), None, None) == -1           # null scales
+    assert q(P(fake), -1, 64, P(fake), P(fake), None) == -1       # negative rows
+    assert q(P(fake), 4, 48, P(fake), P(fake), None) == -1        # K not a multiple of 32
+    assert q(P(fake), 4, 0, P(fake), P(fake), None) == -1         # K = 0
+    assert q(P(fake + 8), 4, 64, P(fake), P(fake), None) == -1    # misaligned x
+    assert q(P(fake), 4, 64, P(fake + 4), P(fake), None) == -1    # misaligned codes
+    assert q(P(fake), 0, 64, P(fake), P(fake), None) == 0         # no rows: nothing enqueued
+    assert q(None, 0, 64, None, None, None) == 0                  # no rows: pointers not looked at
+    assert q(None, 0, 48, None, None, None) == -1                 # ... but K is still checked
