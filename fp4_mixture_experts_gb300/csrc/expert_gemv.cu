@@ -2,13 +2,15 @@
 // weighted combine.
 //
 // w13_swiglu_rows: one warp per (gate row i, up row I+i) pair and a chunk of
-//   up to 4 token rows of one expert; lanes split K in 32-element MX blocks
+//   up to 8 token rows of one expert; lanes split K in 32-element MX blocks
 //   (16 packed bytes + 1 E8M0 byte), decode E2M1 pairs with the hardware
 //   cvt.rn.f16x2.e2m1x2, accumulate in fp32, reduce across the warp and apply
 //   SwiGLU; h is rounded to bf16 (the layer's one rounding point).
 // w2_rows: the same pattern over W2 rows, fp32 y in sorted-row order.
 // combine: out[t] = sum_j w[t, j] * y[slot_pos[t*k + j]] in slot order
-//   (deterministic: no atomics, the MI250 blog's section 3.2 / 4.2 rule).
+//   (deterministic: no atomics, the MI250 blog's section 3.2 / 4.2 rule);
+//   launched early (programmatic dependent launch), it waits for the W2
+//   kernel before reading y.
 #include <cuda_fp16.h>
 
 #include "moe_fp4_internal.cuh"
