@@ -252,7 +252,7 @@ const char* moe_fp4_status_string(int status) {
     case MOE_FP4_ERR_UNSUPPORTED: return "unsupported sizes";
     case MOE_FP4_ERR_WORKSPACE: return "workspace too small";
     case MOE_FP4_ERR_CUDA: return "CUDA runtime error";
-    case MOE_FP4_ERR_DEVICE: return "a kernel reported an out-of-range index";
+    case MOE_FP4_ERR_DEVICE: return "a kernel reported an error (an out-of-range index or a timed-out wait)";
     default: return "unknown status";
   }
 }

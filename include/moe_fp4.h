@@ -193,10 +193,12 @@ int moe_fp4_forward_noalloc(const moe_fp4_dims* dims, const void* x_bf16, const 
 int moe_fp4_mxfp8_quantize(const void* x_bf16, int64_t rows, int32_t K, uint8_t* codes, uint8_t* scales,
                            void* cuda_stream);
 
-/* Synchronises the stream and reads the device error word of the workspace
- * (set by a kernel that met an index out of range, e.g. a corrupted expert
- * id); returns MOE_FP4_OK, MOE_FP4_ERR_DEVICE or MOE_FP4_ERR_CUDA, and clears
- * the word. */
+/* Synchronises the stream and reads the device error word of the workspace,
+ * which the kernels OR bits into: 1 = an index out of range (e.g. a corrupted
+ * expert id, whose slot is dropped); 2 = a pipeline wait gave up after 2 s
+ * (the kernel skipped the rest of its work, so the outputs are incomplete).
+ * Returns MOE_FP4_OK, MOE_FP4_ERR_DEVICE or MOE_FP4_ERR_CUDA, and clears the
+ * word. */
 int moe_fp4_check(void* workspace, void* cuda_stream);
 
 /* Static text for a status code. */
