@@ -299,22 +299,35 @@ def roofline_prefill(res, pk, src):
             "step_frac": round(step_flops / (res["ms_total"] / res["steps"] * 1e-3) / 1e12 / peak, 4)}
 
 
-def cpu_baseline_sample(name, seconds_target=15.0):
+def cpu_baseline_sample(name, seconds_target=15.0, gpu=None):
     """The oracle, as it stands, on a bounded sample of the workload: whole
-    tokens through oracle.forward_tokens until ~seconds_target elapse."""
+    tokens through oracle.forward_tokens until ~seconds_target elapse.  With
+    `gpu` (numpy out [T, d] and topk_ids [T, k] of the CUDA path on the same
+    layer), the sampled tokens' oracle results are compared with it after the
+    timed loop and reported as "parity"."""
     import oracle
     L = make_config(name)
-    toks = 0
+    toks, outs, ids = [], [], []
     t0 = time.perf_counter()
     for t in range(L.T):
-        oracle.forward_tokens(L.x_bf16, L.router_logits, L.w13, L.w13_scale, L.w2, L.w2_scale, L.k, [t])
-        toks += 1
+        i, _, o = oracle.forward_tokens(L.x_bf16, L.router_logits, L.w13, L.w13_scale, L.w2, L.w2_scale, L.k, [t])
+        toks.append(t)
+        ids.append(i[0])
+        outs.append(o[0])
         if time.perf_counter() - t0 >= seconds_target:
             break
     dt = time.perf_counter() - t0
-    return {"value": round(toks / dt, 4), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
-            "sample": f"{toks} of {L.T} tokens of the {name} layer, one token per oracle call "
-                      f"(numpy fp64, BLAS threads = host cores), {dt:.1f} s"}
+    res = {"value": round(len(toks) / dt, 4), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+           "sample": f"{len(toks)} of {L.T} tokens of the {name} layer, one token per oracle call "
+                     f"(numpy fp64, BLAS threads = host cores), {dt:.1f} s"}
+    if gpu is not None:
+        got = np.asarray(gpu["out"], dtype=np.float64)[toks]
+        want = np.stack(outs)
+        res["parity"] = {"tokens": len(toks),
+                         "topk_ids_equal": bool(np.array_equal(np.asarray(gpu["topk_ids"])[toks], np.stack(ids))),
+                         "rel_l2": float(np.linalg.norm(got - want) / np.linalg.norm(want)),
+                         "max_abs": float(np.abs(got - want).max())}
+    return res
 
 
 def run_ours(args):
@@ -374,7 +387,13 @@ def run_ours(args):
             "stage_ms": {k: round(v, 4) for k, v in pre["stage_ms"].items()},
             "roofline": roofline_prefill(pre, pk, src)}
     if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline_sample("decode", args.cpu_seconds)
+        # one more layer call on the measured decode tensors, checked against the oracle's sample
+        x, logits, w13, w13s, w2, w2s, _ = dec["tensors"]
+        import fp4_mixture_experts_gb300 as moe
+        r = moe.forward(x, logits, w13, w13s, w2, w2s, L.k, return_routing=True)
+        torch.cuda.synchronize()
+        gpu = {"out": r["out"].cpu().numpy(), "topk_ids": r["topk_ids"].cpu().numpy()}
+        line["cpu_baseline"] = cpu_baseline_sample("decode", args.cpu_seconds, gpu)
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
