@@ -47,7 +47,11 @@
  * (moe_fp4_workspace_bytes).  moe_fp4_route and moe_fp4_forward only enqueue
  * work on the given stream and never synchronise.  Calls that use different
  * workspaces may run concurrently; calls sharing a workspace must be ordered
- * on one stream.
+ * on one stream.  Inside a call the kernels after routing are launched with
+ * programmatic dependent launch (each waits on the device for the one before
+ * it); the call as a whole keeps ordinary stream order with the caller's work:
+ * its first kernel starts after everything enqueued before it, and its last
+ * kernel lets no later kernel start early.
  *
  * Errors: every function returns a moe_fp4_status.  Argument checks happen on
  * the host before anything is enqueued; on error nothing is launched.  A
