@@ -50,8 +50,12 @@
  * on one stream.  Inside a call the kernels after routing are launched with
  * programmatic dependent launch (each waits on the device for the one before
  * it); the call as a whole keeps ordinary stream order with the caller's work:
- * its first kernel starts after everything enqueued before it, and its last
- * kernel lets no later kernel start early.
+ * its first kernel starts after everything enqueued before it, and the last
+ * kernel of moe_fp4_forward lets no later kernel start early.  (The routing
+ * kernel of moe_fp4_route, T <= 32, does let a following kernel that the
+ * caller launches early start before it ends; such a kernel must wait on the
+ * device, griddepcontrol.wait, before it reads the routing outputs, as any
+ * early-launched kernel must.)
  *
  * Errors: every function returns a moe_fp4_status.  Argument checks happen on
  * the host before anything is enqueued; on error nothing is launched.  A
