@@ -29,3 +29,24 @@ def test_two_gloo_ranks_take_the_max():
         p.join(timeout=60)
         assert p.exitcode == 0
     assert out == [(0, 2.5, 30.0), (1, 2.5, 30.0)]
+
+
+def test_cpu_baseline_reports_parity_of_a_given_result():
+    """The CPU-baseline leg compares its oracle sample with the CUDA path's result it is given."""
+    import numpy as np
+
+    import bench
+    import oracle
+    from moe_inputs import make_config
+    L = make_config("tiny")
+    ref = oracle.forward(L.x_bf16, L.router_logits, L.w13, L.w13_scale, L.w2, L.w2_scale, L.k)
+    good = {"out": ref["out"].astype(np.float32), "topk_ids": ref["topk_ids"]}
+    r = bench.cpu_baseline_sample("tiny", 0.0, good)
+    p = r["parity"]
+    assert p["tokens"] >= 1 and p["topk_ids_equal"] and p["rel_l2"] < 1e-6 and r["kind"] == "oracle"
+    bad_out = good["out"].copy()
+    bad_out[0] *= 1.1
+    bad_ids = good["topk_ids"].copy()
+    bad_ids[0] = bad_ids[0][::-1]
+    p = bench.cpu_baseline_sample("tiny", 0.0, {"out": bad_out, "topk_ids": bad_ids})["parity"]
+    assert not p["topk_ids_equal"] and p["rel_l2"] > 0.05
