@@ -347,6 +347,22 @@ def run_ours(args):
         pre_steps = max(3, min(args.steps, 50))
         pre = measure_workload("prefill", pre_steps, max(3, min(args.warmup, 5)), dist, local)
         pre["steps"] = pre_steps
+    others = {}
+    for name in [n for n in args.also.split(",") if n]:
+        # further workloads on request (tensor-core path), timed like the prefill workload
+        o_steps = max(3, min(args.steps, 50))
+        res = measure_workload(name, o_steps, max(3, min(args.warmup, 5)), dist, local)
+        res["steps"] = o_steps
+        Lo = res["L"]
+        ms_o = res["ms_total"] / o_steps
+        rf = roofline_prefill(res, pk, src)
+        rf["traffic"] = None  # no ncu capture of this workload
+        others[name] = {"workload": f"{name} MoE layer T={Lo.T} d={Lo.d} I={Lo.I} E={Lo.E} k={Lo.k} (seed 0)",
+                        "value": round(world * Lo.T / (ms_o * 1e-3), 1), "unit": "tokens/s", "steps": o_steps,
+                        "ms_per_step": round(ms_o, 4), "stage_ms": {k: round(v, 4) for k, v in res["stage_ms"].items()},
+                        "roofline": rf}
+        del res
+        torch.cuda.empty_cache()
     if sampler:
         sampler.stop()
     if rank != 0:
@@ -386,6 +402,8 @@ def run_ours(args):
             "ms_per_step": round(ms_pre, 4), "ms_per_step_stream_launch": round(pre["ms_stream"] / pre["steps"], 4),
             "stage_ms": {k: round(v, 4) for k, v in pre["stage_ms"].items()},
             "roofline": roofline_prefill(pre, pk, src)}
+    if others:
+        line["other_workloads"] = others
     if not args.no_cpu_baseline:
         # one more layer call on the measured decode tensors, checked against the oracle's sample
         x, logits, w13, w13s, w2, w2s, _ = dec["tensors"]
@@ -482,6 +500,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-prefill", action="store_true")
+    ap.add_argument("--also", default="", help="comma list of further workloads to time after decode and "
+                    "prefill (skewed, large); reported under other_workloads")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES), default=None,
@@ -489,6 +509,9 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    for n in [n for n in args.also.split(",") if n]:
+        if n not in CONFIGS or n in ("decode", "prefill"):
+            ap.error(f"--also takes workloads other than decode and prefill: {sorted(set(CONFIGS) - {'decode', 'prefill'})}")
     if args.profile_case:
         run_profile_case(args)
     elif args.impl == "reference":
