@@ -170,7 +170,9 @@ int moe_fp4_forward_host(const moe_fp4_dims* dims, const void* x_bf16_host,
  * All calls share the array and it keeps the last call's contents: calls
  * that overlap on the GPU (other streams, other host threads) race and give
  * wrong results; order them on one stream.  Otherwise the same arguments,
- * checks and results as moe_fp4_forward, with no optional outputs. */
+ * checks and results as moe_fp4_forward, with no optional outputs.  The
+ * device error word lives in the internal scratch, which moe_fp4_check cannot
+ * be given: callers that need it use moe_fp4_forward with a workspace. */
 #define MOE_FP4_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 int moe_fp4_forward_noalloc(const moe_fp4_dims* dims, const void* x_bf16, const float* router_logits,
                             const uint8_t* w13, const uint8_t* w13_scale,
