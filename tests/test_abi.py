@@ -102,3 +102,21 @@ def test_mxfp8_quantize_rejects_bad_arguments_on_the_host(lib):
     assert q(P(fake), 0, 64, P(fake), P(fake), None) == 0         # no rows: nothing enqueued
     assert q(None, 0, 64, None, None, None) == 0                  # no rows: pointers not looked at
     assert q(None, 0, 48, None, None, None) == -1                 # ... but K is still checked
+
+
+def test_the_header_and_library_work_from_plain_c(lib):
+    """A C99 program compiled against include/moe_fp4.h and linked with the library."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    libdir = os.path.dirname(moe.lib_path())
+    os.makedirs(os.path.join(libdir, "_build"), exist_ok=True)
+    exe = os.path.join(libdir, "_build", "abi_from_c")
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                        os.path.join(ROOT, "tests", "c", "abi_from_c.c"), "-L", libdir, "-lmoe_fp4",
+                        "-Wl,-rpath," + libdir, "-o", str(exe)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert run.returncode == 0, run.stdout + run.stderr
