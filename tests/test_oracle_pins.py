@@ -493,3 +493,21 @@ def test_planted_unstable_sort_is_caught(monkeypatch):
 def test_planted_missing_h_rounding_is_caught(monkeypatch):
     monkeypatch.setattr(om, "bf16_round", lambda v: np.asarray(v, dtype=np.float64))
     assert _fails(test_hand_worked_layer)
+
+
+def test_planted_e8m0_bias_off_by_one_is_caught(monkeypatch):
+    """The format-dialect bug class: an E8M0 bias of 126 instead of 127 doubles every weight."""
+    def e8m0_bias126(s):
+        s = np.asarray(s).astype(np.int64)
+        return np.where(s == 255, np.nan, np.ldexp(1.0, s - 126))
+    monkeypatch.setattr(om, "e8m0_decode", e8m0_bias126)
+    monkeypatch.setattr(oracle, "e8m0_decode", e8m0_bias126)
+    assert _fails(test_e8m0_is_power_of_two_with_bias_127)
+    assert _fails(test_dequant_matches_element_loops_and_nibble_order)
+    assert _fails(test_hand_worked_layer)
+
+
+def test_planted_silu_sign_is_caught(monkeypatch):
+    monkeypatch.setattr(om, "silu", lambda z: z / (1.0 + np.exp(z)))
+    assert _fails(test_top1_reduces_to_dense_swiglu_mlp)
+    assert _fails(test_forward_equals_dense_brute_force)
