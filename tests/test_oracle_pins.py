@@ -511,3 +511,63 @@ def test_planted_silu_sign_is_caught(monkeypatch):
     monkeypatch.setattr(om, "silu", lambda z: z / (1.0 + np.exp(z)))
     assert _fails(test_top1_reduces_to_dense_swiglu_mlp)
     assert _fails(test_forward_equals_dense_brute_force)
+
+
+def _forward_with(token_of_slot, combine_rows):
+    """oracle.forward with two of its index choices replaced (for planting mistakes)."""
+    def forward(x_bf16, router_logits, w13, w13_scale, w2, w2_scale, k):
+        x = om.bf16_bits_to_f64(x_bf16)
+        T, d = x.shape
+        E, I = w13.shape[0], w13.shape[1] // 2
+        ids, w = om.route(router_logits, k)
+        offsets, sorted_slot, slot_pos = om.expert_sort(ids, E)
+        h, y = np.zeros((T * k, I)), np.zeros((T * k, d))
+        for e in range(E):
+            r0, r1 = int(offsets[e]), int(offsets[e + 1])
+            if r0 < r1:
+                tokens = token_of_slot(sorted_slot[r0:r1], k)
+                h[r0:r1], y[r0:r1] = om.expert_ffn(x[tokens], w13[e], w13_scale[e], w2[e], w2_scale[e])
+        out = np.zeros((T, d))
+        rows = combine_rows(sorted_slot, slot_pos).reshape(T, k)
+        for j in range(k):
+            out += w[:, j:j + 1] * y[rows[:, j]]
+        return dict(topk_ids=ids, topk_w=w, expert_offsets=offsets, sorted_slot=sorted_slot, slot_pos=slot_pos,
+                    h=h, out=out)
+    return forward
+
+
+def test_planted_forward_rewrite_is_faithful(monkeypatch):
+    """the helper above with the right choices reproduces the oracle (so the plants below test one change each)"""
+    f = _forward_with(lambda ss, k: ss // k, lambda ss, pos: pos)
+    L = make_layer(T=10, d=64, I=32, E=5, k=2, seed=7)
+    a = f(L.x_bf16, L.router_logits, L.w13, L.w13_scale, L.w2, L.w2_scale, L.k)["out"]
+    assert np.array_equal(a, run(L)["out"])
+
+
+def test_planted_wrong_token_of_slot_is_caught(monkeypatch):
+    f = _forward_with(lambda ss, k: ss % k, lambda ss, pos: pos)
+    monkeypatch.setattr(om, "forward", f)
+    monkeypatch.setattr(oracle, "forward", f)
+    assert _fails(test_forward_equals_dense_brute_force)
+
+
+def test_planted_combine_through_the_wrong_permutation_is_caught(monkeypatch):
+    f = _forward_with(lambda ss, k: ss // k, lambda ss, pos: ss)
+    monkeypatch.setattr(om, "forward", f)
+    monkeypatch.setattr(oracle, "forward", f)
+    assert _fails(test_forward_equals_dense_brute_force)
+
+
+def test_planted_bf16_round_half_away_is_caught(monkeypatch):
+    def away(v):
+        v = np.asarray(v, dtype=np.float64)
+        out = np.zeros_like(v)
+        nz = (v != 0) & np.isfinite(v)
+        a = np.abs(v[nz])
+        _, ex = np.frexp(a)
+        ulp = np.ldexp(1.0, np.maximum(ex - 1, -126) - 7)
+        out[nz] = np.copysign(np.floor(a / ulp + 0.5) * ulp, v[nz])
+        return out
+    monkeypatch.setattr(om, "bf16_round", away)
+    monkeypatch.setattr(oracle, "bf16_round", away)
+    assert _fails(test_bf16_round_matches_torch_on_fp32_values)
