@@ -261,3 +261,17 @@ def test_planted_missing_h_quantisation_is_caught(monkeypatch):
         return h, h, h @ om.dequantize_rows(w2_e, w2s_e).T     # wrong: W2 reads h unquantised
     monkeypatch.setattr(mx, "expert_ffn_mx", ffn)
     assert _fails(test_forward_mx_equals_dense_brute_force)
+
+
+def test_planted_row_wide_scale_is_caught(monkeypatch):
+    """one scale per row instead of one per 32-element block"""
+    def per_row(rows):
+        rows = np.asarray(rows, dtype=np.float64)
+        R, K = rows.shape
+        amax = np.abs(rows).max(axis=1, keepdims=True)
+        _, ex = np.frexp(np.where(amax > 0, amax, 1.0))
+        shared = np.clip(np.where(amax > 0, ex - 1 - mx.E4M3_EMAX, -127), -127, 127)
+        q = mx.e4m3_round(rows / np.ldexp(1.0, shared))
+        return mx.e4m3_encode(q), np.repeat(shared + 127, K // 32, axis=1).astype(np.uint8)
+    monkeypatch.setattr(mx, "mxfp8_quantize", per_row)
+    assert _fails(test_mx_quantize_matches_exhaustive_nearest_search)
