@@ -4,7 +4,9 @@ One step = one pass of the whole layer (routing, expert sort, W13 + SwiGLU,
 W2, combine) over one batch of synthetic inputs resident in HBM.  The
 default workload is the decode-shaped layer (T=32, d=4096, I=2048, E=256,
 k=8); the prefill-shaped layer (T=4608) is measured the same way and
-reported in the "prefill" object of the same line.  Every expert weight
+reported in the "prefill" object of the same line, the skewed-routing
+(T=2048) and large (T=16384, d=7168) layers under "other_workloads", and
+the MXFP8 activation quantiser under "mxfp8_quantize".  Every expert weight
 set touched per step (~2.2 GB decode, 3.4 GB prefill) is far larger than
 L2 (129 MB), so no L2 flush is needed between steps.
 
@@ -107,7 +109,10 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
-    def summary(self, t0, t1):
+    def summary(self, windows):
+        """clocks over the samples taken inside the timed regions `windows`
+        [(t0, t1), ...]; if none landed inside (short regions), the samples
+        within 0.3 s of them"""
         rows = []
         for ts, ln in self.lines:
             parts = [p.strip() for p in ln.split(",")]
@@ -117,8 +122,8 @@ class ClockSampler:
                 rows.append((ts, float(parts[2]), float(parts[3]), parts[5:]))
             except ValueError:
                 continue
-        inside = [r for r in rows if t0 <= r[0] <= t1]
-        window = inside if inside else [r for r in rows if t0 - 0.3 <= r[0] <= t1 + 0.3]
+        inside = [r for r in rows if any(t0 <= r[0] <= t1 for t0, t1 in windows)]
+        window = inside if inside else [r for r in rows if any(t0 - 0.3 <= r[0] <= t1 + 0.3 for t0, t1 in windows)]
         if not window:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
@@ -128,7 +133,8 @@ class ClockSampler:
                 if v.lower().startswith("active"):
                     reasons.add(name)
         return {"sm_mhz": float(np.median([r[1] for r in window])), "sm_max_mhz": max(r[2] for r in window),
-                "reasons": sorted(reasons), "samples": len(inside)}
+                "reasons": sorted(reasons), "samples": len(inside),
+                "window": "inside the timed regions of all workloads" if inside else "within 0.3 s of them"}
 
 
 # ----------------------------------------------------------------------------
@@ -211,6 +217,7 @@ def measure_workload(name, steps, warmup, dist, local, sampler=None):
     barrier(dist)
     t_wall1 = time.time()
     ms_stream = start.elapsed_time(end)
+    windows = [(t_wall0, t_wall1)]
     stage_ms = {name_: float(np.mean([evs[s][i].elapsed_time(evs[s][i + 1]) for s in range(steps)]))
                 for i, name_ in enumerate(STAGES)}
     # the same layer call captured once in a CUDA graph and replayed: the
@@ -234,9 +241,10 @@ def measure_workload(name, steps, warmup, dist, local, sampler=None):
     barrier(dist)
     t_wall1 = time.time()
     ms_graph = start.elapsed_time(end)
+    windows.append((t_wall0, t_wall1))
     res = dict(L=L, touched=touched, ms_total=max_over_ranks(dist, ms_graph),
                ms_stream=max_over_ranks(dist, ms_stream), stage_ms=stage_ms,
-               t_wall=(t_wall0, t_wall1), tensors=(x, logits, w13, w13s, w2, w2s, ws), graph=graph)
+               windows=windows, tensors=(x, logits, w13, w13s, w2, w2s, ws), graph=graph)
     return res
 
 
@@ -285,18 +293,58 @@ def roofline_decode(res, pk, src):
 
 
 def roofline_prefill(res, pk, src):
+    """Dominant kernel of the tensor-core path: W13 + SwiGLU (2/3 of the FLOPs).
+    The timed region lasts tens of milliseconds at full clock, so the peak is
+    the burst figure (cuBLAS bf16, best of 10); the sustained figure (a 4 s
+    loop under the power cap) is reported beside it."""
     L = res["L"]
     st = res["stage_ms"]
     flops_w13 = 4.0 * L.T * L.k * L.d * L.I
     ach = flops_w13 / (st["w13_swiglu"] * 1e-3) / 1e12
-    peak = pk.get("bf16_tflops_sustained", pk["bf16_tflops"])
+    peak = pk["bf16_tflops"]
     step_flops = 6.0 * L.T * L.k * L.d * L.I
-    return {"bound": "tensor", "kernel": "w13_swiglu", "achieved": round(ach, 1), "peak": peak,
-            "unit": "TFLOP/s", "frac": round(ach / peak, 4),
-            "traffic": ncu_traffic("tc_kernel<W13>@prefill"),
-            "peak_source": f"{src} bf16_tflops_sustained (cuBLAS bf16 loop)",
-            "flops_per_launch": flops_w13,
-            "step_frac": round(step_flops / (res["ms_total"] / res["steps"] * 1e-3) / 1e12 / peak, 4)}
+    step_ach = step_flops / (res["ms_total"] / res["steps"] * 1e-3) / 1e12
+    out = {"bound": "tensor", "kernel": "w13_swiglu", "achieved": round(ach, 1), "peak": peak,
+           "unit": "TFLOP/s", "frac": round(ach / peak, 4),
+           "traffic": None,
+           "peak_source": f"{src} bf16_tflops (cuBLAS bf16 burst, the kernel is timed in a short run)",
+           "flops_per_launch": flops_w13,
+           "step_frac": round(step_ach / peak, 4)}
+    if "bf16_tflops_sustained" in pk:
+        out["frac_of_sustained"] = round(ach / pk["bf16_tflops_sustained"], 4)
+    return out
+
+
+def measure_mxfp8(local, warmup=5, iters=50):
+    """The MXFP8 activation quantiser on the prefill layer's permuted-activation
+    shape (36,864 x 4096 bf16, 302 MB: larger than L2), CUDA events over
+    `iters` back-to-back calls; bytes = 2 read + 1 + 1/32 written per element."""
+    import torch
+
+    import fp4_mixture_experts_gb300 as moe
+    R, K = 36864, 4096
+    dev = torch.device("cuda", local)
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    x = torch.randn(R, K, device=dev, generator=g).to(torch.bfloat16)
+    codes = torch.empty(R, K, dtype=torch.uint8, device=dev)
+    scales = torch.empty(R, K // 32, dtype=torch.uint8, device=dev)
+    for _ in range(warmup):
+        moe.mxfp8_quantize(x, codes, scales)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    start.record()
+    for _ in range(iters):
+        moe.mxfp8_quantize(x, codes, scales)
+    end.record()
+    torch.cuda.synchronize()
+    t1 = time.time()
+    ms = start.elapsed_time(end) / iters
+    nbytes = R * K * 2 + R * K + R * K // 32
+    del x, codes, scales
+    return {"shape": [R, K], "us_per_call": round(ms * 1e3, 2), "bytes_per_call": nbytes,
+            "achieved_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}, (t0, t1)
 
 
 def cpu_baseline_sample(name, seconds_target=15.0, gpu=None):
@@ -337,32 +385,41 @@ def run_ours(args):
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
         sampler.start()
+    windows = []
     dec = measure_workload("decode", args.steps, args.warmup, dist, local)
     dec["steps"] = args.steps
-    t0, t1 = dec["t_wall"]
-    clocks = sampler.summary(t0, t1) if sampler else None
+    windows += dec["windows"]
     e2e_dt, h2d, d2h = measure_e2e(dec, args.steps, args.warmup, dist, local)
     pre = None
     if not args.no_prefill:
         pre_steps = max(3, min(args.steps, 50))
         pre = measure_workload("prefill", pre_steps, max(3, min(args.warmup, 5)), dist, local)
         pre["steps"] = pre_steps
+        windows += pre["windows"]
     others = {}
     for name in [n for n in args.also.split(",") if n]:
-        # further workloads on request (tensor-core path), timed like the prefill workload
+        # further workloads (tensor-core path), timed like the prefill workload
         o_steps = max(3, min(args.steps, 50))
         res = measure_workload(name, o_steps, max(3, min(args.warmup, 5)), dist, local)
         res["steps"] = o_steps
+        windows += res["windows"]
         Lo = res["L"]
         ms_o = res["ms_total"] / o_steps
         rf = roofline_prefill(res, pk, src)
-        rf["traffic"] = None  # no ncu capture of this workload
         others[name] = {"workload": f"{name} MoE layer T={Lo.T} d={Lo.d} I={Lo.I} E={Lo.E} k={Lo.k} (seed 0)",
                         "value": round(world * Lo.T / (ms_o * 1e-3), 1), "unit": "tokens/s", "steps": o_steps,
-                        "ms_per_step": round(ms_o, 4), "stage_ms": {k: round(v, 4) for k, v in res["stage_ms"].items()},
+                        "ms_per_step": round(ms_o, 4), "touched_experts": res["touched"],
+                        "stage_ms": {k: round(v, 4) for k, v in res["stage_ms"].items()},
                         "roofline": rf}
         del res
         torch.cuda.empty_cache()
+    mxq = None
+    if rank == 0 and not args.no_mxfp8:
+        mxq, win = measure_mxfp8(local)
+        windows.append(win)
+        mxq["frac"] = round(mxq["achieved_gbs"] / pk["hbm_gbs"], 4)
+        mxq["peak_gbs"] = pk["hbm_gbs"]
+    clocks = sampler.summary(windows) if sampler else None
     if sampler:
         sampler.stop()
     if rank != 0:
@@ -396,14 +453,18 @@ def run_ours(args):
     if pre is not None:
         P = pre["L"]
         ms_pre = pre["ms_total"] / pre["steps"]
+        rf = roofline_prefill(pre, pk, src)
+        rf["traffic"] = ncu_traffic("tc_kernel<W13>@prefill")
         line["prefill"] = {
             "workload": "prefill-shaped MoE layer T=4608 d=4096 I=2048 E=256 k=8 (seed 0)",
             "value": round(world * P.T / (ms_pre * 1e-3), 1), "unit": "tokens/s", "steps": pre["steps"],
             "ms_per_step": round(ms_pre, 4), "ms_per_step_stream_launch": round(pre["ms_stream"] / pre["steps"], 4),
             "stage_ms": {k: round(v, 4) for k, v in pre["stage_ms"].items()},
-            "roofline": roofline_prefill(pre, pk, src)}
+            "roofline": rf}
     if others:
         line["other_workloads"] = others
+    if mxq is not None:
+        line["mxfp8_quantize"] = mxq
     if not args.no_cpu_baseline:
         # one more layer call on the measured decode tensors, checked against the oracle's sample
         x, logits, w13, w13s, w2, w2s, _ = dec["tensors"]
@@ -500,8 +561,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-prefill", action="store_true")
-    ap.add_argument("--also", default="", help="comma list of further workloads to time after decode and "
-                    "prefill (skewed, large); reported under other_workloads")
+    ap.add_argument("--also", default="skewed,large", help="comma list of further workloads to time after "
+                    "decode and prefill (skewed, large; '' for none); reported under other_workloads")
+    ap.add_argument("--no-mxfp8", action="store_true", help="skip timing the MXFP8 activation quantiser")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES), default=None,

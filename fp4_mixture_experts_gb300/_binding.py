@@ -15,6 +15,10 @@ _LIB_NAME = "libmoe_fp4.so"
 FLAG_FORCE_GEMV = 0x1
 FLAG_FORCE_TC = 0x2
 
+FAULT_NONE = 0
+FAULT_TC_TOKEN_TILE = 1
+FAULT_STREAM_STAGE = 2
+
 EXPORTED_SYMBOLS = (
     "moe_fp4_workspace_bytes",
     "moe_fp4_host_workspace_bytes",
@@ -23,6 +27,8 @@ EXPORTED_SYMBOLS = (
     "moe_fp4_forward_profiled",
     "moe_fp4_forward_host",
     "moe_fp4_forward_noalloc",
+    "moe_fp4_noalloc_check",
+    "moe_fp4_set_fault_injection",
     "moe_fp4_mxfp8_quantize",
     "moe_fp4_check",
     "moe_fp4_status_string",
@@ -73,6 +79,10 @@ def load_library():
     lib.moe_fp4_forward_host.restype = ctypes.c_int
     lib.moe_fp4_forward_noalloc.argtypes = [pd, P, P, P, P, P, P, P, ctypes.c_uint, P]
     lib.moe_fp4_forward_noalloc.restype = ctypes.c_int
+    lib.moe_fp4_noalloc_check.argtypes = [P]
+    lib.moe_fp4_noalloc_check.restype = ctypes.c_int
+    lib.moe_fp4_set_fault_injection.argtypes = [ctypes.c_int, ctypes.c_uint32]
+    lib.moe_fp4_set_fault_injection.restype = ctypes.c_int
     lib.moe_fp4_mxfp8_quantize.argtypes = [P, ctypes.c_int64, ctypes.c_int32, P, P, P]
     lib.moe_fp4_mxfp8_quantize.restype = ctypes.c_int
     lib.moe_fp4_check.argtypes = [P, P]
@@ -256,7 +266,24 @@ def forward_noalloc(x_bf16, router_logits, w13, w13_scale, w2, w2_scale, k: int,
 
 
 def check(workspace, stream=None) -> None:
-    """Synchronise and raise if a kernel reported an out-of-range index."""
+    """Synchronise and raise if a kernel of an earlier call on this workspace
+    reported an error (bit 1: an out-of-range expert index; bit 2: a pipeline
+    wait that ran out); the error word is cleared."""
     rc = load_library().moe_fp4_check(_ptr(workspace), _stream(stream))
     if rc != 0:
         raise MoeFp4Error(rc, "moe_fp4_check")
+
+
+def noalloc_check(stream=None) -> None:
+    """check() for the internal scratch of forward_noalloc."""
+    rc = load_library().moe_fp4_noalloc_check(_stream(stream))
+    if rc != 0:
+        raise MoeFp4Error(rc, "moe_fp4_noalloc_check")
+
+
+def set_fault_injection(site: int, wait_limit_us: int = 0) -> None:
+    """Plant a host-chosen fault in later forward calls (failure-path tests
+    only; see moe_fp4_set_fault_injection).  FAULT_NONE restores normal runs."""
+    rc = load_library().moe_fp4_set_fault_injection(int(site), int(wait_limit_us))
+    if rc != 0:
+        raise MoeFp4Error(rc, "moe_fp4_set_fault_injection")

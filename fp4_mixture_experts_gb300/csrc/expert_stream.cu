@@ -28,7 +28,8 @@
 //     writes fp32 y.
 // Waits are bounded; a timeout raises the CTA abort flag, after which every
 // warp runs the same loop without waiting or computing, so all barriers are
-// still met and the kernel exits.
+// still met and the kernel exits; the producer waits (also bounded) for its
+// copies in flight before it leaves.
 #include <cuda_fp16.h>
 
 #include "moe_fp4_internal.cuh"
@@ -66,6 +67,8 @@ struct StreamParams {
   int n_rb;                // row blocks per expert
   int stages;              // ring depth
   int x_pitch;             // bytes per token row of the f16 activation buffer
+  uint64_t wait_ns;        // limit of every mbarrier wait
+  int fault;               // nonzero: CTA 0 withholds its first weight stage (fault-injection test)
 };
 
 __device__ __forceinline__ uint32_t e2m1x2_h2(uint32_t byte) { return e2m1x2_to_f16x2(byte); }
@@ -161,19 +164,40 @@ stream_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__
       const uint64_t pol = l2_evict_first_policy();
       int slot = 0;
       uint32_t phase = 0;
-      for (long long it = it0; it < it1; ++it) {
+      uint32_t nxt = 0;    // bit s: parity of the next copy into slot s (its full-barrier phase)
+      uint32_t has = 0;    // bit s: slot s received a copy
+      bool withhold = P.fault != 0 && blockIdx.x == 0;
+      bool ok = true;
+      for (long long it = it0; it < it1 && ok; ++it) {
         const int c = (int)(it / P.n_rb), rb = (int)(it % P.n_rb);
         const int e = __ldcg(P.chunks + c).x;
         for (int ks = 0; ks < nst; ++ks) {
-          if (!mbar_wait(&empty[slot], phase ^ 1u, abort_flag, P.err, kErrWaitTimeout)) break;
-          issue_stage<W13>(&map_w, &map_s, P, e, rb, ks, ring + (size_t)slot * kStageBytes, &full[slot], pol);
+          if (!mbar_wait(&empty[slot], phase ^ 1u, abort_flag, P.err, kErrWaitTimeout, P.wait_ns) || *abort_flag) {
+            ok = false;
+            break;
+          }
+          // one copy per slot in flight: after an abort a slot may come back
+          // before its previous copy landed (a no-op wait otherwise)
+          if ((has >> slot) & 1)
+            mbar_wait_drain(&full[slot], ((nxt >> slot) & 1) ^ 1u, P.err, kErrWaitTimeout, P.wait_ns);
+          if (withhold) {
+            // fault injection: this stage never arrives, so the consumers'
+            // wait on it runs out and the kernel takes its abort path
+            withhold = false;
+          } else {
+            issue_stage<W13>(&map_w, &map_s, P, e, rb, ks, ring + (size_t)slot * kStageBytes, &full[slot], pol);
+            nxt ^= 1u << slot;
+            has |= 1u << slot;
+          }
           if (++slot == P.stages) {
             slot = 0;
             phase ^= 1u;
           }
         }
-        if (*abort_flag) break;
       }
+      // every issued copy has landed before the CTA may exit
+      for (int q = 0; q < P.stages; ++q)
+        if ((has >> q) & 1) mbar_wait_drain(&full[q], ((nxt >> q) & 1) ^ 1u, P.err, kErrWaitTimeout, P.wait_ns);
     }
     return;
   }
@@ -238,11 +262,14 @@ stream_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__
       asm volatile("bar.sync 1, %0;" ::"r"(kConsWarps * 32) : "memory");
       cur = c;
     }
-    const bool run = !*abort_flag;
+    // wait outcomes are made uniform over the warp, so that the warp-wide
+    // mma.sync below sees all 32 lanes or none
+    const bool run = __all_sync(0xFFFFFFFFu, !*abort_flag);
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     const uint8_t* xg = xs_buf + (size_t)g * P.x_pitch + 16 * t;  // token g, this thread's 8 elements
     for (int ks = 0; ks < nst; ++ks) {
-      const bool ok = run && mbar_wait(&full[slot], phase, abort_flag, P.err, kErrWaitTimeout);
+      const bool ok =
+          run && __all_sync(0xFFFFFFFFu, mbar_wait(&full[slot], phase, abort_flag, P.err, kErrWaitTimeout, P.wait_ns));
       if (ok) {
         const uint8_t* st = ring + (size_t)slot * kStageBytes;
         // packed rows: two 128-byte-swizzled boxes (K 0..255, 256..511) of 128 (or 2 x 64) rows
@@ -353,11 +380,8 @@ cudaError_t launch_stream(const CUtensorMap& mw, const CUtensorMap& ms, StreamPa
   while (P.stages > 2 && smem_needed(P.stages, P.x_pitch) > 227 * 1024) --P.stages;
   const size_t smem = smem_needed(P.stages, P.x_pitch);
   if (smem > 227 * 1024) return cudaErrorInvalidValue;
-  static bool configured = false;
-  if (!configured) {
-    cudaFuncSetAttribute(stream_kernel<W13>, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    configured = true;
-  }
+  const cudaError_t oe = ensure_smem_optin(reinterpret_cast<const void*>(stream_kernel<W13>), 227 * 1024);
+  if (oe != cudaSuccess) return oe;
   return launch_early(stream_kernel<W13>, dim3(num_sms()), dim3(kThreads), smem, st, mw, ms, P);
 }
 
@@ -390,6 +414,8 @@ cudaError_t launch_stream_w13(const moe_fp4_dims& d, const uint16_t* x, const ui
   P.I = d.I;
   P.K = d.d;
   P.n_rb = d.I / 64;
+  P.wait_ns = wait_limit_ns();
+  P.fault = fault_site() == MOE_FP4_FAULT_STREAM_STAGE;
   return launch_stream<true>(mw, ms, P, st);
 }
 
@@ -414,6 +440,8 @@ cudaError_t launch_stream_w2(const moe_fp4_dims& d, const uint8_t* w2, const uin
   P.I = d.I;
   P.K = d.I;
   P.n_rb = d.d / 128;
+  P.wait_ns = wait_limit_ns();
+  P.fault = 0;
   return launch_stream<false>(mw, ms, P, st);
 }
 

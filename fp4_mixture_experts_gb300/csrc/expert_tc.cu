@@ -31,9 +31,10 @@
 //               tcgen05.st (lane = weight row), so that the MMA reads its A
 //               operand from tensor memory; then the epilogue (tcgen05.ld,
 //               SwiGLU + bf16 rounding of h, or y)
-// A stage is full once the token tile has landed and all 8 dequantisers have
-// written their A slots (one mbarrier), and empty once both issuers' MMAs on
-// it have completed (one mbarrier, two tcgen05.commit arrivals).
+// A stage is full once its token tile has landed (one mbarrier, completed by
+// the TMA byte count) and all 8 dequantisers have written their A slots (a
+// second one), and empty once both issuers' MMAs on it have completed (one
+// mbarrier, two tcgen05.commit arrivals).
 // Weights are dequantised exactly (an E2M1 value times a power of two has
 // 2 significant bits), so the MMA multiplies exact products and accumulates
 // them in fp32.  Operands are f16: the weight row is scaled by 2^(s - s_ref)
@@ -41,7 +42,10 @@
 // (x for W13; the f16 copy of h for W2) by a power of two of its own; both
 // factors come back in the epilogue.  Every mbarrier wait is bounded; a
 // timeout sets the error word and an abort flag that releases the other
-// roles, and TMEM is always freed.
+// roles.  On the way out every TMA copy a producer issued has landed and
+// every MMA an issuer issued has completed (waits that ignore the abort flag,
+// also bounded) before shared and tensor memory are given back, and TMEM is
+// always freed.
 #include <cuda.h>
 
 #include <algorithm>
@@ -96,7 +100,7 @@ constexpr int kOffRaw = kOffB + kStages * kBTileBytes;         // [stage][acc]
 constexpr int kOffRowscale = kOffRaw + kStagesRaw * 2 * kRawTileBytes;
 constexpr int kOffBar = kOffRowscale + 2 * kBM * 4;
 constexpr int kSmemTc = kOffBar + 512 + 1024;  // + barriers, 1 KB alignment slack
-static_assert((2 * kStagesRaw + 2 * kStages + 2) * 8 + 8 <= 512, "barrier area exceeded");
+static_assert((2 * kStagesRaw + 3 * kStages + 4) * 8 + 8 <= 512, "barrier area exceeded");
 static_assert(kSmemTc <= 227 * 1024, "shared memory of the tensor-core kernel exceeds 227 KB");
 static_assert(kBTileBytes % 1024 == 0, "token slots must stay 1 KB aligned for the 128-byte swizzle");
 
@@ -115,6 +119,8 @@ struct TcParams {
   int block_rows;          // weight rows advanced per m-block (128 W13, 256 W2)
   int acc1_offset;         // row offset of accumulator 1 (I for up rows, 128 for W2)
   int I, d;
+  uint64_t wait_ns;        // limit of every mbarrier wait
+  int fault;               // nonzero: CTA 0 withholds its first token tile (fault-injection test)
 };
 
 // UMMA shared-memory descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
@@ -256,12 +262,15 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
   float* rowscale = reinterpret_cast<float*>(smem + kOffRowscale);  // [2][128]
   uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint64_t* raw_empty = raw_full + kStagesRaw;
-  uint64_t* full = raw_empty + kStagesRaw;    // [stage]: token tile landed and both A slots written
-  uint64_t* empty = full + kStages;           // [stage]: the MMAs of both accumulators on it completed
+  uint64_t* bfull = raw_empty + kStagesRaw;   // [stage]: token tile landed (TMA byte count)
+  uint64_t* afull = bfull + kStages;          // [stage]: all 8 dequantisers wrote their A slots
+  uint64_t* empty = afull + kStages;          // [stage]: the MMAs of both accumulators on it completed
   uint64_t* acc_full = empty + kStages;       // per item: both accumulators final
   uint64_t* acc_empty = acc_full + 1;         // per item: the epilogue has read the accumulators
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acc_empty + 1);
+  uint64_t* mma_done = acc_empty + 1;         // [2]: every MMA of that issuer completed (on the way out)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint64_t lim = P.wait_ns;
 
   const int items = P.counts[2] * P.mblocks;
   if ((int)blockIdx.x >= items) return;
@@ -275,11 +284,14 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
       mbar_init(&raw_empty[s], kDqWarps);
     }
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], kDqWarps + 1);  // the dequantisers and the token producer's expect_tx
+      mbar_init(&bfull[s], 1);            // the token producer's expect_tx
+      mbar_init(&afull[s], kDqWarps);     // one arrival per dequantiser warp
       mbar_init(&empty[s], 2);            // one commit per MMA issuer
     }
     mbar_init(acc_full, 2);
     mbar_init(acc_empty, kDqWarps);
+    mbar_init(&mma_done[0], 1);
+    mbar_init(&mma_done[1], 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -306,38 +318,60 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
         const TcItem t = tc_item(P, it);
         for (int rs = 0; rs < nrs; ++rs, ++g) {
           const int s = g % kStagesRaw;
-          if (!mbar_wait(&raw_empty[s], ((g / kStagesRaw) & 1) ^ 1u, abort_flag, P.err, kErrWaitTimeout)) {
+          if (!mbar_wait(&raw_empty[s], ((g / kStagesRaw) & 1) ^ 1u, abort_flag, P.err, kErrWaitTimeout, lim) ||
+              *abort_flag) {
             ok = false;
             break;
           }
+          // one copy per slot in flight: after an abort the slot may come back
+          // before its previous copy landed (a no-op wait otherwise)
+          if (g >= kStagesRaw) mbar_wait_drain(&raw_full[s], ((g / kStagesRaw) & 1) ^ 1u, P.err, kErrWaitTimeout, lim);
           mbar_expect_tx(&raw_full[s], 2 * kRawTileBytes);
           uint8_t* raw = smem + kOffRaw + s * 2 * kRawTileBytes;
           tma_load_2d_hint(raw, &map_raw, rs * kRawRowBytes, t.wrow0, &raw_full[s], pol);
           tma_load_2d_hint(raw + kRawTileBytes, &map_raw, rs * kRawRowBytes, t.wrow0 + P.acc1_offset, &raw_full[s], pol);
         }
       }
+      // every issued copy has landed before the CTA may exit
+      for (uint32_t q = g > kStagesRaw ? g - kStagesRaw : 0; q < g; ++q)
+        mbar_wait_drain(&raw_full[q % kStagesRaw], (q / kStagesRaw) & 1, P.err, kErrWaitTimeout, lim);
     }
   } else if (warp == kBWarp) {
     // ---------------- TMA producer: token tiles ----------------
     if (lane == 0) {
-      uint32_t ph = 0;
+      uint32_t ph = 0;     // bit s: parity of slot s's next use
+      uint32_t nxt = 0;    // bit s: parity of the next copy into slot s (its bfull phase)
+      uint32_t has = 0;    // bit s: slot s received a copy
+      bool withhold = P.fault != 0 && blockIdx.x == 0;
       bool ok = true;
       for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
         const TcItem t = tc_item(P, it);
         const int boxes = (t.n_mma + kBBoxRows - 1) / kBBoxRows;
         for (int ks = 0; ks < nk; ++ks) {
           const int s = ks % t.nS;
-          if (!mbar_wait(&empty[s], ((ph >> s) & 1) ^ 1u, abort_flag, P.err, kErrWaitTimeout)) {
+          if (!mbar_wait(&empty[s], ((ph >> s) & 1) ^ 1u, abort_flag, P.err, kErrWaitTimeout, lim) || *abort_flag) {
             ok = false;
             break;
           }
           ph ^= 1u << s;
-          mbar_expect_tx(&full[s], boxes * kBBoxBytes);
+          // one copy per slot in flight (see the packed-weight producer)
+          if ((has >> s) & 1) mbar_wait_drain(&bfull[s], ((nxt >> s) & 1) ^ 1u, P.err, kErrWaitTimeout, lim);
+          if (withhold) {
+            // fault injection: this tile never arrives, so the MMA issuers'
+            // wait on it runs out and the kernel takes its abort path
+            withhold = false;
+            continue;
+          }
+          mbar_expect_tx(&bfull[s], boxes * kBBoxBytes);
           uint8_t* b = smem + kOffB + s * kBTileBytes;
           for (int i = 0; i < boxes; ++i)
-            tma_load_2d(b + i * kBBoxBytes, &map_b, ks * kBK, t.row0 + i * kBBoxRows, &full[s]);
+            tma_load_2d(b + i * kBBoxBytes, &map_b, ks * kBK, t.row0 + i * kBBoxRows, &bfull[s]);
+          nxt ^= 1u << s;
+          has |= 1u << s;
         }
       }
+      for (int s = 0; s < kStages; ++s)
+        if ((has >> s) & 1) mbar_wait_drain(&bfull[s], ((nxt >> s) & 1) ^ 1u, P.err, kErrWaitTimeout, lim);
     }
   } else if (warp == kMmaWarp || warp == kMma1Warp) {
     // ---------------- MMA issuers, one per accumulator ----------------
@@ -349,12 +383,14 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
       for (int it = blockIdx.x; it < items && ok; it += gridDim.x, ++li) {
         const TcItem t = tc_item(P, it);
         // the epilogue of the previous item must have read the accumulators
-        if (li > 0 && !mbar_wait(acc_empty, (li - 1) & 1, abort_flag, P.err, kErrWaitTimeout)) break;
+        if (li > 0 && !mbar_wait(acc_empty, (li - 1) & 1, abort_flag, P.err, kErrWaitTimeout, lim)) break;
         const uint32_t idesc = idesc_f16kind(kBM, t.n_mma, 0u);
         const uint32_t d_tmem = tmem + t.acc0 + acc * t.acc_cols;
         for (int ks = 0; ks < nk; ++ks) {
           const int s = ks % t.nS;
-          if (!mbar_wait(&full[s], (ph >> s) & 1, abort_flag, P.err, kErrWaitTimeout)) {
+          const uint32_t par = (ph >> s) & 1;
+          if (!mbar_wait(&bfull[s], par, abort_flag, P.err, kErrWaitTimeout, lim) ||
+              !mbar_wait(&afull[s], par, abort_flag, P.err, kErrWaitTimeout, lim)) {
             ok = false;
             break;
           }
@@ -367,10 +403,13 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
             umma_tmem_a(d_tmem, a_tmem + kk * 8, desc_sw128(b_addr + kk * 32), idesc, (ks > 0 || kk > 0) ? 1u : 0u);
           umma_commit(&empty[s]);
         }
+        if (!ok) break;
         umma_commit(acc_full);
       }
-      // the last accumulators must be final before TMEM can be freed, also on an abort
-      if (li > 0) mbar_wait(acc_full, (li - 1) & 1, abort_flag, P.err, kErrWaitTimeout);
+      // every MMA this thread issued has completed before TMEM can be freed,
+      // also on an abort (a commit with nothing outstanding arrives at once)
+      umma_commit(&mma_done[acc]);
+      mbar_wait_drain(&mma_done[acc], 0, P.err, kErrWaitTimeout, lim);
     }
   } else {
     // ---------------- dequantisers (one weight row each), then the epilogue ----------------
@@ -430,7 +469,11 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
         const int sub = ks % kRawSteps;
         const uint32_t gs = g + ks / kRawSteps;
         const int rs_slot = gs % kStagesRaw;
-        if (sub == 0 && !mbar_wait(&raw_full[rs_slot], (gs / kStagesRaw) & 1, abort_flag, P.err, kErrWaitTimeout)) {
+        // every wait's outcome is made uniform over the warp, so that the
+        // warp-wide tcgen05 instructions below see all 32 lanes or none
+        if (sub == 0 &&
+            !__all_sync(0xFFFFFFFFu, mbar_wait(&raw_full[rs_slot], (gs / kStagesRaw) & 1, abort_flag, P.err,
+                                                kErrWaitTimeout, lim))) {
           ok = false;
           break;
         }
@@ -454,7 +497,8 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
           sc = sc_next;
           if (ks + 1 < nk) sc_next = *reinterpret_cast<const uint16_t*>(srow + 2 * (ks + 1));
         }
-        if (!mbar_wait(&empty[sa], ((ph >> sa) & 1) ^ 1u, abort_flag, P.err, kErrWaitTimeout)) {
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&empty[sa], ((ph >> sa) & 1) ^ 1u, abort_flag, P.err, kErrWaitTimeout,
+                                                lim))) {
           ok = false;
         } else {
           ph ^= 1u << sa;
@@ -477,7 +521,7 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
           asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
           asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
           __syncwarp();
-          if (lane == 0) mbar_arrive(&full[sa]);
+          if (lane == 0) mbar_arrive(&afull[sa]);
         }
       }
       g += nrs;
@@ -495,7 +539,7 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
       }
       // the row scales written above must be visible to every epilogue warp
       asm volatile("bar.sync 1, %0;" ::"r"(kDqWarps * 32) : "memory");
-      if (ok && mbar_wait(acc_full, li & 1, abort_flag, P.err, kErrWaitTimeout)) {
+      if (ok && __all_sync(0xFFFFFFFFu, mbar_wait(acc_full, li & 1, abort_flag, P.err, kErrWaitTimeout, lim))) {
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const float rs0 = rowscale[r], rs1 = rowscale[128 + r];
 #pragma unroll
@@ -563,11 +607,8 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
 
 template <bool W13>
 cudaError_t launch_tc(const CUtensorMap& b, const CUtensorMap& raw, const TcParams& P, int max_tiles, cudaStream_t st) {
-  static bool configured = false;
-  if (!configured) {
-    cudaFuncSetAttribute(tc_kernel<W13>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemTc);
-    configured = true;
-  }
+  const cudaError_t oe = ensure_smem_optin(reinterpret_cast<const void*>(tc_kernel<W13>), kSmemTc);
+  if (oe != cudaSuccess) return oe;
   // one CTA per SM, each looping over work items; no more CTAs than items
   const long long most = (long long)max_tiles * P.mblocks;
   if (most > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
@@ -603,6 +644,8 @@ cudaError_t launch_tc_w13(const moe_fp4_dims& d, const uint8_t* w13, const uint8
   P.acc1_offset = d.I;
   P.I = d.I;
   P.d = d.d;
+  P.wait_ns = wait_limit_ns();
+  P.fault = fault_site() == MOE_FP4_FAULT_TC_TOKEN_TILE;
   return launch_tc<true>(b, raw, P, ws.max_tc_tiles, st);
 }
 
@@ -630,6 +673,8 @@ cudaError_t launch_tc_w2(const moe_fp4_dims& d, const uint8_t* w2, const uint8_t
   P.acc1_offset = kBM;
   P.I = d.I;
   P.d = d.d;
+  P.wait_ns = wait_limit_ns();
+  P.fault = 0;
   return launch_tc<false>(b, raw, P, ws.max_tc_tiles, st);
 }
 

@@ -62,7 +62,15 @@ bool layout_workspace(const moe_fp4_dims& d, void* base, bool with_staging, Work
 // elements); false if the driver rejects it.
 bool make_map_2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
                  uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw);
+// SM count of the current device (cached per device).
 int num_sms();
+// Raises the kernel's dynamic shared memory limit to `bytes` on the current
+// device, once per (kernel, device); returns the CUDA error of the attempt.
+cudaError_t ensure_smem_optin(const void* kernel, int bytes);
+// Fault-injection setting of moe_fp4_set_fault_injection (process-wide) and
+// the limit of every pipeline wait (2 s unless a fault test lowers it).
+int fault_site();
+uint64_t wait_limit_ns();
 
 // ---- launchers (one per kernel family; each returns cudaGetLastError()) ----
 cudaError_t launch_route(const moe_fp4_dims& d, const float* logits, const Workspace& ws, cudaStream_t st);

@@ -7,8 +7,11 @@
 // is magnitude order), its exponent minus 8 (the largest E4M3 exponent) as
 // the scale, then every element times the exact power of two 2^-scale goes
 // through the CUDA fp8 conversion (round to nearest even, saturating at the
-// largest finite E4M3); two 16-byte stores of codes and one scale byte.  The
-// kernel is bound by HBM: 2 bytes read and 1 + 1/32 written per element.
+// largest finite E4M3); two 16-byte stores of codes and one scale byte.  A
+// block holding an infinity or a NaN gets the NaN scale byte 0xFF and NaN
+// codes (0x7F): its value is undefined, as the MX format has no other way to
+// carry it.  The kernel is bound by HBM: 2 bytes read and 1 + 1/32 written
+// per element.
 #include <cuda_fp8.h>
 
 #include "moe_fp4_internal.cuh"
@@ -45,7 +48,15 @@ mxfp8_quantize_kernel(const uint4* __restrict__ x, long long n_blocks, uint4* __
     uint32_t amax = 0;
 #pragma unroll
     for (int i = 0; i < 16; ++i) amax = max(amax, max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu));
-    // scale exponent in [-127, 119]; 2^-s is then a normal fp32 (exponent field 127 - s in [8, 254])
+    if (amax >= 0x7F80u) {  // an infinity or a NaN in the block (bf16 exponent field all ones)
+      const uint4 nan4 = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+      codes[2 * b] = nan4;
+      codes[2 * b + 1] = nan4;
+      scales[b] = 0xFF;
+      continue;
+    }
+    // finite block: scale exponent in [-127, 119]; 2^-s is then a normal fp32
+    // (exponent field 127 - s in [8, 254])
     const int s = amax == 0 ? -127 : max(bf16_floor_log2(amax) - 8, -127);
     const float inv = __uint_as_float((uint32_t)(127 - s) << 23);
     uint32_t out[8];

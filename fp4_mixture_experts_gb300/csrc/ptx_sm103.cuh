@@ -7,7 +7,7 @@
 
 namespace moe_fp4 {
 
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a wait gives up after 2 s
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // a wait gives up after 2 s (unless a launch sets less)
 constexpr uint32_t kSuspendHintNs = 20000;        // a waiting thread sleeps (up to 20 us) instead of spinning
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
@@ -48,19 +48,33 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
   return t;
 }
 
-// Bounded wait on phase `parity`.  Returns false on timeout (2 s of the global
-// timer; after raising the CTA's abort flag and the device error word) or once
-// another thread aborted.
+// Bounded wait on phase `parity`.  Returns false on timeout (after `limit_ns`
+// of the global timer; it then raises the CTA's abort flag and ORs err_code
+// into the device error word) or once another thread aborted.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int32_t* err,
-                                          int err_code) {
+                                          int err_code, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
     if (mbar_try_wait_sleep(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) break;
+    if (global_timer_ns() - t0 > limit_ns) break;
   }
   *abort_flag = 1;
+  atomicOr(err, err_code);
+  return false;
+}
+
+// Wait used on the way out of a kernel, for asynchronous work this thread
+// started (its TMA copies, its MMAs): it ignores the abort flag, so that the
+// copies have landed and the MMAs have completed before shared memory or
+// tensor memory is given back, and gives up only after `limit_ns`.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, int32_t* err, int err_code,
+                                                uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (global_timer_ns() - t0 <= limit_ns)
+    if (mbar_try_wait_sleep(bar, parity)) return true;
   atomicOr(err, err_code);
   return false;
 }

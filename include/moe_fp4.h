@@ -91,7 +91,8 @@ typedef enum moe_fp4_status {
  * tolerance of the definition; the default picks by shape (expected rows per
  * expert = T*k/E): the streaming GEMV path for few rows, the tensor-core path
  * otherwise. */
-#define MOE_FP4_FLAG_FORCE_GEMV 0x1u    /* CUDA-core streaming path (d, I multiples of 1024) */
+#define MOE_FP4_FLAG_FORCE_GEMV 0x1u    /* streaming path: weights streamed once, warp-level mma.sync
+                                           (d, I multiples of 1024) */
 #define MOE_FP4_FLAG_FORCE_TC   0x2u    /* tcgen05 tensor-core path */
 
 /* Bytes of device workspace a call with these sizes needs (256-byte aligned
@@ -163,21 +164,31 @@ int moe_fp4_forward_host(const moe_fp4_dims* dims, const void* x_bf16_host,
  * Scratch: a fixed device array of MOE_FP4_NOALLOC_SCRATCH_BYTES inside this
  * library, which every GPU that loads the library holds until the process
  * exits.  Problems whose moe_fp4_workspace_bytes exceeds it are rejected with
- * MOE_FP4_ERR_WORKSPACE before anything is enqueued (the decode shape T=32,
- * d=4096, I=2048, E=256, k=8 needs about 7.4 MB).
- * The first call on a device looks the array's device address up (with that
- * device current); make that first call before any stream capture.
+ * MOE_FP4_ERR_WORKSPACE before anything is enqueued.  With E = 256 and k = 8
+ * that allows T <= 73 tokens at d = 4096, I = 2048 (the T = 32 decode batch
+ * needs about 7.4 MB) and T <= 44 at d = 7168, I = 2048; prefill-sized
+ * batches need a workspace (moe_fp4_forward).
+ * The array's device address is looked up (with the call's device current)
+ * on every call made outside a stream capture, so a device reset between calls
+ * is harmless; a call made during a capture uses the address of the last call
+ * outside one, so make one call on each device before capturing.
  * All calls share the array and it keeps the last call's contents: calls
  * that overlap on the GPU (other streams, other host threads) race and give
  * wrong results; order them on one stream.  Otherwise the same arguments,
  * checks and results as moe_fp4_forward, with no optional outputs.  The
- * device error word lives in the internal scratch, which moe_fp4_check cannot
- * be given: callers that need it use moe_fp4_forward with a workspace. */
+ * device error word lives in the internal array: moe_fp4_noalloc_check reads
+ * it. */
 #define MOE_FP4_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
 int moe_fp4_forward_noalloc(const moe_fp4_dims* dims, const void* x_bf16, const float* router_logits,
                             const uint8_t* w13, const uint8_t* w13_scale,
                             const uint8_t* w2, const uint8_t* w2_scale, float* out,
                             unsigned flags, void* cuda_stream);
+
+/* moe_fp4_check for the internal array of moe_fp4_forward_noalloc:
+ * synchronises the stream, reads the device error word left by the calls
+ * enqueued before it (bits as in moe_fp4_check) and clears it.  Returns
+ * MOE_FP4_OK, MOE_FP4_ERR_DEVICE or MOE_FP4_ERR_CUDA.  Allocates nothing. */
+int moe_fp4_noalloc_check(void* cuda_stream);
 
 /* MXFP8 quantisation of bf16 rows: the activation operand of a block-scaled
  * (MX) tensor-core product.  The paper quantises its decode activations
@@ -202,6 +213,27 @@ int moe_fp4_forward_noalloc(const moe_fp4_dims* dims, const void* x_bf16, const 
  * a misaligned x_bf16 / codes; MOE_FP4_ERR_CUDA if the launch fails. */
 int moe_fp4_mxfp8_quantize(const void* x_bf16, int64_t rows, int32_t K, uint8_t* codes, uint8_t* scales,
                            void* cuda_stream);
+
+/* Fault injection, for tests of the failure path only (the layer's own
+ * failure handling: every pipeline wait in the kernels is bounded, and a wait
+ * that runs out sets bit 2 of the device error word, releases the kernel's
+ * other roles, lets every copy and MMA in flight finish, frees tensor memory
+ * and returns).  While a site other than MOE_FP4_FAULT_NONE is set, every
+ * later moe_fp4_forward* call in this process, from any thread, plants the
+ * fault on the host's instruction, and every pipeline wait gives up after
+ * wait_limit_us microseconds instead of 2 s:
+ *   MOE_FP4_FAULT_TC_TOKEN_TILE   the tensor-core W13 kernel's first CTA never
+ *                                 loads its first token tile;
+ *   MOE_FP4_FAULT_STREAM_STAGE    the streaming W13 kernel's first CTA never
+ *                                 loads its first weight stage.
+ * Nothing faults, traps or hangs: the waiting threads give up, the outputs of
+ * that call are incomplete, and moe_fp4_check reports MOE_FP4_ERR_DEVICE.
+ * MOE_FP4_FAULT_NONE (wait_limit_us ignored) restores normal operation.
+ * Returns MOE_FP4_ERR_INVALID_ARG for an unknown site or a zero limit. */
+#define MOE_FP4_FAULT_NONE 0
+#define MOE_FP4_FAULT_TC_TOKEN_TILE 1
+#define MOE_FP4_FAULT_STREAM_STAGE 2
+int moe_fp4_set_fault_injection(int site, uint32_t wait_limit_us);
 
 /* Synchronises the stream and reads the device error word of the workspace,
  * which the kernels OR bits into: 1 = an index out of range (e.g. a corrupted

@@ -26,6 +26,10 @@ The readings used here, where the pages say nothing:
   value, ties to the even mantissa; magnitudes beyond 448 saturate to 448
   (amax / X lies in [256, 512), so only the top binade can exceed it).  The
   sign of zero is kept: -0 gives the code 0x80.
+* Non-finite input: a block holding an infinity or a NaN has no finite
+  power-of-two scale, and E8M0 has no infinity, so its scale is the NaN byte
+  0xFF (OCP Microscaling v1.0: a NaN scale makes the whole block NaN) and its
+  elements are the E4M3 NaN code 0x7F.
 * Where: x (bf16) per token row before W13; h after its bf16 rounding, per
   slot row, before W2.  Routing, the sort, SwiGLU, the bf16 rounding of h and
   the combine are those of moe_oracle.forward.
@@ -98,20 +102,26 @@ def mxfp8_quantize(rows: np.ndarray):
     if K % MX_BLOCK:
         raise ValueError("K must be a multiple of 32")
     blocks = rows.reshape(R, K // MX_BLOCK, MX_BLOCK)
+    bad = ~np.all(np.isfinite(blocks), axis=2)          # blocks holding an infinity or a NaN
+    blocks = np.where(bad[:, :, None], 0.0, blocks)
     amax = np.abs(blocks).max(axis=2)
     _, ex = np.frexp(np.where(amax > 0, amax, 1.0))
     shared = np.where(amax > 0, ex - 1 - E4M3_EMAX, -127)
     shared = np.clip(shared, -127, 127)
     q = e4m3_round(blocks / np.ldexp(1.0, shared)[:, :, None])
-    return e4m3_encode(q).reshape(R, K), (shared + 127).astype(np.uint8)
+    codes = np.where(bad[:, :, None], np.uint8(0x7F), e4m3_encode(q))
+    scales = np.where(bad, np.uint8(0xFF), (shared + 127).astype(np.uint8))
+    return codes.reshape(R, K).astype(np.uint8), scales.astype(np.uint8)
 
 
 def mxfp8_dequantize(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
-    """Values of MXFP8 rows: e4m3(code) * 2**(s - 127) -> fp64 [R, K]."""
+    """Values of MXFP8 rows: e4m3(code) * 2**(s - 127) -> fp64 [R, K]; the
+    scale byte 0xFF is NaN."""
     codes = np.asarray(codes, dtype=np.uint8)
     R, K = codes.shape
     s = np.asarray(scales).astype(np.int64)
-    return e4m3_decode(codes) * np.repeat(np.ldexp(1.0, s - 127), MX_BLOCK, axis=1)
+    X = np.where(s == 255, np.nan, np.ldexp(1.0, s - 127))
+    return e4m3_decode(codes) * np.repeat(X, MX_BLOCK, axis=1)
 
 
 def mx_round_trip(rows: np.ndarray) -> np.ndarray:

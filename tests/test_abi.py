@@ -120,3 +120,10 @@ def test_the_header_and_library_work_from_plain_c(lib):
     assert r.returncode == 0, r.stderr
     run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
     assert run.returncode == 0, run.stdout + run.stderr
+
+
+def test_fault_injection_setting_is_checked_on_the_host(lib):
+    assert lib.moe_fp4_set_fault_injection(9, 1000) == -1
+    assert lib.moe_fp4_set_fault_injection(-1, 1000) == -1
+    assert lib.moe_fp4_set_fault_injection(1, 0) == -1
+    assert lib.moe_fp4_set_fault_injection(0, 0) == 0

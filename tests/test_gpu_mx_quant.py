@@ -5,7 +5,8 @@ Codes and scale bytes are integers, and both sides decide them exactly (the
 inputs are bf16 values and the scales powers of two), so they must match bit
 for bit: random bit patterns over the whole finite bf16 range (subnormals and
 signed zeros included), exact E4M3 ties, saturating blocks, zero blocks, and
-the activation shapes of the decode and prefill layers.
+the activation shapes of the decode and prefill layers; blocks holding an
+infinity or a NaN get the NaN scale byte and NaN codes.
 """
 import numpy as np
 import pytest
@@ -108,3 +109,14 @@ def test_rows_zero_enqueues_nothing(moe):
     x = torch.empty(0, 64, dtype=torch.bfloat16, device="cuda")
     codes, scales = moe.mxfp8_quantize(x)
     assert codes.shape == (0, 64) and scales.shape == (0, 2)
+
+
+def test_non_finite_blocks(moe):
+    rng = np.random.default_rng(7)
+    bits = random_finite_bits(rng, 4, 256)
+    bits[0, 3] = 0x7F80    # +inf
+    bits[1, 40] = 0xFF80   # -inf
+    bits[2, 200] = 0x7FC1  # NaN
+    bits[3, 31] = 0xFFFF   # NaN with the sign set
+    bits[3, 32] = 0x7F80   # the next block too
+    check(moe, bits)

@@ -154,6 +154,30 @@ def test_mx_zero_block_and_negative_zero():
     assert mx.e4m3_decode(codes[0, 40]) * 2.0 ** (int(scales[0, 1]) - 127) == 1.0
 
 
+def test_mx_non_finite_block_gets_the_nan_scale_and_leaves_its_neighbours_alone():
+    # an infinity or a NaN has no finite power-of-two scale and E8M0 has no
+    # infinity: the block's scale is the NaN byte, which makes every element
+    # of that block NaN, while the other blocks of the row quantise exactly as
+    # they would alone
+    rng = np.random.default_rng(31)
+    rows = rng.standard_normal((3, 128))
+    rows[0, 5] = np.inf
+    rows[1, 70] = -np.inf
+    rows[2, 100] = np.nan
+    codes, scales = mx.mxfp8_quantize(rows)
+    bad = {(0, 0), (1, 2), (2, 3)}
+    for r in range(3):
+        for b in range(4):
+            blk = rows[r, 32 * b:32 * b + 32]
+            if (r, b) in bad:
+                assert scales[r, b] == 0xFF and np.all(codes[r, 32 * b:32 * b + 32] == 0x7F)
+                assert np.all(np.isnan(mx.mxfp8_dequantize(codes[r:r + 1, 32 * b:32 * b + 32],
+                                                           scales[r:r + 1, b:b + 1])))
+            else:
+                c1, s1 = mx.mxfp8_quantize(blk[None, :])
+                assert scales[r, b] == s1[0, 0] and np.array_equal(codes[r, 32 * b:32 * b + 32], c1[0])
+
+
 # ----------------------------------------------------------------------------
 # the layer
 # ----------------------------------------------------------------------------
