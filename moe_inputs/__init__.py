@@ -5,6 +5,6 @@ tensor formats. It holds none of the layer's arithmetic (no decoding,
 routing, sorting or matrix products), so both the CPU oracle and the CUDA
 path can consume its output without sharing any of the method.
 """
-from .synth import CONFIGS, LayerInputs, make_layer, make_config, routing_sample_tokens
+from .synth import CONFIGS, LayerInputs, make_config, make_gate_weights, make_layer, routing_sample_tokens
 
-__all__ = ["CONFIGS", "LayerInputs", "make_layer", "make_config", "routing_sample_tokens"]
+__all__ = ["CONFIGS", "LayerInputs", "make_config", "make_gate_weights", "make_layer", "routing_sample_tokens"]

@@ -17,6 +17,12 @@ happen in this order):
 5. ``w2``: uint8 [E, d, I/2], raw generator bytes as for ``w13``.
 6. ``w2_scale``: uint8 [E, d, I/32], E8M0 bytes as for ``w13_scale``.
 
+Router weights (for the router projection ahead of top-k) come from a
+stream of their own, ``make_gate_weights(E, d, seed)``: a PCG64 generator
+seeded with ``[seed, 1]`` draws fp32 standard normal [E, d], divided by
+sqrt(d) (so that logits of N(0, 1) tokens are about N(0, 1), like the
+workloads' router logits) and rounded to bf16.
+
 The five named workloads are the ones the FP4 routed-MoE layer is measured
 on: a tiny layer, a decode-shaped layer (T=32), a prefill-shaped layer
 (T=4608, the paper's 4,604-token prompt rounded up to 36 x 128), a skewed
@@ -93,6 +99,13 @@ def make_layer(T: int, d: int, I: int, E: int, k: int, exp_lo: int = -7, exp_hi:
     w2 = _uniform_bytes(rng, (E, d, I // 2))
     w2_scale = _scale_bytes(rng, (E, d, I // 32), exp_lo, exp_hi)
     return LayerInputs(T, d, I, E, k, x, np.ascontiguousarray(logits), w13, w13_scale, w2, w2_scale)
+
+
+def make_gate_weights(E: int, d: int, seed: int = 0) -> np.ndarray:
+    """Router weights Wg as bf16 bit patterns [E, d] (see the module docstring)."""
+    rng = np.random.default_rng([seed, 1])
+    w = rng.standard_normal((E, d), dtype=np.float32) / np.float32(math.sqrt(d))
+    return _f32_to_bf16_bits(w.astype(np.float32))
 
 
 def make_config(name: str, seed: int | None = None) -> LayerInputs:
