@@ -14,6 +14,7 @@ _LIB_NAME = "libmoe_fp4.so"
 
 FLAG_FORCE_GEMV = 0x1
 FLAG_FORCE_TC = 0x2
+FLAG_PERSISTENT = 0x4
 
 FAULT_NONE = 0
 FAULT_TC_TOKEN_TILE = 1
@@ -23,6 +24,8 @@ EXPORTED_SYMBOLS = (
     "moe_fp4_workspace_bytes",
     "moe_fp4_host_workspace_bytes",
     "moe_fp4_route",
+    "moe_fp4_router",
+    "moe_fp4_forward_gated",
     "moe_fp4_forward",
     "moe_fp4_forward_profiled",
     "moe_fp4_forward_host",
@@ -73,6 +76,11 @@ def load_library():
     lib.moe_fp4_route.restype = ctypes.c_int
     lib.moe_fp4_forward.argtypes = [pd, P, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_uint, P, ctypes.c_size_t, P]
     lib.moe_fp4_forward.restype = ctypes.c_int
+    lib.moe_fp4_router.argtypes = [pd, P, P, P, P]
+    lib.moe_fp4_router.restype = ctypes.c_int
+    lib.moe_fp4_forward_gated.argtypes = [pd, P, P, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_uint, P,
+                                          ctypes.c_size_t, P]
+    lib.moe_fp4_forward_gated.restype = ctypes.c_int
     lib.moe_fp4_forward_profiled.argtypes = lib.moe_fp4_forward.argtypes + [ctypes.POINTER(ctypes.c_void_p)]
     lib.moe_fp4_forward_profiled.restype = ctypes.c_int
     lib.moe_fp4_forward_host.argtypes = [pd, P, P, P, P, P, P, P, ctypes.c_uint, P, ctypes.c_size_t, P]
@@ -220,6 +228,58 @@ def forward(x_bf16, router_logits, w13, w13_scale, w2, w2_scale, k: int, out=Non
         extras["out"] = out
         return extras
     return out
+
+
+def router(x_bf16, w_gate_bf16, logits=None, stream=None):
+    """Router logits fp32 [T, E] = x (bf16 [T, d]) . w_gate (bf16 [E, d])^T on the GPU."""
+    import torch
+    T, d = x_bf16.shape
+    E = w_gate_bf16.shape[0]
+    if w_gate_bf16.shape[1] != d:
+        raise ValueError("w_gate must be [E, d]")
+    dims = _dims(T, d, 128, E, 1)
+    if logits is None:
+        logits = torch.empty(T, E, dtype=torch.float32, device=x_bf16.device)
+    rc = load_library().moe_fp4_router(ctypes.byref(dims), _ptr(x_bf16), _ptr(w_gate_bf16), _ptr(logits),
+                                       _stream(stream))
+    if rc != 0:
+        raise MoeFp4Error(rc, "moe_fp4_router")
+    return logits
+
+
+def forward_gated(x_bf16, w_gate_bf16, w13, w13_scale, w2, w2_scale, k: int, out=None, flags: int = 0,
+                  workspace=None, return_routing: bool = False, return_h: bool = False, stream=None):
+    """The whole layer from x and the router weights (bf16 [E, d]).  Returns a
+    dict with out and router_logits, plus the requested extras."""
+    import torch
+    T, d = x_bf16.shape
+    E, twoI, _ = w13.shape
+    I = twoI // 2
+    dims = _dims(T, d, I, E, k)
+    lib = load_library()
+    nbytes = lib.moe_fp4_workspace_bytes(ctypes.byref(dims))
+    if nbytes == 0:
+        raise MoeFp4Error(-2, "moe_fp4_forward_gated")
+    dev = x_bf16.device
+    ws = _workspace(nbytes, dev, workspace)
+    if out is None:
+        out = torch.empty(T, d, dtype=torch.float32, device=dev)
+    res = {"out": out, "router_logits": torch.empty(T, E, dtype=torch.float32, device=dev)}
+    if return_routing:
+        res.update(topk_ids=torch.empty(T, k, dtype=torch.int32, device=dev),
+                   topk_weights=torch.empty(T, k, dtype=torch.float32, device=dev),
+                   expert_offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+                   sorted_slot=torch.empty(T * k, dtype=torch.int32, device=dev))
+    if return_h:
+        res["h"] = torch.empty(T * k, I, dtype=torch.bfloat16, device=dev)
+    rc = lib.moe_fp4_forward_gated(ctypes.byref(dims), _ptr(x_bf16), _ptr(w_gate_bf16), _ptr(res["router_logits"]),
+                                   _ptr(w13), _ptr(w13_scale), _ptr(w2), _ptr(w2_scale), _ptr(out),
+                                   _ptr(res.get("topk_ids")), _ptr(res.get("topk_weights")),
+                                   _ptr(res.get("expert_offsets")), _ptr(res.get("sorted_slot")), _ptr(res.get("h")),
+                                   int(flags), _ptr(ws), ws.numel(), _stream(stream))
+    if rc != 0:
+        raise MoeFp4Error(rc, "moe_fp4_forward_gated")
+    return res
 
 
 def forward_host(x_bf16_host, router_logits_host, w13, w13_scale, w2, w2_scale, k: int, out_host=None,

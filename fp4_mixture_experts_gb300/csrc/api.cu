@@ -97,7 +97,10 @@ int run_forward(const moe_fp4_dims& d, const void* x, const float* logits, const
   mark(1);
   if (use_gemv_path(d, flags)) {
     mark(2);
-    if (stream_path_supported(d)) {
+    if (stream_path_supported(d) && (flags & MOE_FP4_FLAG_PERSISTENT)) {
+      e = launch_stream_fused(d, xb, w13, w13s, w2, w2s, ws, st);  // both projections: the W2 stage reads 0
+      mark(3);
+    } else if (stream_path_supported(d)) {
       e = launch_stream_w13(d, xb, w13, w13s, ws, st);
       mark(3);
       if (e == cudaSuccess) e = launch_stream_w2(d, w2, w2s, ws, st);
@@ -121,7 +124,7 @@ int run_forward(const moe_fp4_dims& d, const void* x, const float* logits, const
 }
 
 int check_flags(unsigned flags) {
-  const unsigned known = MOE_FP4_FLAG_FORCE_GEMV | MOE_FP4_FLAG_FORCE_TC;
+  const unsigned known = MOE_FP4_FLAG_FORCE_GEMV | MOE_FP4_FLAG_FORCE_TC | MOE_FP4_FLAG_PERSISTENT;
   if (flags & ~known) return MOE_FP4_ERR_INVALID_ARG;
   if ((flags & MOE_FP4_FLAG_FORCE_GEMV) && (flags & MOE_FP4_FLAG_FORCE_TC)) return MOE_FP4_ERR_INVALID_ARG;
   return MOE_FP4_OK;
@@ -189,6 +192,48 @@ int moe_fp4_forward_profiled(const moe_fp4_dims* dims, const void* x_bf16, const
   return run_forward(d, x_bf16, router_logits, w13, w13_scale, w2, w2_scale, out, topk_ids, topk_weights,
                      expert_offsets, sorted_slot, h_bf16, flags, ws, static_cast<cudaStream_t>(cuda_stream),
                      stage_events);
+}
+
+int moe_fp4_router(const moe_fp4_dims* dims, const void* x_bf16, const void* w_gate_bf16, float* router_logits,
+                   void* cuda_stream) {
+  if (!dims || !x_bf16 || !w_gate_bf16 || !router_logits) return MOE_FP4_ERR_INVALID_ARG;
+  const moe_fp4_dims d = *dims;
+  Workspace ws;
+  if (!layout_workspace(d, nullptr, false, &ws)) return MOE_FP4_ERR_UNSUPPORTED;
+  if (!aligned(x_bf16, 16) || !aligned(w_gate_bf16, 16) || !aligned(router_logits, 4)) return MOE_FP4_ERR_INVALID_ARG;
+  return launch_router(d, static_cast<const uint16_t*>(x_bf16), static_cast<const uint16_t*>(w_gate_bf16),
+                       router_logits, static_cast<cudaStream_t>(cuda_stream)) == cudaSuccess
+             ? MOE_FP4_OK
+             : MOE_FP4_ERR_CUDA;
+}
+
+int moe_fp4_forward_gated(const moe_fp4_dims* dims, const void* x_bf16, const void* w_gate_bf16,
+                          float* router_logits, const uint8_t* w13, const uint8_t* w13_scale, const uint8_t* w2,
+                          const uint8_t* w2_scale, float* out, int32_t* topk_ids, float* topk_weights,
+                          int32_t* expert_offsets, int32_t* sorted_slot, void* h_bf16, unsigned flags,
+                          void* workspace, size_t workspace_bytes, void* cuda_stream) {
+  if (!dims || !w_gate_bf16 || !router_logits) return MOE_FP4_ERR_INVALID_ARG;
+  // the layer's own checks first (x, weights, out, workspace, flags), so that
+  // nothing is enqueued when any argument is bad
+  if (!x_bf16 || !w13 || !w13_scale || !w2 || !w2_scale || !out || !workspace) return MOE_FP4_ERR_INVALID_ARG;
+  if (check_flags(flags) != MOE_FP4_OK) return MOE_FP4_ERR_INVALID_ARG;
+  const moe_fp4_dims d = *dims;
+  Workspace ws;
+  if (!layout_workspace(d, workspace, false, &ws)) return MOE_FP4_ERR_UNSUPPORTED;
+  if (!aligned(w_gate_bf16, 16) || !aligned(router_logits, 4) || !aligned(workspace, 256) || !aligned(x_bf16, 16) ||
+      !aligned(w13, 16) || !aligned(w2, 16) || !aligned(out, 16) || !aligned(w13_scale, 16) ||
+      !aligned(w2_scale, 16) || (h_bf16 && !aligned(h_bf16, 16)) || (topk_ids && !aligned(topk_ids, 4)) ||
+      (topk_weights && !aligned(topk_weights, 4)) || (expert_offsets && !aligned(expert_offsets, 4)) ||
+      (sorted_slot && !aligned(sorted_slot, 4)))
+    return MOE_FP4_ERR_INVALID_ARG;
+  if ((flags & MOE_FP4_FLAG_FORCE_GEMV) && (d.d % 1024 != 0 || d.I % 1024 != 0)) return MOE_FP4_ERR_UNSUPPORTED;
+  if (workspace_bytes < ws.total) return MOE_FP4_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  if (launch_router(d, static_cast<const uint16_t*>(x_bf16), static_cast<const uint16_t*>(w_gate_bf16),
+                    router_logits, st) != cudaSuccess)
+    return MOE_FP4_ERR_CUDA;
+  return run_forward(d, x_bf16, router_logits, w13, w13_scale, w2, w2_scale, out, topk_ids, topk_weights,
+                     expert_offsets, sorted_slot, h_bf16, flags, ws, st);
 }
 
 int moe_fp4_forward(const moe_fp4_dims* dims, const void* x_bf16, const float* router_logits,

@@ -27,9 +27,9 @@
 //   - the W13 epilogue applies SwiGLU and rounds h to bf16, the W2 epilogue
 //     writes fp32 y.
 // Waits are bounded; a timeout raises the CTA abort flag, after which every
-// warp runs the same loop without waiting or computing, so all barriers are
-// still met and the kernel exits; the producer waits (also bounded) for its
-// copies in flight before it leaves.
+// warp runs the same loop without waiting (its arithmetic discarded), so all
+// barriers are still met and the kernel exits; the producer waits (also
+// bounded) for its copies in flight before it leaves.
 #include <cuda_fp16.h>
 
 #include "moe_fp4_internal.cuh"
@@ -69,6 +69,7 @@ struct StreamParams {
   int x_pitch;             // bytes per token row of the f16 activation buffer
   uint64_t wait_ns;        // limit of every mbarrier wait
   int fault;               // nonzero: CTA 0 withholds its first weight stage (fault-injection test)
+  int act_l2;              // nonzero: read the activations through L2 only (written by other SMs in this launch)
 };
 
 __device__ __forceinline__ uint32_t e2m1x2_h2(uint32_t byte) { return e2m1x2_to_f16x2(byte); }
@@ -121,89 +122,123 @@ __device__ __forceinline__ void issue_stage(const CUtensorMap* map_w, const CUte
   }
 }
 
-template <bool W13>
-__global__ void __launch_bounds__(kThreads, 1)
-stream_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_s,
-              const StreamParams P) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* ring = smem;
-  uint8_t* xs_buf = ring + (size_t)P.stages * kStageBytes;          // [8 tokens][x_pitch] f16
-  float4* red = reinterpret_cast<float4*>(xs_buf + (size_t)kMaxTok * P.x_pitch);  // [2][kKSplit-1][8 tiles][32]
-  float* tok_scale = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(red) + kRedBytes);  // [8]
-  uint64_t* full = reinterpret_cast<uint64_t*>(tok_scale + kMaxTok);
-  uint64_t* empty = full + P.stages;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + P.stages);
+// Shared memory of the streaming kernels (one layout for every phase).
+struct StreamSmem {
+  uint8_t* ring;           // [stages][kStageBytes]
+  uint8_t* xs_buf;         // [8 tokens][x_pitch] f16 activations of the current chunk
+  float4* red;             // [2][kKSplit-1][8 tiles][32] partial sums of the K split
+  float* tok_scale;        // [8]
+  uint64_t* full;          // [stages]
+  uint64_t* empty;         // [stages]
+  volatile int* abort_flag;
+};
 
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) {
-    for (int i = 0; i < P.stages; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kConsWarps);
+__device__ __forceinline__ StreamSmem stream_smem(uint8_t* smem_raw, int stages, int x_pitch) {
+  StreamSmem S;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  S.ring = smem;
+  S.xs_buf = S.ring + (size_t)stages * kStageBytes;
+  S.red = reinterpret_cast<float4*>(S.xs_buf + (size_t)kMaxTok * x_pitch);
+  S.tok_scale = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(S.red) + kRedBytes);
+  S.full = reinterpret_cast<uint64_t*>(S.tok_scale + kMaxTok);
+  S.empty = S.full + stages;
+  S.abort_flag = reinterpret_cast<volatile int*>(S.empty + stages);
+  return S;
+}
+
+__device__ __forceinline__ void stream_init(const StreamSmem& S, int stages) {
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < stages; ++i) {
+      mbar_init(&S.full[i], 1);
+      mbar_init(&S.empty[i], kConsWarps);
     }
-    *abort_flag = 0;
+    *S.abort_flag = 0;
     mbar_fence_init();
   }
   __syncthreads();
-  // Both kernels are launched early.  W13 waits here for the routing kernel
-  // (the work list); W2 was let start only after every W13 CTA had passed
-  // that wait, so the work list is complete, and it reads it through L2
-  // (ld.global.cg) so that its producer can stream weights while W13 ends;
-  // its consumers wait for W13 (h) below.
-  if (W13) griddep_wait();
-  griddep_launch_dependents();
+}
+
+// The producer's ring state, carried from one phase to the next.
+struct ProdRing {
+  int slot = 0;
+  uint32_t phase = 0;
+  uint32_t nxt = 0;    // bit s: parity of the next copy into slot s (its full-barrier phase)
+  uint32_t has = 0;    // bit s: slot s received a copy
+  bool ok = true;
+};
+
+// The consumers' ring state, carried from one phase to the next.
+struct ConsRing {
+  int slot = 0;
+  int rbuf = 0;
+  uint32_t phase = 0;
+};
+
+// This CTA's share [it0, it1) of the items (chunk, row block) of one projection.
+__device__ __forceinline__ void stream_items(const StreamParams& P, long long& it0, long long& it1) {
   const int n_chunks = __ldcg(P.counts + 1);
   const long long n_items = (long long)n_chunks * P.n_rb;
-  const long long it0 = n_items * blockIdx.x / gridDim.x;
-  const long long it1 = n_items * (blockIdx.x + 1) / gridDim.x;
+  it0 = n_items * blockIdx.x / gridDim.x;
+  it1 = n_items * (blockIdx.x + 1) / gridDim.x;
+}
+
+// Producer (one thread): streams the weight stages of this CTA's items.
+template <bool W13>
+__device__ __forceinline__ void stream_produce(const CUtensorMap* map_w, const CUtensorMap* map_s,
+                                               const StreamParams& P, const StreamSmem& S, ProdRing& R) {
+  long long it0, it1;
+  stream_items(P, it0, it1);
   const int nst = P.K / kKStage;
-
-  if (warp == kConsWarps) {
-    // ---------------- producer warp ----------------
-    if (lane == 0) {
-      const uint64_t pol = l2_evict_first_policy();
-      int slot = 0;
-      uint32_t phase = 0;
-      uint32_t nxt = 0;    // bit s: parity of the next copy into slot s (its full-barrier phase)
-      uint32_t has = 0;    // bit s: slot s received a copy
-      bool withhold = P.fault != 0 && blockIdx.x == 0;
-      bool ok = true;
-      for (long long it = it0; it < it1 && ok; ++it) {
-        const int c = (int)(it / P.n_rb), rb = (int)(it % P.n_rb);
-        const int e = __ldcg(P.chunks + c).x;
-        for (int ks = 0; ks < nst; ++ks) {
-          if (!mbar_wait(&empty[slot], phase ^ 1u, abort_flag, P.err, kErrWaitTimeout, P.wait_ns) || *abort_flag) {
-            ok = false;
-            break;
-          }
-          // one copy per slot in flight: after an abort a slot may come back
-          // before its previous copy landed (a no-op wait otherwise)
-          if ((has >> slot) & 1)
-            mbar_wait_drain(&full[slot], ((nxt >> slot) & 1) ^ 1u, P.err, kErrWaitTimeout, P.wait_ns);
-          if (withhold) {
-            // fault injection: this stage never arrives, so the consumers'
-            // wait on it runs out and the kernel takes its abort path
-            withhold = false;
-          } else {
-            issue_stage<W13>(&map_w, &map_s, P, e, rb, ks, ring + (size_t)slot * kStageBytes, &full[slot], pol);
-            nxt ^= 1u << slot;
-            has |= 1u << slot;
-          }
-          if (++slot == P.stages) {
-            slot = 0;
-            phase ^= 1u;
-          }
-        }
+  const uint64_t pol = l2_evict_first_policy();
+  bool withhold = P.fault != 0 && blockIdx.x == 0;
+  for (long long it = it0; it < it1 && R.ok; ++it) {
+    const int c = (int)(it / P.n_rb), rb = (int)(it % P.n_rb);
+    const int e = __ldcg(P.chunks + c).x;
+    for (int ks = 0; ks < nst; ++ks) {
+      if (!mbar_wait(&S.empty[R.slot], R.phase ^ 1u, S.abort_flag, P.err, kErrWaitTimeout, P.wait_ns) ||
+          *S.abort_flag) {
+        R.ok = false;
+        break;
       }
-      // every issued copy has landed before the CTA may exit
-      for (int q = 0; q < P.stages; ++q)
-        if ((has >> q) & 1) mbar_wait_drain(&full[q], ((nxt >> q) & 1) ^ 1u, P.err, kErrWaitTimeout, P.wait_ns);
+      // (a slot comes back only once every consumer read its stage, or saw
+      // the abort that the check above catches: one copy per slot in flight)
+      if (withhold) {
+        // fault injection: this stage never arrives, so the consumers' wait
+        // on it runs out and the kernel takes its abort path
+        withhold = false;
+      } else {
+        issue_stage<W13>(map_w, map_s, P, e, rb, ks, S.ring + (size_t)R.slot * kStageBytes, &S.full[R.slot], pol);
+        R.nxt ^= 1u << R.slot;
+        R.has |= 1u << R.slot;
+      }
+      if (++R.slot == P.stages) {
+        R.slot = 0;
+        R.phase ^= 1u;
+      }
     }
-    return;
   }
+}
 
-  // ---------------- consumer warps ----------------
-  if (!W13) griddep_wait();  // h comes from the W13 kernel
+// Every copy the producer issued has landed before the CTA may exit.
+__device__ __forceinline__ void stream_drain(const StreamParams& P, const StreamSmem& S, const ProdRing& R) {
+  for (int q = 0; q < P.stages; ++q)
+    if ((R.has >> q) & 1) mbar_wait_drain(&S.full[q], ((R.nxt >> q) & 1) ^ 1u, P.err, kErrWaitTimeout, P.wait_ns);
+}
+
+// Consumer warps (16): this CTA's items of one projection.
+template <bool W13>
+__device__ __forceinline__ void stream_consume(const StreamParams& P, const StreamSmem& S, ConsRing& R) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  long long it0, it1;
+  stream_items(P, it0, it1);
+  const int nst = P.K / kKStage;
+  uint8_t* const ring = S.ring;
+  uint8_t* const xs_buf = S.xs_buf;
+  float4* const red = S.red;
+  float* const tok_scale = S.tok_scale;
+  uint64_t* const full = S.full;
+  uint64_t* const empty = S.empty;
+  volatile int* const abort_flag = S.abort_flag;
   const int g = lane >> 2, t = lane & 3;
   const int tile = warp % kTiles, kpart = warp / kTiles;  // 16-row tile, share of the stage's blocks
   // rows of this thread inside the stage's 128 rows (A-fragment rows g and g+8)
@@ -216,8 +251,9 @@ stream_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__
   const int baseB = (W13 ? (rowB >> 6) * 16384 : 0) + rbw * 128 + 4 * t;
   const int swA_ = ra & 7, swB_ = rbw & 7;
   int cur = -1, row0 = 0, mt = 0;
-  int slot = 0, rbuf = 0;
-  uint32_t phase = 0;
+  int& slot = R.slot;
+  int& rbuf = R.rbuf;
+  uint32_t& phase = R.phase;
   for (long long it = it0; it < it1; ++it) {
     const int c = (int)(it / P.n_rb), rb = (int)(it % P.n_rb);
     if (c != cur) {
@@ -234,7 +270,7 @@ stream_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__
         const uint4* src = reinterpret_cast<const uint4*>(P.act + (size_t)src_row * P.K);
         uint32_t emax = 1;
         for (int v = lane; v < P.K / 8; v += 32) {
-          const uint4 q = src[v];
+          const uint4 q = P.act_l2 ? __ldcg(src + v) : src[v];
           const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
           for (int i = 0; i < 4; ++i) emax = max(emax, max((w[i] >> 7) & 0xFFu, (w[i] >> 23) & 0xFFu));
@@ -244,7 +280,7 @@ stream_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__
         const int shift = 141 - (int)emax;  // the largest magnitude lands in [2^14, 2^15)
         const float f1 = pow2f(shift / 2), f2 = pow2f(shift - shift / 2);
         for (int v = lane; v < P.K / 8; v += 32) {
-          const uint4 q = src[v];
+          const uint4 q = P.act_l2 ? __ldcg(src + v) : src[v];
           const uint32_t w[4] = {q.x, q.y, q.z, q.w};
           uint32_t o[4];
 #pragma unroll
@@ -262,15 +298,15 @@ stream_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__
       asm volatile("bar.sync 1, %0;" ::"r"(kConsWarps * 32) : "memory");
       cur = c;
     }
-    // wait outcomes are made uniform over the warp, so that the warp-wide
-    // mma.sync below sees all 32 lanes or none
-    const bool run = __all_sync(0xFFFFFFFFu, !*abort_flag);
+    // after an abort the waits are skipped but the arithmetic still runs (on
+    // whatever the ring holds; nothing is kept), so that the warp-wide
+    // mma.sync below always sees all 32 lanes
+    const bool run = !*abort_flag;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     const uint8_t* xg = xs_buf + (size_t)g * P.x_pitch + 16 * t;  // token g, this thread's 8 elements
     for (int ks = 0; ks < nst; ++ks) {
-      const bool ok =
-          run && __all_sync(0xFFFFFFFFu, mbar_wait(&full[slot], phase, abort_flag, P.err, kErrWaitTimeout, P.wait_ns));
-      if (ok) {
+      if (run) mbar_wait(&full[slot], phase, abort_flag, P.err, kErrWaitTimeout, P.wait_ns);
+      {
         const uint8_t* st = ring + (size_t)slot * kStageBytes;
         // packed rows: two 128-byte-swizzled boxes (K 0..255, 256..511) of 128 (or 2 x 64) rows
         const uint8_t* pa = st + baseA;
@@ -368,6 +404,82 @@ stream_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__
   }
 }
 
+template <bool W13>
+__global__ void __launch_bounds__(kThreads, 1)
+stream_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__ CUtensorMap map_s,
+              const StreamParams P) {
+  extern __shared__ uint8_t smem_raw[];
+  const StreamSmem S = stream_smem(smem_raw, P.stages, P.x_pitch);
+  stream_init(S, P.stages);
+  // Both kernels are launched early.  W13 waits here for the routing kernel
+  // (the work list); W2 was let start only after every W13 CTA had passed
+  // that wait, so the work list is complete, and it reads it through L2
+  // (ld.global.cg) so that its producer can stream weights while W13 ends;
+  // its consumers wait for W13 (h) below.
+  if (W13) griddep_wait();
+  griddep_launch_dependents();
+  if ((threadIdx.x >> 5) == kConsWarps) {
+    if ((threadIdx.x & 31) == 0) {
+      ProdRing R;
+      stream_produce<W13>(&map_w, &map_s, P, S, R);
+      stream_drain(P, S, R);
+    }
+    return;
+  }
+  if (!W13) griddep_wait();  // h comes from the W13 kernel
+  ConsRing R;
+  stream_consume<W13>(P, S, R);
+}
+
+// The decode layer's two projections in one persistent launch: W13 + SwiGLU
+// over this CTA's items, a grid-wide arrival counter, then W2.  One weight
+// ring serves both phases, so the producer streams W2's first stages while
+// the consumers finish W13 (weights do not depend on h).  The counter lives
+// in the workspace (zeroed by the routing kernel of the same call); its wait
+// is bounded, and on a timeout the consumers skip W2's arithmetic (error bit
+// 2).  Launched cooperatively: all CTAs (one per SM) are resident together.
+__global__ void __launch_bounds__(kThreads, 1)
+stream_fused_kernel(const __grid_constant__ CUtensorMap map_w13, const __grid_constant__ CUtensorMap map_s13,
+                    const __grid_constant__ CUtensorMap map_w2, const __grid_constant__ CUtensorMap map_s2,
+                    const StreamParams P13, const StreamParams P2, int32_t* arrivals) {
+  extern __shared__ uint8_t smem_raw[];
+  const StreamSmem S = stream_smem(smem_raw, P13.stages, P13.x_pitch);
+  stream_init(S, P13.stages);
+  griddep_launch_dependents();
+  if ((threadIdx.x >> 5) == kConsWarps) {
+    if ((threadIdx.x & 31) == 0) {
+      ProdRing R;
+      stream_produce<true>(&map_w13, &map_s13, P13, S, R);
+      stream_produce<false>(&map_w2, &map_s2, P2, S, R);
+      stream_drain(P2, S, R);
+    }
+    return;
+  }
+  ConsRing R;
+  stream_consume<true>(P13, S, R);
+  // grid-wide barrier between the phases: every CTA's h is written
+  asm volatile("bar.sync 1, %0;" ::"r"(kConsWarps * 32) : "memory");
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(arrivals, 1);
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+      int seen;
+      asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(seen) : "l"(arrivals) : "memory");
+      if (seen >= (int)gridDim.x) break;
+      if (global_timer_ns() - t0 > P2.wait_ns) {
+        *S.abort_flag = 1;
+        atomicOr(P2.err, kErrWaitTimeout);
+        break;
+      }
+      __nanosleep(200);
+    }
+    __threadfence();
+  }
+  asm volatile("bar.sync 1, %0;" ::"r"(kConsWarps * 32) : "memory");
+  stream_consume<false>(P2, S, R);
+}
+
 size_t smem_needed(int stages, int x_pitch) {
   return 1024 /* alignment slack */ + (size_t)stages * kStageBytes + (size_t)kMaxTok * x_pitch + kRedBytes +
          kMaxTok * sizeof(float) + 2 * stages * sizeof(uint64_t) + 16;
@@ -385,23 +497,23 @@ cudaError_t launch_stream(const CUtensorMap& mw, const CUtensorMap& ms, StreamPa
   return launch_early(stream_kernel<W13>, dim3(num_sms()), dim3(kThreads), smem, st, mw, ms, P);
 }
 
-}  // namespace
-
-bool stream_path_supported(const moe_fp4_dims& d) {
-  // whole 512-K stages, 64-row W13 blocks, 128-row W2 blocks; 8 token rows of
-  // K f16 activations must fit shared memory next to the ring
-  return d.d % 1024 == 0 && d.I % 1024 == 0 && d.d <= 7168 && d.I <= 7168;
+bool maps_w13(const moe_fp4_dims& d, const uint8_t* w13, const uint8_t* w13s, CUtensorMap* mw, CUtensorMap* ms) {
+  const uint64_t rows = (uint64_t)d.E * 2 * d.I;
+  return make_map_2d(mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w13, d.d / 2, rows, d.d / 2, 128, 64,
+                     CU_TENSOR_MAP_SWIZZLE_128B) &&
+         make_map_2d(ms, CU_TENSOR_MAP_DATA_TYPE_UINT8, w13s, d.d / 32, rows, d.d / 32, 16, 64,
+                     CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
-cudaError_t launch_stream_w13(const moe_fp4_dims& d, const uint16_t* x, const uint8_t* w13, const uint8_t* w13s,
-                              const Workspace& ws, cudaStream_t st) {
-  CUtensorMap mw, ms;
-  const uint64_t rows = (uint64_t)d.E * 2 * d.I;
-  if (!make_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w13, d.d / 2, rows, d.d / 2, 128, 64,
-                   CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map_2d(&ms, CU_TENSOR_MAP_DATA_TYPE_UINT8, w13s, d.d / 32, rows, d.d / 32, 16, 64,
-                   CU_TENSOR_MAP_SWIZZLE_NONE))
-    return cudaErrorInvalidValue;
+bool maps_w2(const moe_fp4_dims& d, const uint8_t* w2, const uint8_t* w2s, CUtensorMap* mw, CUtensorMap* ms) {
+  const uint64_t rows = (uint64_t)d.E * d.d;
+  return make_map_2d(mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w2, d.I / 2, rows, d.I / 2, 128, 128,
+                     CU_TENSOR_MAP_SWIZZLE_128B) &&
+         make_map_2d(ms, CU_TENSOR_MAP_DATA_TYPE_UINT8, w2s, d.I / 32, rows, d.I / 32, 16, 128,
+                     CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+StreamParams params_w13(const moe_fp4_dims& d, const uint16_t* x, const Workspace& ws) {
   StreamParams P{};
   P.chunks = ws.gemv_chunks;
   P.counts = ws.counts;
@@ -416,18 +528,10 @@ cudaError_t launch_stream_w13(const moe_fp4_dims& d, const uint16_t* x, const ui
   P.n_rb = d.I / 64;
   P.wait_ns = wait_limit_ns();
   P.fault = fault_site() == MOE_FP4_FAULT_STREAM_STAGE;
-  return launch_stream<true>(mw, ms, P, st);
+  return P;
 }
 
-cudaError_t launch_stream_w2(const moe_fp4_dims& d, const uint8_t* w2, const uint8_t* w2s, const Workspace& ws,
-                             cudaStream_t st) {
-  CUtensorMap mw, ms;
-  const uint64_t rows = (uint64_t)d.E * d.d;
-  if (!make_map_2d(&mw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w2, d.I / 2, rows, d.I / 2, 128, 128,
-                   CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map_2d(&ms, CU_TENSOR_MAP_DATA_TYPE_UINT8, w2s, d.I / 32, rows, d.I / 32, 16, 128,
-                   CU_TENSOR_MAP_SWIZZLE_NONE))
-    return cudaErrorInvalidValue;
+StreamParams params_w2(const moe_fp4_dims& d, const Workspace& ws) {
   StreamParams P{};
   P.chunks = ws.gemv_chunks;
   P.counts = ws.counts;
@@ -442,7 +546,61 @@ cudaError_t launch_stream_w2(const moe_fp4_dims& d, const uint8_t* w2, const uin
   P.n_rb = d.d / 128;
   P.wait_ns = wait_limit_ns();
   P.fault = 0;
-  return launch_stream<false>(mw, ms, P, st);
+  return P;
+}
+
+}  // namespace
+
+bool stream_path_supported(const moe_fp4_dims& d) {
+  // whole 512-K stages, 64-row W13 blocks, 128-row W2 blocks; 8 token rows of
+  // K f16 activations must fit shared memory next to the ring
+  return d.d % 1024 == 0 && d.I % 1024 == 0 && d.d <= 7168 && d.I <= 7168;
+}
+
+cudaError_t launch_stream_w13(const moe_fp4_dims& d, const uint16_t* x, const uint8_t* w13, const uint8_t* w13s,
+                              const Workspace& ws, cudaStream_t st) {
+  CUtensorMap mw, ms;
+  if (!maps_w13(d, w13, w13s, &mw, &ms)) return cudaErrorInvalidValue;
+  return launch_stream<true>(mw, ms, params_w13(d, x, ws), st);
+}
+
+cudaError_t launch_stream_w2(const moe_fp4_dims& d, const uint8_t* w2, const uint8_t* w2s, const Workspace& ws,
+                             cudaStream_t st) {
+  CUtensorMap mw, ms;
+  if (!maps_w2(d, w2, w2s, &mw, &ms)) return cudaErrorInvalidValue;
+  return launch_stream<false>(mw, ms, params_w2(d, ws), st);
+}
+
+cudaError_t launch_stream_fused(const moe_fp4_dims& d, const uint16_t* x, const uint8_t* w13, const uint8_t* w13s,
+                                const uint8_t* w2, const uint8_t* w2s, const Workspace& ws, cudaStream_t st) {
+  CUtensorMap mw13, ms13, mw2, ms2;
+  if (!maps_w13(d, w13, w13s, &mw13, &ms13) || !maps_w2(d, w2, w2s, &mw2, &ms2)) return cudaErrorInvalidValue;
+  StreamParams P13 = params_w13(d, x, ws), P2 = params_w2(d, ws);
+  // one shared-memory layout for both phases: the wider activation rows
+  const int x_pitch = (d.d > d.I ? d.d : d.I) * 2 + 64;
+  int stages = 4;
+  while (stages > 2 && smem_needed(stages, x_pitch) > 227 * 1024) --stages;
+  const size_t smem = smem_needed(stages, x_pitch);
+  if (smem > 227 * 1024) return cudaErrorInvalidValue;
+  P13.x_pitch = P2.x_pitch = x_pitch;
+  P13.stages = P2.stages = stages;
+  P2.act_l2 = 1;  // h is written by the other CTAs of the same launch
+  const cudaError_t oe = ensure_smem_optin(reinterpret_cast<const void*>(stream_fused_kernel), 227 * 1024);
+  if (oe != cudaSuccess) return oe;
+  // the CTAs wait on one another (the arrival counter): a cooperative launch
+  // makes them all resident at once, one per SM
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_sms());
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int32_t* arrivals = ws.counts + 3;
+  return cudaLaunchKernelEx(&cfg, stream_fused_kernel, mw13, ms13, mw2, ms2, P13, P2, arrivals);
 }
 
 }  // namespace moe_fp4

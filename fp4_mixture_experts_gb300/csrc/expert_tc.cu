@@ -31,9 +31,9 @@
 //               tcgen05.st (lane = weight row), so that the MMA reads its A
 //               operand from tensor memory; then the epilogue (tcgen05.ld,
 //               SwiGLU + bf16 rounding of h, or y)
-// A stage is full once its token tile has landed (one mbarrier, completed by
-// the TMA byte count) and all 8 dequantisers have written their A slots (a
-// second one), and empty once both issuers' MMAs on it have completed (one
+// A stage is full once the token tile has landed and all 8 dequantisers have
+// written their A slots (one mbarrier: the producer's expect_tx and 8
+// arrivals), and empty once both issuers' MMAs on it have completed (one
 // mbarrier, two tcgen05.commit arrivals).
 // Weights are dequantised exactly (an E2M1 value times a power of two has
 // 2 significant bits), so the MMA multiplies exact products and accumulates
@@ -42,10 +42,13 @@
 // (x for W13; the f16 copy of h for W2) by a power of two of its own; both
 // factors come back in the epilogue.  Every mbarrier wait is bounded; a
 // timeout sets the error word and an abort flag that releases the other
-// roles.  On the way out every TMA copy a producer issued has landed and
-// every MMA an issuer issued has completed (waits that ignore the abort flag,
-// also bounded) before shared and tensor memory are given back, and TMEM is
-// always freed.
+// roles.  No warp leaves a loop early (after an abort it stops waiting and
+// computes on whatever the buffers hold), so warp-wide instructions always
+// see the whole warp.  On the way out every copy a producer issued has
+// landed (the token producer adds the arrivals the stopped dequantisers never
+// made to its last stages, then waits for them) and every MMA an issuer
+// issued has completed, before shared and tensor memory are given back; TMEM
+// is always freed.
 #include <cuda.h>
 
 #include <algorithm>
@@ -53,9 +56,12 @@
 
 #include "moe_fp4_internal.cuh"
 #include "ptx_sm103.cuh"
+#include "tc_helpers.cuh"
 
 namespace moe_fp4 {
 namespace {
+
+using namespace tc;
 
 constexpr int kBM = 128;                 // weight rows per accumulator
 constexpr int kBK = 64;                  // K elements per stage
@@ -100,126 +106,9 @@ constexpr int kOffRaw = kOffB + kStages * kBTileBytes;         // [stage][acc]
 constexpr int kOffRowscale = kOffRaw + kStagesRaw * 2 * kRawTileBytes;
 constexpr int kOffBar = kOffRowscale + 2 * kBM * 4;
 constexpr int kSmemTc = kOffBar + 512 + 1024;  // + barriers, 1 KB alignment slack
-static_assert((2 * kStagesRaw + 3 * kStages + 4) * 8 + 8 <= 512, "barrier area exceeded");
+static_assert((2 * kStagesRaw + 2 * kStages + 4) * 8 + 8 + 4 * kDqWarps <= 512, "barrier area exceeded");
 static_assert(kSmemTc <= 227 * 1024, "shared memory of the tensor-core kernel exceeds 227 KB");
 static_assert(kBTileBytes % 1024 == 0, "token slots must stay 1 KB aligned for the 128-byte swizzle");
-
-struct TcParams {
-  const uint8_t* w;        // packed E2M1 weights [rows][K/2]
-  const uint8_t* scales;   // E8M0 [rows][K/32]
-  const int4* tiles;       // (expert, first sorted row, rows, 0)
-  const int32_t* counts;   // counts[2] = number of tiles
-  int32_t* err;
-  uint16_t* h_out;         // W13: h [S, I]
-  float* y_out;            // W2: y [S, d]
-  const float* x_scale;    // W13: per sorted row, the inverse activation scale
-  int K;                   // reduction length
-  int rows_per_expert;     // rows of the weight tensor per expert (2I or d)
-  int mblocks;             // CTAs per token tile along the weight rows
-  int block_rows;          // weight rows advanced per m-block (128 W13, 256 W2)
-  int acc1_offset;         // row offset of accumulator 1 (I for up rows, 128 for W2)
-  int I, d;
-  uint64_t wait_ns;        // limit of every mbarrier wait
-  int fault;               // nonzero: CTA 0 withholds its first token tile (fault-injection test)
-};
-
-// UMMA shared-memory descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
-__device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) {
-  uint64_t d = 0;
-  d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)(16u >> 4) << 16;     // leading byte offset (unused for swizzled K-major)
-  d |= (uint64_t)(1024u >> 4) << 32;   // stride byte offset
-  d |= (uint64_t)1 << 46;              // descriptor version
-  d |= (uint64_t)2 << 61;              // 128-byte swizzle
-  return d;
-}
-
-// Instruction descriptor of kind::f16 with f32 accumulation, both operands
-// K-major; A and B share one type (f16 = 0, bf16 = 1).
-__device__ __forceinline__ uint32_t idesc_f16kind(int M, int N, uint32_t ab_type) {
-  return (1u << 4)                                // D format f32
-         | (ab_type << 7) | (ab_type << 10)       // A, B format
-         | ((uint32_t)(N >> 3) << 17)             // N
-         | ((uint32_t)(M >> 4) << 24);            // M
-}
-
-// D[tmem] (+)= A[tmem] * B[smem]: the A operand is read from tensor memory
-__device__ __forceinline__ void umma_tmem_a(uint32_t tmem_d, uint32_t tmem_a, uint64_t b, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(tmem_d),
-      "r"(tmem_a), "l"(b), "r"(idesc), "r"(acc)
-      : "memory");
-}
-
-// this thread's TMEM lane, 32 consecutive 32-bit columns from taddr
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
-      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
-      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
-      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
-      : "memory");
-}
-
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-}
-
-// this thread's TMEM lane, 32 columns from each of two addresses, with one
-// wait for both loads
-__device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, float (&va)[32], float (&vb)[32]) {
-  uint32_t a[32], b[32];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n\t"
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
-      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n\t"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]),
-        "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]), "=r"(a[14]), "=r"(a[15]),
-        "=r"(a[16]), "=r"(a[17]), "=r"(a[18]), "=r"(a[19]), "=r"(a[20]), "=r"(a[21]), "=r"(a[22]), "=r"(a[23]),
-        "=r"(a[24]), "=r"(a[25]), "=r"(a[26]), "=r"(a[27]), "=r"(a[28]), "=r"(a[29]), "=r"(a[30]), "=r"(a[31]),
-        "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3]), "=r"(b[4]), "=r"(b[5]), "=r"(b[6]), "=r"(b[7]),
-        "=r"(b[8]), "=r"(b[9]), "=r"(b[10]), "=r"(b[11]), "=r"(b[12]), "=r"(b[13]), "=r"(b[14]), "=r"(b[15]),
-        "=r"(b[16]), "=r"(b[17]), "=r"(b[18]), "=r"(b[19]), "=r"(b[20]), "=r"(b[21]), "=r"(b[22]), "=r"(b[23]),
-        "=r"(b[24]), "=r"(b[25]), "=r"(b[26]), "=r"(b[27]), "=r"(b[28]), "=r"(b[29]), "=r"(b[30]), "=r"(b[31])
-      : "r"(ta), "r"(tb)
-      : "memory");
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    va[i] = __uint_as_float(a[i]);
-    vb[i] = __uint_as_float(b[i]);
-  }
-}
-
-// 4 consecutive bytes of shared memory, one per register (zero-extended):
-// one load instead of a word load and three shifts on the busy ALU pipe.  Not
-// volatile, so it may be scheduled early; the memory clobber keeps it after the
-// barrier waits that make the bytes valid.
-__device__ __forceinline__ void lds_bytes4(const uint8_t* p, uint32_t (&b)[4]) {
-  asm("ld.shared.v4.u8 {%0,%1,%2,%3}, [%4];"
-      : "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3])
-      : "r"(smem_u32(p))
-      : "memory");
-}
-
-__device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
-  uint32_t r;
-  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
-  return r;
-}
-
-// f16x2 (m, m) with m = 2^e for e in [-24, 15]: normal for e >= -14,
-// subnormal below; 0 for e < -24
-__device__ __forceinline__ uint32_t f16x2_pow2(int e) {
-  const uint32_t b = e >= -14 ? (uint32_t)(e + 15) << 10 : (e >= -24 ? 1u << (e + 24) : 0u);
-  return b | (b << 16);
-}
-
 
 // Geometry of one work item: token rows [row0, row0 + n) of one expert (n <=
 // 192) times two 128-row weight blocks (m-block mb).  TMEM holds the ring of
@@ -262,14 +151,14 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
   float* rowscale = reinterpret_cast<float*>(smem + kOffRowscale);  // [2][128]
   uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint64_t* raw_empty = raw_full + kStagesRaw;
-  uint64_t* bfull = raw_empty + kStagesRaw;   // [stage]: token tile landed (TMA byte count)
-  uint64_t* afull = bfull + kStages;          // [stage]: all 8 dequantisers wrote their A slots
-  uint64_t* empty = afull + kStages;          // [stage]: the MMAs of both accumulators on it completed
+  uint64_t* full = raw_empty + kStagesRaw;    // [stage]: token tile landed and both A slots written
+  uint64_t* empty = full + kStages;           // [stage]: the MMAs of both accumulators on it completed
   uint64_t* acc_full = empty + kStages;       // per item: both accumulators final
   uint64_t* acc_empty = acc_full + 1;         // per item: the epilogue has read the accumulators
   uint64_t* mma_done = acc_empty + 1;         // [2]: every MMA of that issuer completed (on the way out)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* dq_arrived = abort_flag + 1;  // [8]: stages each dequantiser signalled (published on the way out)
   const uint64_t lim = P.wait_ns;
 
   const int items = P.counts[2] * P.mblocks;
@@ -284,8 +173,7 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
       mbar_init(&raw_empty[s], kDqWarps);
     }
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bfull[s], 1);            // the token producer's expect_tx
-      mbar_init(&afull[s], kDqWarps);     // one arrival per dequantiser warp
+      mbar_init(&full[s], kDqWarps + 1);  // the dequantisers and the token producer's expect_tx
       mbar_init(&empty[s], 2);            // one commit per MMA issuer
     }
     mbar_init(acc_full, 2);
@@ -323,9 +211,8 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
             ok = false;
             break;
           }
-          // one copy per slot in flight: after an abort the slot may come back
-          // before its previous copy landed (a no-op wait otherwise)
-          if (g >= kStagesRaw) mbar_wait_drain(&raw_full[s], ((g / kStagesRaw) & 1) ^ 1u, P.err, kErrWaitTimeout, lim);
+          // (a slot comes back only once every dequantiser read its bytes, or
+          // saw the abort that the check above catches: one copy per slot)
           mbar_expect_tx(&raw_full[s], 2 * kRawTileBytes);
           uint8_t* raw = smem + kOffRaw + s * 2 * kRawTileBytes;
           tma_load_2d_hint(raw, &map_raw, rs * kRawRowBytes, t.wrow0, &raw_full[s], pol);
@@ -338,40 +225,62 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
     }
   } else if (warp == kBWarp) {
     // ---------------- TMA producer: token tiles ----------------
+    // A slot comes back (empty) only after the MMAs ran on its previous use,
+    // whose copy had landed: at most one copy per slot is ever in flight.
+    int slot_g[kStages];       // per slot: the stage (counted over all items) of its last copy, or -1
+    uint32_t slot_par = 0;     // bit s: phase parity of that copy
+    uint32_t slot_real = 0;    // bit s: the copy was issued (not withheld)
+#pragma unroll
+    for (int s = 0; s < kStages; ++s) slot_g[s] = -1;
     if (lane == 0) {
-      uint32_t ph = 0;     // bit s: parity of slot s's next use
-      uint32_t nxt = 0;    // bit s: parity of the next copy into slot s (its bfull phase)
-      uint32_t has = 0;    // bit s: slot s received a copy
+      uint32_t ph = 0;
+      int g = 0;
       bool withhold = P.fault != 0 && blockIdx.x == 0;
       bool ok = true;
       for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
         const TcItem t = tc_item(P, it);
         const int boxes = (t.n_mma + kBBoxRows - 1) / kBBoxRows;
-        for (int ks = 0; ks < nk; ++ks) {
+        for (int ks = 0; ks < nk; ++ks, ++g) {
           const int s = ks % t.nS;
-          if (!mbar_wait(&empty[s], ((ph >> s) & 1) ^ 1u, abort_flag, P.err, kErrWaitTimeout, lim) || *abort_flag) {
+          const uint32_t par = (ph >> s) & 1;
+          if (!mbar_wait(&empty[s], par ^ 1u, abort_flag, P.err, kErrWaitTimeout, lim) || *abort_flag) {
             ok = false;
             break;
           }
           ph ^= 1u << s;
-          // one copy per slot in flight (see the packed-weight producer)
-          if ((has >> s) & 1) mbar_wait_drain(&bfull[s], ((nxt >> s) & 1) ^ 1u, P.err, kErrWaitTimeout, lim);
+          slot_g[s] = g;
+          slot_par = (slot_par & ~(1u << s)) | (par << s);
           if (withhold) {
             // fault injection: this tile never arrives, so the MMA issuers'
-            // wait on it runs out and the kernel takes its abort path
+            // wait on the stage runs out and the kernel takes its abort path
             withhold = false;
+            slot_real &= ~(1u << s);
             continue;
           }
-          mbar_expect_tx(&bfull[s], boxes * kBBoxBytes);
+          slot_real |= 1u << s;
+          mbar_expect_tx(&full[s], boxes * kBBoxBytes);
           uint8_t* b = smem + kOffB + s * kBTileBytes;
           for (int i = 0; i < boxes; ++i)
-            tma_load_2d(b + i * kBBoxBytes, &map_b, ks * kBK, t.row0 + i * kBBoxRows, &bfull[s]);
-          nxt ^= 1u << s;
-          has |= 1u << s;
+            tma_load_2d(b + i * kBBoxBytes, &map_b, ks * kBK, t.row0 + i * kBBoxRows, &full[s]);
         }
       }
-      for (int s = 0; s < kStages; ++s)
-        if ((has >> s) & 1) mbar_wait_drain(&bfull[s], ((nxt >> s) & 1) ^ 1u, P.err, kErrWaitTimeout, lim);
+    }
+    // wait for the dequantisers to stop, then (after an abort) let each copy
+    // still in flight complete its stage: add the arrivals of the
+    // dequantisers that stopped before it, and wait for the bytes
+    __syncwarp();
+    asm volatile("bar.sync 3, %0;" ::"r"((kDqWarps + 1) * 32) : "memory");
+    if (lane == 0 && *abort_flag) {
+#pragma unroll
+      for (int s = 0; s < kStages; ++s) {
+        if (slot_g[s] < 0 || !((slot_real >> s) & 1)) continue;
+        int arrived = 0;
+        for (int w = 0; w < kDqWarps; ++w) arrived += dq_arrived[w] > slot_g[s] ? 1 : 0;
+        if (arrived < kDqWarps)
+          asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(&full[s])),
+                       "r"(kDqWarps - arrived) : "memory");
+        mbar_wait_drain(&full[s], (slot_par >> s) & 1, P.err, kErrWaitTimeout, lim);
+      }
     }
   } else if (warp == kMmaWarp || warp == kMma1Warp) {
     // ---------------- MMA issuers, one per accumulator ----------------
@@ -388,9 +297,7 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
         const uint32_t d_tmem = tmem + t.acc0 + acc * t.acc_cols;
         for (int ks = 0; ks < nk; ++ks) {
           const int s = ks % t.nS;
-          const uint32_t par = (ph >> s) & 1;
-          if (!mbar_wait(&bfull[s], par, abort_flag, P.err, kErrWaitTimeout, lim) ||
-              !mbar_wait(&afull[s], par, abort_flag, P.err, kErrWaitTimeout, lim)) {
+          if (!mbar_wait(&full[s], (ph >> s) & 1, abort_flag, P.err, kErrWaitTimeout, lim)) {
             ok = false;
             break;
           }
@@ -422,8 +329,10 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
     uint32_t ph = 0;                         // A-slot phase bits
     uint32_t g = 0;                          // packed-weight stages consumed so far (all items)
     int li = 0;
-    bool ok = true;
-    for (int it = blockIdx.x; it < items && ok; it += gridDim.x, ++li) {
+    int gdq = 0;                             // stages this warp signalled full (lane 0's count)
+    bool ok = true;                          // this lane's waits have all succeeded
+    bool stop = false;                       // all dequantisers stop after this item (uniform)
+    for (int it = blockIdx.x; it < items && !stop; it += gridDim.x, ++li) {
       const TcItem t = tc_item(P, it);
       // a W2 tile whose second block runs past the expert's d rows (d % 256 ==
       // 128) reads a valid row there instead (its results are not written),
@@ -464,19 +373,16 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
         sc_next = *reinterpret_cast<const uint16_t*>(srow);
       }
 #pragma unroll kDqUnroll
-      for (int ks = 0; ks < nk && ok; ++ks) {
+      for (int ks = 0; ks < nk; ++ks) {
         const int sa = ks % t.nS;
         const int sub = ks % kRawSteps;
         const uint32_t gs = g + ks / kRawSteps;
         const int rs_slot = gs % kStagesRaw;
-        // every wait's outcome is made uniform over the warp, so that the
-        // warp-wide tcgen05 instructions below see all 32 lanes or none
-        if (sub == 0 &&
-            !__all_sync(0xFFFFFFFFu, mbar_wait(&raw_full[rs_slot], (gs / kStagesRaw) & 1, abort_flag, P.err,
-                                                kErrWaitTimeout, lim))) {
-          ok = false;
-          break;
-        }
+        // once a wait has failed (or seen the abort) this lane stops waiting
+        // but keeps converting, so that the warp-wide tcgen05 instructions
+        // below always see all 32 lanes
+        if (sub == 0 && ok)
+          ok = mbar_wait(&raw_full[rs_slot], (gs / kStagesRaw) & 1, abort_flag, P.err, kErrWaitTimeout, lim);
         // 128-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ (r mod 8),
         // so the 8 rows of a warp's quarter hit 8 different bank groups.  The
         // packed bytes are read as they are converted (one byte per register);
@@ -497,11 +403,9 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
           sc = sc_next;
           if (ks + 1 < nk) sc_next = *reinterpret_cast<const uint16_t*>(srow + 2 * (ks + 1));
         }
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&empty[sa], ((ph >> sa) & 1) ^ 1u, abort_flag, P.err, kErrWaitTimeout,
-                                                lim))) {
-          ok = false;
-        } else {
-          ph ^= 1u << sa;
+        if (ok) ok = mbar_wait(&empty[sa], ((ph >> sa) & 1) ^ 1u, abort_flag, P.err, kErrWaitTimeout, lim);
+        ph ^= 1u << sa;
+        {
           const uint32_t s0 = sc & 0xFFu, s1 = (sc >> 8) & 0xFFu;
           const uint32_t m0 = f16x2_pow2((int)s0 - s_ref), m1 = f16x2_pow2((int)s1 - s_ref);
           uint32_t av[32];  // column j = K elements (2j, 2j+1) of this row
@@ -515,13 +419,16 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
           }
           if (sub == kRawSteps - 1 || ks == nk - 1) {
             __syncwarp();
-            if (lane == 0) mbar_arrive(&raw_empty[rs_slot]);  // the stage's packed bytes have all been read
+            if (lane == 0 && ok) mbar_arrive(&raw_empty[rs_slot]);  // the stage's packed bytes have all been read
           }
           tmem_st32(lane_base + (sa * 2 + acc) * kASlotCols, av);
           asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
           asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
           __syncwarp();
-          if (lane == 0) mbar_arrive(&afull[sa]);
+          if (lane == 0 && ok) {
+            mbar_arrive(&full[sa]);
+            ++gdq;
+          }
         }
       }
       g += nrs;
@@ -539,7 +446,7 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
       }
       // the row scales written above must be visible to every epilogue warp
       asm volatile("bar.sync 1, %0;" ::"r"(kDqWarps * 32) : "memory");
-      if (ok && __all_sync(0xFFFFFFFFu, mbar_wait(acc_full, li & 1, abort_flag, P.err, kErrWaitTimeout, lim))) {
+      if (__all_sync(0xFFFFFFFFu, ok && mbar_wait(acc_full, li & 1, abort_flag, P.err, kErrWaitTimeout, lim))) {
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         const float rs0 = rowscale[r], rs1 = rowscale[128 + r];
 #pragma unroll
@@ -582,15 +489,18 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
       // before any of them writes the next item's A slots (which may cover
       // them); a failure seen by any of them stops all of them together, so
       // that they keep meeting at the same named barriers
-      uint32_t stop;
+      uint32_t st;
       asm volatile(
           "{\n\t.reg .pred pin, pout;\n\tsetp.ne.u32 pin, %1, 0;\n\tbar.red.or.pred pout, 1, %2, pin;\n\t"
           "selp.u32 %0, 1, 0, pout;\n}"
-          : "=r"(stop)
+          : "=r"(st)
           : "r"((!ok || *abort_flag) ? 1u : 0u), "r"(kDqWarps * 32)
           : "memory");
-      if (stop) ok = false;
+      stop = st != 0;
     }
+    // how far this warp got, for the token producer's way out
+    if (lane == 0) dq_arrived[dq] = gdq;
+    asm volatile("bar.arrive 3, %0;" ::"r"((kDqWarps + 1) * 32) : "memory");
   }
   // every warp reconverges first: lanes that skipped a lane-0 role must not
   // arrive at the CTA barrier ahead of their lane 0 (an aligned barrier counts

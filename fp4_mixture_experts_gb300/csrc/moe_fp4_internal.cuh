@@ -85,11 +85,15 @@ cudaError_t launch_stream_w13(const moe_fp4_dims& d, const uint16_t* x, const ui
                               const Workspace& ws, cudaStream_t st);
 cudaError_t launch_stream_w2(const moe_fp4_dims& d, const uint8_t* w2, const uint8_t* w2s, const Workspace& ws,
                              cudaStream_t st);
+cudaError_t launch_stream_fused(const moe_fp4_dims& d, const uint16_t* x, const uint8_t* w13, const uint8_t* w13s,
+                                const uint8_t* w2, const uint8_t* w2s, const Workspace& ws, cudaStream_t st);
 cudaError_t launch_tc_w13(const moe_fp4_dims& d, const uint8_t* w13, const uint8_t* w13s, const Workspace& ws,
                           cudaStream_t st);
 cudaError_t launch_tc_w2(const moe_fp4_dims& d, const uint8_t* w2, const uint8_t* w2s, const Workspace& ws,
                          cudaStream_t st);
 cudaError_t launch_combine(const moe_fp4_dims& d, float* out, const Workspace& ws, cudaStream_t st);
+cudaError_t launch_router(const moe_fp4_dims& d, const uint16_t* x, const uint16_t* wg, float* logits,
+                          cudaStream_t st);
 
 // ---------------------------------------------------------------------------
 // device helpers

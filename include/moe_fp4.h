@@ -94,6 +94,14 @@ typedef enum moe_fp4_status {
 #define MOE_FP4_FLAG_FORCE_GEMV 0x1u    /* streaming path: weights streamed once, warp-level mma.sync
                                            (d, I multiples of 1024) */
 #define MOE_FP4_FLAG_FORCE_TC   0x2u    /* tcgen05 tensor-core path */
+/* On the streaming path: both projections in one persistent launch (W13 +
+ * SwiGLU, a grid-wide arrival counter with a bounded wait, then W2), one CTA
+ * per SM launched cooperatively, instead of two launches (the paper's
+ * per-layer synchronisation and launch cost, abstract: limits).  The same
+ * results; in moe_fp4_forward_profiled the W13 stage then covers both
+ * projections and the W2 stage is empty.  May be combined with
+ * MOE_FP4_FLAG_FORCE_GEMV; ignored on the tensor-core path. */
+#define MOE_FP4_FLAG_PERSISTENT 0x4u
 
 /* Bytes of device workspace a call with these sizes needs (256-byte aligned
  * base required).  Returns 0 when the sizes are invalid or unsupported:
@@ -113,13 +121,39 @@ int moe_fp4_route(const moe_fp4_dims* dims, const float* router_logits,
 /* The whole layer (steps 1-4) on device buffers.  out is required; the
  * routing outputs and h are optional (NULL: kept in the workspace only).
  * x, w13, w13_scale, w2, w2_scale, out and h must be 16-byte aligned,
- * the routing outputs 4-byte aligned, the workspace 256-byte aligned.  flags: 0 or one MOE_FP4_FLAG_FORCE_*. */
+ * the routing outputs 4-byte aligned, the workspace 256-byte aligned.  flags: 0 or one MOE_FP4_FLAG_FORCE_*,
+ * optionally with MOE_FP4_FLAG_PERSISTENT. */
 int moe_fp4_forward(const moe_fp4_dims* dims, const void* x_bf16, const float* router_logits,
                     const uint8_t* w13, const uint8_t* w13_scale,
                     const uint8_t* w2, const uint8_t* w2_scale, float* out,
                     int32_t* topk_ids, float* topk_weights, int32_t* expert_offsets,
                     int32_t* sorted_slot, void* h_bf16, unsigned flags,
                     void* workspace, size_t workspace_bytes, void* cuda_stream);
+
+/* The router (gate) projection, the step ahead of top-k routing:
+ *   router_logits[t, e] = sum_K x[t, K] * w_gate[e, K]
+ * with bf16 x [T, d] and bf16 w_gate [E, d] (row e = expert e's gate
+ * vector), every product exact, fp32 accumulation, fp32 logits [T, E] (the
+ * MI250 correctness blog, section 4.1: low-precision inputs with FP32
+ * accumulation for the gate network, FP32 values for the top-k comparison).
+ * The sum order is fixed, so the logits are the same on every call.  x and
+ * w_gate 16-byte aligned, router_logits 4-byte aligned; dims as for
+ * moe_fp4_forward (I and k are not used).  One kernel is enqueued; no
+ * workspace. */
+int moe_fp4_router(const moe_fp4_dims* dims, const void* x_bf16, const void* w_gate_bf16,
+                   float* router_logits, void* cuda_stream);
+
+/* The whole layer starting from x and the router weights: moe_fp4_router
+ * writes router_logits (a required [T, E] fp32 device buffer owned by the
+ * caller), then moe_fp4_forward runs on them.  Same arguments, checks and
+ * results as moe_fp4_forward otherwise; every argument is checked before
+ * anything is enqueued. */
+int moe_fp4_forward_gated(const moe_fp4_dims* dims, const void* x_bf16, const void* w_gate_bf16,
+                          float* router_logits, const uint8_t* w13, const uint8_t* w13_scale,
+                          const uint8_t* w2, const uint8_t* w2_scale, float* out,
+                          int32_t* topk_ids, float* topk_weights, int32_t* expert_offsets,
+                          int32_t* sorted_slot, void* h_bf16, unsigned flags,
+                          void* workspace, size_t workspace_bytes, void* cuda_stream);
 
 /* moe_fp4_forward that also records caller-created CUDA events (cudaEvent_t
  * handles, MOE_FP4_NUM_STAGE_EVENTS of them) on the stream between its

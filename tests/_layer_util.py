@@ -21,9 +21,16 @@ MAX_ABS = 2e-2
 # v = silu(g) u gives the interval of v, and h may be the bf16 rounding of
 # any value in it: an element whose exact v lies within that distance of a
 # bf16 rounding boundary may come out one bf16 ulp away from the oracle's h,
-# and where g or u cancel the interval widens accordingly.
+# and where g or u cancel the interval widens accordingly.  At the bottom of
+# the fp32 range the fast SiLU loses its result: for g below about -88,
+# exp(-g) overflows and silu(g) evaluates to 0 although its exact value,
+# about g e^g, is still a (tiny) fp32 number, and products below the smallest
+# normal fp32 are flushed to zero; where |silu(g)| < 2^-119 or |v| < 2^-125
+# the interval reaches 0.
 H_SUM_ERR = 4.0
 H_EVAL_ERR = 2.0 ** -20
+SILU_UNDERFLOW = 2.0 ** -119
+V_UNDERFLOW = 2.0 ** -125
 
 
 def to_device(L, dev="cuda:0"):
@@ -59,7 +66,11 @@ def h_interval(x_rows, w13_e, w13s_e):
     """For token rows x_rows (fp64 [m, d]) of one expert: the range of bf16 values
     an fp32 evaluation of h = bf16(silu(g) u) may produce, from the exact g and
     u and the error model above.  Returns (lo, hi), fp64 [m, I]."""
-    W = oracle.dequantize_rows(w13_e, w13s_e)
+    return h_interval_w(x_rows, oracle.dequantize_rows(w13_e, w13s_e))
+
+
+def h_interval_w(x_rows, W):
+    """h_interval with the expert's dequantised W13 rows W (fp64 [2I, d])."""
     I = W.shape[0] // 2
     K = W.shape[1]
     g = x_rows @ W[:I].T
@@ -76,6 +87,8 @@ def h_interval(x_rows, w13_e, w13s_e):
         v = silu * u
         dv = np.abs(dsilu * u) * eg + np.abs(silu) * eu + H_EVAL_ERR * np.abs(v)
     dv = np.nan_to_num(dv, nan=np.inf)
+    under = (np.abs(silu) < SILU_UNDERFLOW) | (np.abs(v) < V_UNDERFLOW)
+    dv = np.where(under, np.maximum(dv, np.abs(v)), dv)
     return oracle.bf16_round(v - dv), oracle.bf16_round(v + dv)
 
 
@@ -108,3 +121,44 @@ def assert_h_within(got_bits, want, lo, hi, what=""):
                           f"got {got[mism][~ok][:4]}, want {want[mism][~ok][:4]}, "
                           f"interval {lo[mism][~ok][:4]} .. {hi[mism][~ok][:4]}")
     return int(mism.sum())
+
+
+def assert_out_within(got, want, L, toks=None, what=""):
+    """out from the GPU against the oracle's out (rows `toks` of the layer, or
+    all): relative L2 and cosine over the whole array, and every element
+    within MAX_ABS plus the slack that legitimate h rounding decisions imply.
+
+    Where an exact h value lies within fp32 error of a bf16 rounding boundary
+    the kernel may round it the other way (h_interval); one bf16 ulp of a large
+    h (ulp 1 at |h| >= 128) times a W2 weight (up to 6 * 2^-5) times the
+    routing weight moves out by several 1e-2.  For every token with an element
+    beyond MAX_ABS the slack is sum_j w_tj sum_i dh_i |W2_e[n, i]|, with dh the
+    distance from the oracle's h to the far end of its interval: computed from
+    the oracle's own values only.  Returns the metrics and the largest excess
+    over MAX_ABS that the slack had to cover."""
+    m = out_metrics(got, want)
+    assert m["rel_l2"] <= REL_L2 and m["cosine"] >= COSINE, f"{what}: {m}"
+    got = np.asarray(got, dtype=np.float64)
+    toks = np.arange(L.T) if toks is None else np.asarray(toks)
+    diff = np.abs(got - want)
+    bad = np.nonzero((diff > MAX_ABS).any(axis=1))[0]
+    if bad.size == 0:
+        return m, 0.0
+    x = oracle.bf16_bits_to_f64(L.x_bf16)
+    ids, w = oracle.route(L.router_logits[toks[bad]], L.k)
+    slack = np.zeros((bad.size, L.d))
+    for e in np.unique(ids):
+        rows, slots = np.nonzero(ids == e)
+        xr = x[toks[bad][rows]]
+        W13 = oracle.dequantize_rows(L.w13[e], L.w13_scale[e])
+        lo, hi = h_interval_w(xr, W13)
+        h, _ = oracle.expert_ffn(xr, L.w13[e], L.w13_scale[e], L.w2[e], L.w2_scale[e])
+        dh = np.maximum(hi - h, h - lo)
+        W2 = np.abs(oracle.dequantize_rows(L.w2[e], L.w2_scale[e]))
+        slack[rows] += w[rows, slots][:, None] * (dh @ W2.T)
+    excess = diff[bad] - MAX_ABS
+    ok = excess <= slack * (1 + 1e-6)
+    assert ok.all(), (f"{what}: out beyond MAX_ABS + h-rounding slack at token {toks[bad][np.nonzero(~ok)[0][:4]]}: "
+                      f"excess {excess[~ok][:4]}, slack {slack[~ok][:4]}")
+    m["tokens_beyond_max_abs"] = int(bad.size)
+    return m, float(excess.max())

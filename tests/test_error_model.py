@@ -58,3 +58,32 @@ def test_interval_rejects_a_one_percent_error():
     bad = oracle.bf16_round(h * 1.01)
     big = np.abs(h) > 1e-3 * np.abs(h).max()
     assert np.mean((bad[big] < lo[big]) | (bad[big] > hi[big])) > 0.9
+
+
+def test_interval_reaches_zero_where_fp32_silu_underflows():
+    # g far below -88: exp(-g) overflows fp32 and the fast SiLU gives 0, while
+    # the exact h is a tiny nonzero value; 0 must lie in the interval
+    L = make_layer(T=4, d=64, I=32, E=1, k=1, seed=74)
+    x = oracle.bf16_bits_to_f64(L.x_bf16)
+    W = oracle.dequantize_rows(L.w13[0], L.w13_scale[0])
+    W[:32] *= 200.0 / np.abs(x @ W[:32].T).max()   # |g| up to 200
+    from _layer_util import h_interval_w
+    lo, hi = h_interval_w(x, W)
+    g = x @ W[:32].T
+    deep = g < -100
+    assert deep.any()
+    assert np.all((lo[deep] <= 0) & (hi[deep] >= 0))
+
+
+def test_out_slack_covers_a_flip_and_nothing_more():
+    # an h element one bf16 ulp off (inside its interval) moves out by at most
+    # the slack; an error in W2 (a weight doubled) is not covered
+    from _layer_util import MAX_ABS, assert_out_within, h_interval_w
+    L = make_layer(T=6, d=128, I=64, E=2, k=1, seed=75)
+    ref = oracle.forward(L.x_bf16, L.router_logits, L.w13, L.w13_scale, L.w2, L.w2_scale, L.k)
+    assert_out_within(ref["out"], ref["out"], L)
+    wrong = ref["out"].copy()
+    wrong[2, 5] += 50 * MAX_ABS
+    import pytest
+    with pytest.raises(AssertionError):
+        assert_out_within(wrong, ref["out"], L)
