@@ -59,6 +59,7 @@ bool layout_workspace(const moe_fp4_dims& d, void* base, bool with_staging, Work
   ws->h_scale = ws->x_scale;
   ws->h = (uint16_t*)take(S * d.I * sizeof(uint16_t));
   ws->y = (float*)take(S * d.d * sizeof(float));
+  ws->combine_cnt = (int32_t*)take((size_t)d.T * ((d.d + 255) / 256) * sizeof(int32_t));
   if (with_staging) {
     ws->stage_x = (uint16_t*)take((size_t)d.T * d.d * sizeof(uint16_t));
     ws->stage_logits = (float*)take((size_t)d.T * d.E * sizeof(float));
@@ -95,6 +96,7 @@ int run_forward(const moe_fp4_dims& d, const void* x, const float* logits, const
   cudaError_t e = launch_route(d, logits, ws, st);
   if (e != cudaSuccess) return MOE_FP4_ERR_CUDA;
   mark(1);
+  bool fused_combine = false;
   if (use_gemv_path(d, flags)) {
     mark(2);
     if (stream_path_supported(d) && (flags & MOE_FP4_FLAG_PERSISTENT)) {
@@ -112,19 +114,22 @@ int run_forward(const moe_fp4_dims& d, const void* x, const float* logits, const
   } else {
     e = launch_gather(d, xb, ws, st);
     mark(2);
-    if (e == cudaSuccess) e = launch_tc_w13(d, w13, w13s, ws, st);
+    const bool pairs = (flags & MOE_FP4_FLAG_CTA_PAIRS) != 0;
+    if (e == cudaSuccess) e = launch_tc_w13(d, w13, w13s, ws, pairs, st);
     mark(3);
     if (e == cudaSuccess) e = launch_h_f16(d, ws, st);  // counted in the W2 stage
-    if (e == cudaSuccess) e = launch_tc_w2(d, w2, w2s, ws, st);
+    if (e == cudaSuccess) e = launch_tc_w2(d, w2, w2s, ws, out, pairs, st);
+    fused_combine = tc_fused_combine(pairs);
   }
   mark(4);
-  if (e == cudaSuccess) e = launch_combine(d, out, ws, st);
+  if (e == cudaSuccess && !fused_combine) e = launch_combine(d, out, ws, st);
   mark(5);
   return e == cudaSuccess ? MOE_FP4_OK : MOE_FP4_ERR_CUDA;
 }
 
 int check_flags(unsigned flags) {
-  const unsigned known = MOE_FP4_FLAG_FORCE_GEMV | MOE_FP4_FLAG_FORCE_TC | MOE_FP4_FLAG_PERSISTENT;
+  const unsigned known =
+      MOE_FP4_FLAG_FORCE_GEMV | MOE_FP4_FLAG_FORCE_TC | MOE_FP4_FLAG_PERSISTENT | MOE_FP4_FLAG_CTA_PAIRS;
   if (flags & ~known) return MOE_FP4_ERR_INVALID_ARG;
   if ((flags & MOE_FP4_FLAG_FORCE_GEMV) && (flags & MOE_FP4_FLAG_FORCE_TC)) return MOE_FP4_ERR_INVALID_ARG;
   return MOE_FP4_OK;

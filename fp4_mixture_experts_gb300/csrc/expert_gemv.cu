@@ -146,7 +146,9 @@ w2_rows_kernel(const uint16_t* __restrict__ h, const uint8_t* __restrict__ w2,
 // so every bf16 value within 2^31 of it converts exactly.  One warp per row.
 __global__ void __launch_bounds__(256)
 gather_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ sorted_slot, int S, int k, int d,
-              uint16_t* __restrict__ x_perm, float* __restrict__ x_scale) {
+              uint16_t* __restrict__ x_perm, float* __restrict__ x_scale, int32_t* __restrict__ zero, int n_zero) {
+  // the W2 kernel's combine counters of this call start at zero
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_zero; i += gridDim.x * blockDim.x) zero[i] = 0;
   // sorted_slot == nullptr: row r of x itself (the f16 copy of h for the tensor-core W2)
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   const int nwarps = (gridDim.x * blockDim.x) >> 5;
@@ -227,14 +229,15 @@ cudaError_t launch_gather(const moe_fp4_dims& d, const uint16_t* x, const Worksp
   const int S = d.T * d.k;
   int blocks = (S + 7) / 8;
   if (blocks > num_sms() * 16) blocks = num_sms() * 16;
-  gather_kernel<<<blocks, 256, 0, st>>>(x, ws.sorted_slot, S, d.k, d.d, ws.x_perm, ws.x_scale);
+  gather_kernel<<<blocks, 256, 0, st>>>(x, ws.sorted_slot, S, d.k, d.d, ws.x_perm, ws.x_scale, ws.combine_cnt,
+                                       d.T * ((d.d + 255) / 256));
   return cudaGetLastError();
 }
 
 cudaError_t launch_h_f16(const moe_fp4_dims& d, const Workspace& ws, cudaStream_t st) {
   const int S = d.T * d.k;
   const int blocks = (S + 7) / 8 < num_sms() * 16 ? (S + 7) / 8 : num_sms() * 16;
-  gather_kernel<<<blocks, 256, 0, st>>>(ws.h, nullptr, S, 1, d.I, ws.h16, ws.h_scale);
+  gather_kernel<<<blocks, 256, 0, st>>>(ws.h, nullptr, S, 1, d.I, ws.h16, ws.h_scale, nullptr, 0);
   return cudaGetLastError();
 }
 

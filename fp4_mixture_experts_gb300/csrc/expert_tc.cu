@@ -97,6 +97,12 @@ constexpr uint32_t kASlotCols = kBK / 2;
 static_assert(2 * ((kBN + 31) / 32 * 32) + 2 * 2 * kASlotCols <= kTmemCols, "TMEM columns exceeded at the widest tile");
 static_assert(kStages >= 2 && kStages <= 4, "ring of 2 to 4 stages");
 
+#ifndef MOE_TC_FUSED_COMBINE
+#define MOE_TC_FUSED_COMBINE 1
+#endif
+// 1: the pair kernel's W2 epilogue also performs the weighted combine
+constexpr bool kFusedCombine = MOE_TC_FUSED_COMBINE != 0;
+constexpr int kPairBoxRows = 32;                  // token rows per TMA box of the pair kernel
 constexpr int kBBoxRows = 64;                     // token rows per TMA box
 constexpr int kBBoxBytes = kBBoxRows * kBK * 2;   // 8 KB
 constexpr int kBTileBytes = (kBN + kBBoxRows - 1) / kBBoxRows * kBBoxBytes;  // whole 64-row boxes
@@ -248,7 +254,9 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
             break;
           }
           ph ^= 1u << s;
-          slot_g[s] = g;
+#pragma unroll
+          for (int q = 0; q < kStages; ++q)  // unrolled: the records stay in registers
+            if (q == s) slot_g[q] = g;
           slot_par = (slot_par & ~(1u << s)) | (par << s);
           if (withhold) {
             // fault injection: this tile never arrives, so the MMA issuers'
@@ -531,13 +539,13 @@ cudaError_t launch_tc(const CUtensorMap& b, const CUtensorMap& raw, const TcPara
 }  // namespace
 
 cudaError_t launch_tc_w13(const moe_fp4_dims& d, const uint8_t* w13, const uint8_t* w13s, const Workspace& ws,
-                          cudaStream_t st) {
+                          bool pairs, cudaStream_t st) {
   const size_t S = (size_t)d.T * d.k;
   CUtensorMap b, raw;
   if (!make_map_2d(&raw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w13, d.d / 2, (uint64_t)d.E * 2 * d.I, d.d / 2, kRawRowBytes, kBM,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map_2d(&b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws.x_perm, d.d, S, (uint64_t)d.d * 2, kBK, kBBoxRows,
-                   CU_TENSOR_MAP_SWIZZLE_128B))
+      !make_map_2d(&b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws.x_perm, d.d, S, (uint64_t)d.d * 2, kBK,
+                   pairs ? kPairBoxRows : kBBoxRows, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   TcParams P{};
   P.w = w13;
@@ -549,24 +557,36 @@ cudaError_t launch_tc_w13(const moe_fp4_dims& d, const uint8_t* w13, const uint8
   P.x_scale = ws.x_scale;
   P.K = d.d;
   P.rows_per_expert = 2 * d.I;
-  P.mblocks = d.I / kBM;
-  P.block_rows = kBM;
-  P.acc1_offset = d.I;
   P.I = d.I;
   P.d = d.d;
   P.wait_ns = wait_limit_ns();
   P.fault = fault_site() == MOE_FP4_FAULT_TC_TOKEN_TILE;
+  if (pairs) {
+    // a pair covers 256 i-values (128 per CTA); gate rows i, up rows I + i
+    P.mblocks = (d.I + 2 * kBM - 1) / (2 * kBM);
+    P.block_rows = 2 * kBM;
+    P.cta_rows = kBM;
+    P.acc_idx_step = 0;
+    P.acc_row_off = d.I;
+    P.limit = d.I;
+    return launch_tc2<true>(b, raw, P, ws.max_tc_tiles, st);
+  }
+  P.mblocks = d.I / kBM;
+  P.block_rows = kBM;
+  P.acc1_offset = d.I;
   return launch_tc<true>(b, raw, P, ws.max_tc_tiles, st);
 }
 
+bool tc_fused_combine(bool pairs) { return pairs && kFusedCombine; }
+
 cudaError_t launch_tc_w2(const moe_fp4_dims& d, const uint8_t* w2, const uint8_t* w2s, const Workspace& ws,
-                         cudaStream_t st) {
+                         float* out, bool pairs, cudaStream_t st) {
   const size_t S = (size_t)d.T * d.k;
   CUtensorMap b, raw;
   if (!make_map_2d(&raw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w2, d.I / 2, (uint64_t)d.E * d.d, d.I / 2, kRawRowBytes, kBM,
                    CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_map_2d(&b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws.h16, d.I, S, (uint64_t)d.I * 2, kBK, kBBoxRows,
-                   CU_TENSOR_MAP_SWIZZLE_128B))
+      !make_map_2d(&b, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, ws.h16, d.I, S, (uint64_t)d.I * 2, kBK,
+                   pairs ? kPairBoxRows : kBBoxRows, CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   TcParams P{};
   P.w = w2;
@@ -578,13 +598,31 @@ cudaError_t launch_tc_w2(const moe_fp4_dims& d, const uint8_t* w2, const uint8_t
   P.x_scale = ws.h_scale;
   P.K = d.I;
   P.rows_per_expert = d.d;
-  P.mblocks = (d.d + 2 * kBM - 1) / (2 * kBM);  // d % 256 == 128 leaves a 128-row last block
-  P.block_rows = 2 * kBM;
-  P.acc1_offset = kBM;
   P.I = d.I;
   P.d = d.d;
   P.wait_ns = wait_limit_ns();
   P.fault = 0;
+  if (pairs) {
+    // a pair covers 512 output features (256 per CTA, two 128-row accumulators)
+    P.mblocks = (d.d + 4 * kBM - 1) / (4 * kBM);
+    P.block_rows = 4 * kBM;
+    P.cta_rows = 2 * kBM;
+    P.acc_idx_step = kBM;
+    P.acc_row_off = 0;
+    P.limit = d.d;
+    if (kFusedCombine) {
+      P.out = out;
+      P.topk_w = ws.topk_w;
+      P.sorted_slot = ws.sorted_slot;
+      P.slot_pos = ws.slot_pos;
+      P.combine_cnt = ws.combine_cnt;
+      P.k = d.k;
+    }
+    return launch_tc2<false>(b, raw, P, ws.max_tc_tiles, st);
+  }
+  P.mblocks = (d.d + 2 * kBM - 1) / (2 * kBM);  // d % 256 == 128 leaves a 128-row last block
+  P.block_rows = 2 * kBM;
+  P.acc1_offset = kBM;
   return launch_tc<false>(b, raw, P, ws.max_tc_tiles, st);
 }
 

@@ -44,6 +44,8 @@ struct Workspace {
                           //        shares x_perm's region, which is dead once W13 has run
   float* h_scale;         // [S]    the inverse of that power of two (shares x_scale's region)
   float* y;               // [S, d] fp32 expert outputs in sorted-row order
+  int32_t* combine_cnt;   // [T, ceil(d/256)] per (token, 256-feature block): slots whose y is written
+                          //        (tensor-core path; zeroed by the token gather of each call)
   // staging for the host-buffer entry point (only laid out when requested)
   uint16_t* stage_x;      // [T, d]
   float* stage_logits;    // [T, E]
@@ -88,10 +90,13 @@ cudaError_t launch_stream_w2(const moe_fp4_dims& d, const uint8_t* w2, const uin
 cudaError_t launch_stream_fused(const moe_fp4_dims& d, const uint16_t* x, const uint8_t* w13, const uint8_t* w13s,
                                 const uint8_t* w2, const uint8_t* w2s, const Workspace& ws, cudaStream_t st);
 cudaError_t launch_tc_w13(const moe_fp4_dims& d, const uint8_t* w13, const uint8_t* w13s, const Workspace& ws,
-                          cudaStream_t st);
+                          bool pairs, cudaStream_t st);
 cudaError_t launch_tc_w2(const moe_fp4_dims& d, const uint8_t* w2, const uint8_t* w2s, const Workspace& ws,
-                         cudaStream_t st);
+                         float* out, bool pairs, cudaStream_t st);
 cudaError_t launch_combine(const moe_fp4_dims& d, float* out, const Workspace& ws, cudaStream_t st);
+// true: the tensor-core W2 kernel writes out itself (the weighted combine in
+// its epilogue; the CTA-pair kernel does)
+bool tc_fused_combine(bool pairs);
 cudaError_t launch_router(const moe_fp4_dims& d, const uint16_t* x, const uint16_t* wg, float* logits,
                           cudaStream_t st);
 

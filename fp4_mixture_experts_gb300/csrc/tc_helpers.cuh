@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "ptx_sm103.cuh"
@@ -34,6 +35,15 @@ struct TcParams {
   // expert * rows_per_expert + a * acc_row_off + index; indices at or beyond
   // limit are not written
   int cta_rows, acc_idx_step, acc_row_off, limit;
+  // CTA pairs, W2 with the combine in the epilogue (out != nullptr): out[t] =
+  // sum_j topk_w[t, j] * y[slot_pos[t k + j]] for each 256-feature block,
+  // written by the CTA whose item brings the block's last slot (counters)
+  float* out;
+  const float* topk_w;
+  const int32_t* sorted_slot;
+  const int32_t* slot_pos;
+  int32_t* combine_cnt;
+  int k;
 };
 
 // UMMA shared-memory descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
@@ -135,4 +145,10 @@ __device__ __forceinline__ uint32_t f16x2_pow2(int e) {
 
 
 }  // namespace tc
+
+// the pair kernel's launcher (expert_tc2.cu)
+template <bool W13>
+cudaError_t launch_tc2(const CUtensorMap& b, const CUtensorMap& raw, const tc::TcParams& P, int max_tiles,
+                       cudaStream_t st);
+
 }  // namespace moe_fp4

@@ -102,6 +102,16 @@ typedef enum moe_fp4_status {
  * projections and the W2 stage is empty.  May be combined with
  * MOE_FP4_FLAG_FORCE_GEMV; ignored on the tensor-core path. */
 #define MOE_FP4_FLAG_PERSISTENT 0x4u
+/* On the tensor-core path: run both projections on pairs of SMs (tcgen05
+ * cta_group::2: one MMA instruction covers M = 256 weight rows, 128 from each
+ * CTA's tensor memory, with the token tile split between the two CTAs), and
+ * the weighted combine inside the W2 kernel (per-token counters; the CTA
+ * that completes a token's k slots sums them in slot order, deterministic).
+ * The same results within the layer's tolerance; slower than the default
+ * one-SM kernels on GB300 (the dequantisers' tensor-memory stores wait while
+ * the pair's MMAs read both SMs' tensor memory).  Ignored on the streaming
+ * path. */
+#define MOE_FP4_FLAG_CTA_PAIRS 0x8u
 
 /* Bytes of device workspace a call with these sizes needs (256-byte aligned
  * base required).  Returns 0 when the sizes are invalid or unsupported:
@@ -199,7 +209,7 @@ int moe_fp4_forward_host(const moe_fp4_dims* dims, const void* x_bf16_host,
  * library, which every GPU that loads the library holds until the process
  * exits.  Problems whose moe_fp4_workspace_bytes exceeds it are rejected with
  * MOE_FP4_ERR_WORKSPACE before anything is enqueued.  With E = 256 and k = 8
- * that allows T <= 73 tokens at d = 4096, I = 2048 (the T = 32 decode batch
+ * that allows T <= 72 tokens at d = 4096, I = 2048 (the T = 32 decode batch
  * needs about 7.4 MB) and T <= 44 at d = 7168, I = 2048; prefill-sized
  * batches need a workspace (moe_fp4_forward).
  * The array's device address is looked up (with the call's device current)

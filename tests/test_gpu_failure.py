@@ -32,7 +32,7 @@ def moe():
     return m
 
 
-@pytest.mark.parametrize("site,flags", [(1, TC), (2, GEMV), (2, GEMV | 0x4)])
+@pytest.mark.parametrize("site,flags", [(1, TC), (1, TC | 0x8), (2, GEMV), (2, GEMV | 0x4)])
 def test_timed_out_wait_is_reported_and_the_next_call_is_correct(moe, site, flags):
     L = make_layer(T=48, d=1024, I=1024, E=8, k=2, seed=61)
     D = to_device(L)

@@ -20,6 +20,7 @@ pytestmark = pytest.mark.gpu
 GEMV = 0x1
 TC = 0x2
 PERSIST = 0x4
+PAIRS = TC | 0x8
 
 
 @pytest.fixture(scope="module")
@@ -76,14 +77,14 @@ def test_tiny_config(moe):
     full_check(moe, make_config("tiny"))
 
 
-@pytest.mark.parametrize("flags", [GEMV, TC, GEMV | PERSIST])
+@pytest.mark.parametrize("flags", [GEMV, TC, GEMV | PERSIST, PAIRS])
 def test_several_tiles_ragged(moe, flags):
     # 300 tokens x 4 slots over 16 experts: ~75 rows per expert, ragged chunk and tile tails
     L = make_layer(T=300, d=1024, I=1024, E=16, k=4, seed=3)
     full_check(moe, L, flags)
 
 
-@pytest.mark.parametrize("flags", [0, TC])
+@pytest.mark.parametrize("flags", [0, TC, PAIRS])
 def test_non_1024_multiples(moe, flags):
     L = make_layer(T=37, d=384, I=640, E=12, k=3, seed=4)
     full_check(moe, L, flags)
@@ -121,7 +122,7 @@ def test_k_equals_E(moe):
     full_check(moe, make_layer(T=9, d=256, I=256, E=5, k=5, seed=10), TC)
 
 
-@pytest.mark.parametrize("flags", [GEMV, TC])
+@pytest.mark.parametrize("flags", [GEMV, TC, PAIRS])
 def test_w2_layout_probe(moe, flags):
     """A single nonzero W2 code must land on its own output column only."""
     L = make_layer(T=24, d=1024, I=1024, E=4, k=2, seed=11)
@@ -135,7 +136,7 @@ def test_w2_layout_probe(moe, flags):
     assert_out_close(out, ref["out"], "w2 probe")
 
 
-@pytest.mark.parametrize("flags", [GEMV, TC])
+@pytest.mark.parametrize("flags", [GEMV, TC, PAIRS])
 def test_w13_nibble_and_gate_up_probe(moe, flags):
     L = make_layer(T=12, d=1024, I=1024, E=2, k=1, seed=12)
     L.w13[:] = 0
@@ -159,7 +160,7 @@ def test_zero_codes_give_zero(moe):
 
 def test_run_twice_bit_identical(moe):
     L = make_layer(T=200, d=1024, I=1024, E=16, k=4, seed=14)
-    for flags in (GEMV, TC):
+    for flags in (GEMV, TC, PAIRS):
         a = run_gpu(moe, L, flags)["out"].cpu().numpy()
         b = run_gpu(moe, L, flags)["out"].cpu().numpy()
         assert np.array_equal(a, b)
@@ -241,13 +242,13 @@ def test_persistent_decode_is_bit_identical_to_two_launches(moe, shape):
     assert torch.equal(a["h"], b["h"]) and torch.equal(a["out"], b["out"])
 
 
-@pytest.mark.parametrize("name", ["prefill", "skewed"])
-def test_full_size_every_token(moe, name):
+@pytest.mark.parametrize("name,flags", [("prefill", 0), ("skewed", 0), ("skewed", PAIRS)])
+def test_full_size_every_token(moe, name, flags):
     """the prefill and skewed workloads, whole: routing bit-exact, every h
     element and every out element against the oracle (the default path, the
     tensor-core kernels, with the launch configuration the benchmark times)"""
     L = make_config(name)
-    r = run_gpu(moe, L)
+    r = run_gpu(moe, L, flags)
     ref = oracle.forward(L.x_bf16, L.router_logits, L.w13, L.w13_scale, L.w2, L.w2_scale, L.k)
     check_routing(r, ref)
     n_diff = check_h(r, ref, L)
@@ -303,13 +304,21 @@ def test_d7168_streaming_path(moe):
     full_check(moe, make_layer(T=12, d=7168, I=2048, E=12, k=2, exp_lo=-8, exp_hi=-6, seed=31), GEMV)
 
 
+@pytest.mark.parametrize("d,I", [(8192, 1024), (1024, 9216)])
+def test_streaming_path_beyond_7168(moe, d, I):
+    """d or I above 7168 on the streaming path: the activations of 8 tokens no
+    longer fit next to the weight ring, so the CUDA-core row kernels
+    (w13_swiglu_rows, w2_rows) run instead; they must match the oracle too"""
+    full_check(moe, make_layer(T=8, d=d, I=I, E=8, k=2, seed=d + I), GEMV)
+
+
 def test_routing_block_boundary(moe):
     """T = 32 runs the one-cluster routing kernel, T = 33 the three-kernel one"""
     for T in (32, 33):
         full_check(moe, make_layer(T=T, d=1024, I=1024, E=64, k=8, seed=32 + T))
 
 
-@pytest.mark.parametrize("flags", [GEMV, TC])
+@pytest.mark.parametrize("flags", [GEMV, TC, PAIRS])
 def test_wide_dynamic_range(moe, flags):
     # E8M0 exponents spread over 24 binades inside every weight row, token rows
     # scaled by powers of two from 2^-16 to 2^16 and one all-zero token: every
@@ -339,7 +348,7 @@ def test_wide_dynamic_range(moe, flags):
         assert rel <= 5e-3, f"token {t} (x scaled by 2^{shift[t]}): relative L2 {rel}"
 
 
-@pytest.mark.parametrize("flags", [GEMV, TC, GEMV | PERSIST])
+@pytest.mark.parametrize("flags", [GEMV, TC, GEMV | PERSIST, PAIRS])
 def test_cuda_graph_capture_replays_bit_identical(moe, flags):
     # the layer call allocates nothing and never waits on the host, so it can
     # be captured in a CUDA graph; replays recompute everything from the inputs

@@ -93,7 +93,7 @@ def test_noalloc_rejects_problems_beyond_its_scratch(moe):
     lib = moe.load_library()
     dims = moe.Dims(4096, 4096, 2048, 256, 8)
     assert moe.workspace_bytes(4096, 4096, 2048, 256, 8) > SCRATCH
-    assert _largest_T(moe, 4096, 2048, 256, 8) == 73
+    assert _largest_T(moe, 4096, 2048, 256, 8) == 72
     assert _largest_T(moe, 7168, 2048, 256, 8) == 44
     fake = ctypes.c_void_p(0x100000)  # never dereferenced: the size check comes first
     rc = lib.moe_fp4_forward_noalloc(ctypes.byref(dims), fake, fake, fake, fake, fake, fake, fake, 0, None)
