@@ -34,6 +34,8 @@ EXPORTED_SYMBOLS = (
     "moe_fp4_noalloc_check",
     "moe_fp4_set_fault_injection",
     "moe_fp4_mxfp8_quantize",
+    "moe_fp4_mx_workspace_bytes",
+    "moe_fp4_forward_mx",
     "moe_fp4_check",
     "moe_fp4_status_string",
 )
@@ -94,6 +96,10 @@ def load_library():
     lib.moe_fp4_set_fault_injection.restype = ctypes.c_int
     lib.moe_fp4_mxfp8_quantize.argtypes = [P, ctypes.c_int64, ctypes.c_int32, P, P, P]
     lib.moe_fp4_mxfp8_quantize.restype = ctypes.c_int
+    lib.moe_fp4_mx_workspace_bytes.argtypes = [pd]
+    lib.moe_fp4_mx_workspace_bytes.restype = ctypes.c_size_t
+    lib.moe_fp4_forward_mx.argtypes = [pd, P, P, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
+    lib.moe_fp4_forward_mx.restype = ctypes.c_int
     lib.moe_fp4_check.argtypes = [P, P]
     lib.moe_fp4_check.restype = ctypes.c_int
     lib.moe_fp4_status_string.argtypes = [ctypes.c_int]
@@ -228,6 +234,50 @@ def forward(x_bf16, router_logits, w13, w13_scale, w2, w2_scale, k: int, out=Non
     if extras:
         extras["out"] = out
         return extras
+    return out
+
+
+def mx_workspace_bytes(T, d, I, E, k) -> int:
+    return int(load_library().moe_fp4_mx_workspace_bytes(ctypes.byref(_dims(T, d, I, E, k))))
+
+
+def forward_mx(x_bf16, router_logits, w13, w13_scale, w2, w2_scale, k: int, out=None, workspace=None,
+               return_operands: bool = False, stream=None):
+    """The layer with MXFP8 activations on block-scaled tensor cores
+    (moe_fp4_forward_mx).  Arguments as in forward; w13 and w2 32-byte aligned.
+    Returns out fp32 [T, d], or with return_operands a dict with out and, in
+    sorted-row order, h (bf16 [S, I]), h_codes / h_scales (MXFP8 of h) and
+    x_codes / x_scales (MXFP8 of each row's token)."""
+    import torch
+    T, d = x_bf16.shape
+    E, twoI, _ = w13.shape
+    I = twoI // 2
+    dims = _dims(T, d, I, E, k)
+    lib = load_library()
+    nbytes = lib.moe_fp4_mx_workspace_bytes(ctypes.byref(dims))
+    if nbytes == 0:
+        raise MoeFp4Error(-2, "moe_fp4_forward_mx")
+    dev = x_bf16.device
+    ws = _workspace(nbytes, dev, workspace)
+    if out is None:
+        out = torch.empty(T, d, dtype=torch.float32, device=dev)
+    S = T * k
+    ex = {}
+    if return_operands:
+        ex = dict(h=torch.empty(S, I, dtype=torch.bfloat16, device=dev),
+                  h_codes=torch.empty(S, I, dtype=torch.uint8, device=dev),
+                  h_scales=torch.empty(S, I // 32, dtype=torch.uint8, device=dev),
+                  x_codes=torch.empty(S, d, dtype=torch.uint8, device=dev),
+                  x_scales=torch.empty(S, d // 32, dtype=torch.uint8, device=dev))
+    rc = lib.moe_fp4_forward_mx(ctypes.byref(dims), _ptr(x_bf16), _ptr(router_logits), _ptr(w13), _ptr(w13_scale),
+                                _ptr(w2), _ptr(w2_scale), _ptr(out), _ptr(ex.get("h")), _ptr(ex.get("h_codes")),
+                                _ptr(ex.get("h_scales")), _ptr(ex.get("x_codes")), _ptr(ex.get("x_scales")),
+                                _ptr(ws), ws.numel(), _stream(stream))
+    if rc != 0:
+        raise MoeFp4Error(rc, "moe_fp4_forward_mx")
+    if ex:
+        ex["out"] = out
+        return ex
     return out
 
 

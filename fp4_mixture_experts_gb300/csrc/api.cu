@@ -28,7 +28,7 @@ bool aligned(const void* p, size_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
 
 }  // namespace
 
-bool layout_workspace(const moe_fp4_dims& d, void* base, bool with_staging, Workspace* ws) {
+bool layout_workspace(const moe_fp4_dims& d, void* base, bool with_staging, Workspace* ws, bool mx) {
   if (!dims_supported(d)) return false;
   memset(ws, 0, sizeof(*ws));
   const size_t S = (size_t)d.T * d.k;
@@ -60,6 +60,14 @@ bool layout_workspace(const moe_fp4_dims& d, void* base, bool with_staging, Work
   ws->h = (uint16_t*)take(S * d.I * sizeof(uint16_t));
   ws->y = (float*)take(S * d.d * sizeof(float));
   ws->combine_cnt = (int32_t*)take((size_t)d.T * ((d.d + 255) / 256) * sizeof(int32_t));
+  if (mx) {
+    // S*(d + I) code bytes fit the x_perm region (2 S max(d, I) bytes); the
+    // offset S*d keeps hq 128-byte aligned (d is a multiple of 128)
+    ws->xq = reinterpret_cast<uint8_t*>(ws->x_perm);
+    ws->hq = base ? ws->xq + S * d.d : nullptr;
+    ws->xq_scales = (uint8_t*)take(S * (d.d / 32));
+    ws->hq_scales = (uint8_t*)take(S * (d.I / 32));
+  }
   if (with_staging) {
     ws->stage_x = (uint16_t*)take((size_t)d.T * d.d * sizeof(uint16_t));
     ws->stage_logits = (float*)take((size_t)d.T * d.E * sizeof(float));
@@ -278,6 +286,41 @@ int moe_fp4_forward_host(const moe_fp4_dims* dims, const void* x_bf16_host, cons
   if (rc != MOE_FP4_OK) return rc;
   if (cudaMemcpyAsync(out_host, ws.stage_out, ob, cudaMemcpyDeviceToHost, st) != cudaSuccess) return MOE_FP4_ERR_CUDA;
   return cudaStreamSynchronize(st) == cudaSuccess ? MOE_FP4_OK : MOE_FP4_ERR_CUDA;
+}
+
+size_t moe_fp4_mx_workspace_bytes(const moe_fp4_dims* dims) {
+  if (!dims) return 0;
+  Workspace ws;
+  return layout_workspace(*dims, nullptr, false, &ws, true) ? ws.total : 0;
+}
+
+int moe_fp4_forward_mx(const moe_fp4_dims* dims, const void* x_bf16, const float* router_logits,
+                       const uint8_t* w13, const uint8_t* w13_scale, const uint8_t* w2, const uint8_t* w2_scale,
+                       float* out, void* h_bf16, uint8_t* h_codes, uint8_t* h_scales, uint8_t* x_codes,
+                       uint8_t* x_scales, void* workspace, size_t workspace_bytes, void* cuda_stream) {
+  if (!dims || !x_bf16 || !router_logits || !w13 || !w13_scale || !w2 || !w2_scale || !out || !workspace)
+    return MOE_FP4_ERR_INVALID_ARG;
+  const moe_fp4_dims d = *dims;
+  Workspace ws;
+  if (!layout_workspace(d, workspace, false, &ws, true)) return MOE_FP4_ERR_UNSUPPORTED;
+  // the weights are read by the tensor memory accelerator as 4-bit elements:
+  // 32-byte aligned bases
+  if (!aligned(workspace, 256) || !aligned(x_bf16, 16) || !aligned(w13, 32) || !aligned(w2, 32) ||
+      !aligned(out, 16) || !aligned(router_logits, 4) || !aligned(w13_scale, 16) || !aligned(w2_scale, 16) ||
+      (h_bf16 && !aligned(h_bf16, 16)) || (h_codes && !aligned(h_codes, 16)) || (x_codes && !aligned(x_codes, 16)))
+    return MOE_FP4_ERR_INVALID_ARG;
+  if (workspace_bytes < ws.total) return MOE_FP4_ERR_WORKSPACE;
+  if (h_bf16) ws.h = static_cast<uint16_t*>(h_bf16);
+  if (h_codes) ws.hq = h_codes;
+  if (h_scales) ws.hq_scales = h_scales;
+  if (x_codes) ws.xq = x_codes;
+  if (x_scales) ws.xq_scales = x_scales;
+  cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  cudaError_t e = launch_route(d, router_logits, ws, st);
+  if (e == cudaSuccess)
+    e = launch_mx_forward(d, static_cast<const uint16_t*>(x_bf16), w13, w13_scale, w2, w2_scale, ws, st);
+  if (e == cudaSuccess) e = launch_combine(d, out, ws, st);
+  return e == cudaSuccess ? MOE_FP4_OK : MOE_FP4_ERR_CUDA;
 }
 
 int moe_fp4_check(void* workspace, void* cuda_stream) {

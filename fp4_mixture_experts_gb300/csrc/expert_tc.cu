@@ -212,13 +212,12 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
         const TcItem t = tc_item(P, it);
         for (int rs = 0; rs < nrs; ++rs, ++g) {
           const int s = g % kStagesRaw;
-          if (!mbar_wait(&raw_empty[s], ((g / kStagesRaw) & 1) ^ 1u, abort_flag, P.err, kErrWaitTimeout, lim) ||
-              *abort_flag) {
+          if (!mbar_wait(&raw_empty[s], ((g / kStagesRaw) & 1) ^ 1u, abort_flag, P.err, kErrWaitTimeout, lim)) {
             ok = false;
             break;
           }
-          // (a slot comes back only once every dequantiser read its bytes, or
-          // saw the abort that the check above catches: one copy per slot)
+          // (a slot comes back only once every dequantiser read its bytes:
+          // one copy per slot in flight)
           mbar_expect_tx(&raw_full[s], 2 * kRawTileBytes);
           uint8_t* raw = smem + kOffRaw + s * 2 * kRawTileBytes;
           tma_load_2d_hint(raw, &map_raw, rs * kRawRowBytes, t.wrow0, &raw_full[s], pol);
@@ -233,39 +232,24 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
     // ---------------- TMA producer: token tiles ----------------
     // A slot comes back (empty) only after the MMAs ran on its previous use,
     // whose copy had landed: at most one copy per slot is ever in flight.
-    int slot_g[kStages];       // per slot: the stage (counted over all items) of its last copy, or -1
-    uint32_t slot_par = 0;     // bit s: phase parity of that copy
-    uint32_t slot_real = 0;    // bit s: the copy was issued (not withheld)
-#pragma unroll
-    for (int s = 0; s < kStages; ++s) slot_g[s] = -1;
+    uint32_t ph = 0;   // bit s: parity of slot s's next use
+    int g = 0;         // stages passed (issued, or withheld by the fault injection)
+    const bool fault_cta = P.fault != 0 && blockIdx.x == 0;
     if (lane == 0) {
-      uint32_t ph = 0;
-      int g = 0;
-      bool withhold = P.fault != 0 && blockIdx.x == 0;
       bool ok = true;
       for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
         const TcItem t = tc_item(P, it);
         const int boxes = (t.n_mma + kBBoxRows - 1) / kBBoxRows;
         for (int ks = 0; ks < nk; ++ks, ++g) {
           const int s = ks % t.nS;
-          const uint32_t par = (ph >> s) & 1;
-          if (!mbar_wait(&empty[s], par ^ 1u, abort_flag, P.err, kErrWaitTimeout, lim) || *abort_flag) {
+          if (!mbar_wait(&empty[s], ((ph >> s) & 1) ^ 1u, abort_flag, P.err, kErrWaitTimeout, lim)) {
             ok = false;
             break;
           }
           ph ^= 1u << s;
-#pragma unroll
-          for (int q = 0; q < kStages; ++q)  // unrolled: the records stay in registers
-            if (q == s) slot_g[q] = g;
-          slot_par = (slot_par & ~(1u << s)) | (par << s);
-          if (withhold) {
-            // fault injection: this tile never arrives, so the MMA issuers'
-            // wait on the stage runs out and the kernel takes its abort path
-            withhold = false;
-            slot_real &= ~(1u << s);
-            continue;
-          }
-          slot_real |= 1u << s;
+          // fault injection: the first tile of the first CTA never arrives,
+          // so the MMA issuers' wait on the stage runs out
+          if (fault_cta && g == 0) continue;
           mbar_expect_tx(&full[s], boxes * kBBoxBytes);
           uint8_t* b = smem + kOffB + s * kBTileBytes;
           for (int i = 0; i < boxes; ++i)
@@ -279,15 +263,29 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
     __syncwarp();
     asm volatile("bar.sync 3, %0;" ::"r"((kDqWarps + 1) * 32) : "memory");
     if (lane == 0 && *abort_flag) {
+      // the last stage of each slot: replay the slot sequence up to g
+      int last[kStages];
+#pragma unroll
+      for (int q = 0; q < kStages; ++q) last[q] = -1;
+      int g2 = 0;
+      for (int it = blockIdx.x; it < items && g2 < g; it += gridDim.x) {
+        const TcItem t = tc_item(P, it);
+        for (int ks = 0; ks < nk && g2 < g; ++ks, ++g2) {
+          const int s2 = ks % t.nS;
+#pragma unroll
+          for (int q = 0; q < kStages; ++q)
+            if (q == s2) last[q] = g2;
+        }
+      }
 #pragma unroll
       for (int s = 0; s < kStages; ++s) {
-        if (slot_g[s] < 0 || !((slot_real >> s) & 1)) continue;
+        if (last[s] < 0 || (fault_cta && last[s] == 0)) continue;  // no copy (or a withheld one)
         int arrived = 0;
-        for (int w = 0; w < kDqWarps; ++w) arrived += dq_arrived[w] > slot_g[s] ? 1 : 0;
+        for (int w = 0; w < kDqWarps; ++w) arrived += dq_arrived[w] > last[s] ? 1 : 0;
         if (arrived < kDqWarps)
           asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(&full[s])),
                        "r"(kDqWarps - arrived) : "memory");
-        mbar_wait_drain(&full[s], (slot_par >> s) & 1, P.err, kErrWaitTimeout, lim);
+        mbar_wait_drain(&full[s], ((ph >> s) & 1) ^ 1u, P.err, kErrWaitTimeout, lim);
       }
     }
   } else if (warp == kMmaWarp || warp == kMma1Warp) {

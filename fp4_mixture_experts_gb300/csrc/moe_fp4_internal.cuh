@@ -46,6 +46,11 @@ struct Workspace {
   float* y;               // [S, d] fp32 expert outputs in sorted-row order
   int32_t* combine_cnt;   // [T, ceil(d/256)] per (token, 256-feature block): slots whose y is written
                           //        (tensor-core path; zeroed by the token gather of each call)
+  // block-scaled (MX) layer only: MXFP8 operands in sorted-row order
+  uint8_t* xq;            // [S, d] E4M3 codes of x   (in x_perm's region)
+  uint8_t* hq;            // [S, I] E4M3 codes of h   (in x_perm's region, after xq)
+  uint8_t* xq_scales;     // [S, d/32] E8M0
+  uint8_t* hq_scales;     // [S, I/32] E8M0
   // staging for the host-buffer entry point (only laid out when requested)
   uint16_t* stage_x;      // [T, d]
   float* stage_logits;    // [T, E]
@@ -57,8 +62,9 @@ struct Workspace {
 };
 
 // Lays the workspace out from `base` (nullptr: sizes only).  Returns false for
-// unsupported sizes.
-bool layout_workspace(const moe_fp4_dims& d, void* base, bool with_staging, Workspace* ws);
+// unsupported sizes.  with_staging: host-buffer staging regions; mx: the
+// MXFP8 operand regions of the block-scaled layer.
+bool layout_workspace(const moe_fp4_dims& d, void* base, bool with_staging, Workspace* ws, bool mx = false);
 
 // TMA tensor map of a 2-D row-major array (inner = contiguous dimension, in
 // elements); false if the driver rejects it.
@@ -99,6 +105,10 @@ cudaError_t launch_combine(const moe_fp4_dims& d, float* out, const Workspace& w
 bool tc_fused_combine(bool pairs);
 cudaError_t launch_router(const moe_fp4_dims& d, const uint16_t* x, const uint16_t* wg, float* logits,
                           cudaStream_t st);
+// block-scaled layer after routing: quantising gather, W13 (+ SwiGLU, h and
+// its MXFP8 form) and W2 on kind::mxf8f6f4 tensor cores; y in ws.y
+cudaError_t launch_mx_forward(const moe_fp4_dims& d, const uint16_t* x, const uint8_t* w13, const uint8_t* w13s,
+                              const uint8_t* w2, const uint8_t* w2s, const Workspace& ws, cudaStream_t st);
 
 // ---------------------------------------------------------------------------
 // device helpers

@@ -15,21 +15,10 @@
 #include <cuda_fp8.h>
 
 #include "moe_fp4_internal.cuh"
+#include "mx_common.cuh"
 
 namespace moe_fp4 {
 namespace {
-
-// floor(log2(v)) of a nonzero bf16 magnitude given by its 15 low bits.
-__device__ __forceinline__ int bf16_floor_log2(uint32_t mag) {
-  const int e = (int)(mag >> 7);
-  if (e > 0) return e - 127;
-  return -133 + (31 - __clz(mag));  // subnormal: mag * 2^-133, mag in [1, 127]
-}
-
-__device__ __forceinline__ uint32_t e4m3_code(uint32_t bf16_bits, float inv_scale) {
-  const float v = __uint_as_float(bf16_bits << 16) * inv_scale;
-  return (uint32_t)__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3);
-}
 
 __global__ void __launch_bounds__(256)
 mxfp8_quantize_kernel(const uint4* __restrict__ x, long long n_blocks, uint4* __restrict__ codes,
@@ -48,27 +37,24 @@ mxfp8_quantize_kernel(const uint4* __restrict__ x, long long n_blocks, uint4* __
     uint32_t amax = 0;
 #pragma unroll
     for (int i = 0; i < 16; ++i) amax = max(amax, max(w[i] & 0x7FFFu, (w[i] >> 16) & 0x7FFFu));
-    if (amax >= 0x7F80u) {  // an infinity or a NaN in the block (bf16 exponent field all ones)
+    const uint32_t sb = mx_scale_byte(amax);
+    if (sb == 0xFFu) {  // an infinity or a NaN in the block (bf16 exponent field all ones)
       const uint4 nan4 = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
       codes[2 * b] = nan4;
       codes[2 * b + 1] = nan4;
       scales[b] = 0xFF;
       continue;
     }
-    // finite block: scale exponent in [-127, 119]; 2^-s is then a normal fp32
-    // (exponent field 127 - s in [8, 254])
-    const int s = amax == 0 ? -127 : max(bf16_floor_log2(amax) - 8, -127);
-    const float inv = __uint_as_float((uint32_t)(127 - s) << 23);
     uint32_t out[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const uint32_t a = w[2 * i], c = w[2 * i + 1];
-      out[i] = e4m3_code(a & 0xFFFFu, inv) | (e4m3_code(a >> 16, inv) << 8) | (e4m3_code(c & 0xFFFFu, inv) << 16) |
-               (e4m3_code(c >> 16, inv) << 24);
+      out[i] = mx_e4m3_code(a & 0xFFFFu, sb) | (mx_e4m3_code(a >> 16, sb) << 8) |
+               (mx_e4m3_code(c & 0xFFFFu, sb) << 16) | (mx_e4m3_code(c >> 16, sb) << 24);
     }
     codes[2 * b] = make_uint4(out[0], out[1], out[2], out[3]);
     codes[2 * b + 1] = make_uint4(out[4], out[5], out[6], out[7]);
-    scales[b] = (uint8_t)(s + 127);
+    scales[b] = (uint8_t)sb;
   }
 }
 

@@ -258,6 +258,42 @@ int moe_fp4_noalloc_check(void* cuda_stream);
 int moe_fp4_mxfp8_quantize(const void* x_bf16, int64_t rows, int32_t K, uint8_t* codes, uint8_t* scales,
                            void* cuda_stream);
 
+/* Workspace bytes of moe_fp4_forward_mx (256-byte aligned base); 0 for the
+ * sizes moe_fp4_workspace_bytes rejects. */
+size_t moe_fp4_mx_workspace_bytes(const moe_fp4_dims* dims);
+
+/* The layer with MXFP8 activations into both projections, on block-scaled
+ * tensor cores (tcgen05.mma kind::mxf8f6f4: the E2M1 weights and their E8M0
+ * scales as stored, E4M3 activations with one E8M0 scale per 32 elements,
+ * fp32 accumulation).  Steps as in moe_fp4_forward, with two quantisations
+ * added (the MXFP8 conversion of moe_fp4_mxfp8_quantize):
+ *   x_q = MXFP8(x) per token row (blocks of 32 along d) before W13;
+ *   h   = bf16(silu(g) * u) as in moe_fp4_forward, then
+ *   h_q = MXFP8(h) per slot row (blocks of 32 along I) before W2;
+ *   y   = h_q . W2_e^T; out = sum_j w_j y_j.
+ * The paper quantises its decode activations (abstract: INT8 activation
+ * quantisation) and the MI250 blog names block-wise FP8 as the next gain;
+ * this is that layer in the weights' own MX block format, not the exact
+ * layer: out differs from moe_fp4_forward by the activation rounding.
+ * Routing and the sort are those of moe_fp4_route, bit for bit.
+ * Arguments as in moe_fp4_forward, except: w13 and w2 must be 32-byte
+ * aligned; there are no flags; the optional outputs (NULL: kept in the
+ * workspace only) are, in sorted-row order (S = T*k, row r = the r-th row of
+ * the expert sort):
+ *   h_bf16    bf16  [S, I]     16-byte aligned
+ *   h_codes   uint8 [S, I]     E4M3 codes of h_q, 16-byte aligned
+ *   h_scales  uint8 [S, I/32]  E8M0 scales of h_q
+ *   x_codes   uint8 [S, d]     E4M3 codes of x_q of the row's token, 16-byte aligned
+ *   x_scales  uint8 [S, d/32]  E8M0 scales of x_q
+ * Enqueues the routing kernel, the quantising gather, the two block-scaled
+ * projections and the combine; never synchronises.  A block of x or h that
+ * holds an infinity or a NaN gets the NaN scale 0xFF and NaN codes, and the
+ * rows it feeds come out NaN. */
+int moe_fp4_forward_mx(const moe_fp4_dims* dims, const void* x_bf16, const float* router_logits,
+                       const uint8_t* w13, const uint8_t* w13_scale, const uint8_t* w2, const uint8_t* w2_scale,
+                       float* out, void* h_bf16, uint8_t* h_codes, uint8_t* h_scales, uint8_t* x_codes,
+                       uint8_t* x_scales, void* workspace, size_t workspace_bytes, void* cuda_stream);
+
 /* Fault injection, for tests of the failure path only (the layer's own
  * failure handling: every pipeline wait in the kernels is bounded, and a wait
  * that runs out sets bit 2 of the device error word, releases the kernel's

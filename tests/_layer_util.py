@@ -162,3 +162,77 @@ def assert_out_within(got, want, L, toks=None, what=""):
                       f"excess {excess[~ok][:4]}, slack {slack[~ok][:4]}")
     m["tokens_beyond_max_abs"] = int(bad.size)
     return m, float(excess.max())
+
+
+def mx_hq_bound(lo, hi, hq):
+    """Per element, the largest distance between the oracle's MXFP8 h_q (fp64
+    values [R, I]) and the MXFP8 form of any h' with lo <= h' <= hi (the bf16
+    values the error model allows for h, h_interval).
+
+    A block whose 32 intervals are single points has one MXFP8 form: 0.  Else
+    the block's scale exponent floor(log2 amax') - 8 ranges over the binades
+    of amax' in [amax_min, amax_max], and for each scale X the rounding
+    RN(h'/X) X is monotone in h', so its extremes are those of lo and hi; if
+    every interval holds 0 the block may also be all zero (any scale), and
+    |q(h')| <= 2 |h'| covers every scale."""
+    from oracle.mx_activations import E4M3_EMAX, e4m3_round
+    R, I = lo.shape
+    nb = I // 32
+    lo3, hi3, hq3 = (np.asarray(a, dtype=np.float64).reshape(R, nb, 32) for a in (lo, hi, hq))
+    out = np.zeros((R, nb, 32))
+    wide = np.any(lo3 != hi3, axis=2)
+    if not wide.any():
+        return out.reshape(R, I)
+    L, H, Q = lo3[wide], hi3[wide], hq3[wide]
+    mag_min = np.where((L <= 0) & (H >= 0), 0.0, np.minimum(np.abs(L), np.abs(H)))
+    mag_max = np.maximum(np.abs(L), np.abs(H))
+    amin, amax = mag_min.max(axis=1), mag_max.max(axis=1)
+    ex = lambda a: np.frexp(np.where(a > 0, a, 1.0))[1] - 1
+    e_hi = ex(amax)
+    e_lo = np.where(amin > 0, ex(amin), e_hi)
+    dev = np.zeros_like(L)
+    for o in range(int((e_hi - e_lo).max()) + 1):
+        e = np.minimum(e_lo + o, e_hi)
+        X = np.ldexp(1.0, np.clip(e - E4M3_EMAX, -127, 127))[:, None]
+        qlo = e4m3_round(L / X) * X
+        qhi = e4m3_round(H / X) * X
+        dev = np.maximum(dev, np.maximum(np.abs(qlo - Q), np.abs(qhi - Q)))
+    zero_ok = (amin == 0)[:, None]
+    dev = np.where(zero_ok, np.maximum(dev, np.abs(Q) + 2.0 * mag_max.max(axis=1, keepdims=True)), dev)
+    out[wide] = dev
+    return out.reshape(R, I)
+
+
+def assert_out_within_mx(got, want, L, toks=None, what=""):
+    """out of the MXFP8 layer against the oracle's (oracle.mx_activations):
+    relative L2 and cosine over the whole array; every element within MAX_ABS
+    plus the slack of legitimate h rounding decisions, which here reach the
+    W2 operand through its MXFP8 form: sum_j w_tj sum_i dq_i |W2_e[n, i]| with
+    dq = mx_hq_bound of h's interval (computed from the oracle's values
+    only).  Returns the metrics and the largest excess over MAX_ABS."""
+    from oracle import mx_activations as mxa
+    m = out_metrics(got, want)
+    assert m["rel_l2"] <= REL_L2 and m["cosine"] >= COSINE, f"{what}: {m}"
+    got = np.asarray(got, dtype=np.float64)
+    toks = np.arange(L.T) if toks is None else np.asarray(toks)
+    diff = np.abs(got - want)
+    bad = np.nonzero((diff > MAX_ABS).any(axis=1))[0]
+    if bad.size == 0:
+        return m, 0.0
+    xq = mxa.mx_round_trip(oracle.bf16_bits_to_f64(L.x_bf16[toks[bad]]))
+    ids, w = oracle.route(L.router_logits[toks[bad]], L.k)
+    slack = np.zeros((bad.size, L.d))
+    for e in np.unique(ids):
+        rows, slots = np.nonzero(ids == e)
+        W13 = oracle.dequantize_rows(L.w13[e], L.w13_scale[e])
+        lo, hi = h_interval_w(xq[rows], W13)
+        _, hq, _ = mxa.expert_ffn_mx(xq[rows], L.w13[e], L.w13_scale[e], L.w2[e], L.w2_scale[e])
+        dq = mx_hq_bound(lo, hi, hq)
+        W2 = np.abs(oracle.dequantize_rows(L.w2[e], L.w2_scale[e]))
+        slack[rows] += w[rows, slots][:, None] * (dq @ W2.T)
+    excess = diff[bad] - MAX_ABS
+    ok = excess <= slack * (1 + 1e-6)
+    assert ok.all(), (f"{what}: out beyond MAX_ABS + h-rounding slack at token {toks[bad][np.nonzero(~ok)[0][:4]]}: "
+                      f"excess {excess[~ok][:4]}, slack {slack[~ok][:4]}")
+    m["tokens_beyond_max_abs"] = int(bad.size)
+    return m, float(excess.max())
