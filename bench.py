@@ -520,12 +520,14 @@ def run_reference(args):
 
 
 PROFILE_CASES = {
-    # name: (workload, experts override, tokens override) -- smaller expert counts keep
-    # ncu captures to about a GB on the device while the weights stay larger than L2
-    "decode": ("decode", None, None),
-    "prefill": ("prefill", None, None),
-    "decode-e64": ("decode", 64, 32),
-    "prefill-e64": ("prefill", 64, 1152),
+    # name: (workload, experts override, tokens override, MXFP8 layer) -- smaller expert
+    # counts keep ncu captures to about a GB on the device while the weights stay larger than L2
+    "decode": ("decode", None, None, False),
+    "prefill": ("prefill", None, None, False),
+    "decode-e64": ("decode", 64, 32, False),
+    "prefill-e64": ("prefill", 64, 1152, False),
+    "prefill-mx": ("prefill", None, None, True),
+    "prefill-mx-e64": ("prefill", 64, 1152, True),
 }
 
 
@@ -536,7 +538,7 @@ def run_profile_case(args):
 
     import fp4_mixture_experts_gb300 as moe
     from moe_inputs import make_layer
-    name, E, T = PROFILE_CASES[args.profile_case]
+    name, E, T, mx = PROFILE_CASES[args.profile_case]
     c = dict(CONFIGS[name])
     if E is not None:
         c["E"], c["T"] = E, T
@@ -544,10 +546,11 @@ def run_profile_case(args):
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
     x = t(L.x_bf16.view(np.int16)).view(torch.bfloat16)
     args_ = (x, t(L.router_logits), t(L.w13), t(L.w13_scale), t(L.w2), t(L.w2_scale), L.k)
-    ws = torch.empty(moe.workspace_bytes(L.T, L.d, L.I, L.E, L.k), dtype=torch.uint8, device="cuda")
+    nbytes = (moe.mx_workspace_bytes if mx else moe.workspace_bytes)(L.T, L.d, L.I, L.E, L.k)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
     out = torch.empty(L.T, L.d, dtype=torch.float32, device="cuda")
     for _ in range(args.warmup + args.steps):
-        moe.forward(*args_, out=out, workspace=ws)
+        (moe.forward_mx if mx else moe.forward)(*args_, out=out, workspace=ws)
     torch.cuda.synchronize()
     moe.check(ws)
     print(f"profile case {args.profile_case}: T={L.T} d={L.d} I={L.I} E={L.E} k={L.k}, "

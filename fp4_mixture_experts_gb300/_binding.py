@@ -98,7 +98,8 @@ def load_library():
     lib.moe_fp4_mxfp8_quantize.restype = ctypes.c_int
     lib.moe_fp4_mx_workspace_bytes.argtypes = [pd]
     lib.moe_fp4_mx_workspace_bytes.restype = ctypes.c_size_t
-    lib.moe_fp4_forward_mx.argtypes = [pd, P, P, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
+    lib.moe_fp4_forward_mx.argtypes = [pd, P, P, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P,
+                                       ctypes.POINTER(ctypes.c_void_p)]
     lib.moe_fp4_forward_mx.restype = ctypes.c_int
     lib.moe_fp4_check.argtypes = [P, P]
     lib.moe_fp4_check.restype = ctypes.c_int
@@ -132,6 +133,15 @@ def _stream(stream):
     import torch
     s = stream if stream is not None else torch.cuda.current_stream()
     return ctypes.c_void_p(s.cuda_stream)
+
+
+def _events(stage_events):
+    """ctypes array of cudaEvent_t handles (torch.cuda.Event, each recorded once so that it exists), or None"""
+    if stage_events is None:
+        return None
+    if len(stage_events) != 6:
+        raise ValueError("stage_events takes 6 events")
+    return (ctypes.c_void_p * len(stage_events))(*[ctypes.c_void_p(ev.cuda_event) for ev in stage_events])
 
 
 def _workspace(nbytes, device, workspace):
@@ -224,9 +234,7 @@ def forward(x_bf16, router_logits, w13, w13_scale, w2, w2_scale, k: int, out=Non
             _ptr(extras.get("sorted_slot")), _ptr(extras.get("h")), int(flags), _ptr(ws),
             ws.numel(), _stream(stream)]
     if stage_events is not None:
-        # torch.cuda.Event handles; each must have been recorded once so that it exists
-        arr = (ctypes.c_void_p * len(stage_events))(*[ctypes.c_void_p(ev.cuda_event) for ev in stage_events])
-        rc = lib.moe_fp4_forward_profiled(*args, arr)
+        rc = lib.moe_fp4_forward_profiled(*args, _events(stage_events))
     else:
         rc = lib.moe_fp4_forward(*args)
     if rc != 0:
@@ -242,7 +250,7 @@ def mx_workspace_bytes(T, d, I, E, k) -> int:
 
 
 def forward_mx(x_bf16, router_logits, w13, w13_scale, w2, w2_scale, k: int, out=None, workspace=None,
-               return_operands: bool = False, stream=None):
+               return_operands: bool = False, stream=None, stage_events=None):
     """The layer with MXFP8 activations on block-scaled tensor cores
     (moe_fp4_forward_mx).  Arguments as in forward; w13 and w2 32-byte aligned.
     Returns out fp32 [T, d], or with return_operands a dict with out and, in
@@ -272,7 +280,7 @@ def forward_mx(x_bf16, router_logits, w13, w13_scale, w2, w2_scale, k: int, out=
     rc = lib.moe_fp4_forward_mx(ctypes.byref(dims), _ptr(x_bf16), _ptr(router_logits), _ptr(w13), _ptr(w13_scale),
                                 _ptr(w2), _ptr(w2_scale), _ptr(out), _ptr(ex.get("h")), _ptr(ex.get("h_codes")),
                                 _ptr(ex.get("h_scales")), _ptr(ex.get("x_codes")), _ptr(ex.get("x_scales")),
-                                _ptr(ws), ws.numel(), _stream(stream))
+                                _ptr(ws), ws.numel(), _stream(stream), _events(stage_events))
     if rc != 0:
         raise MoeFp4Error(rc, "moe_fp4_forward_mx")
     if ex:

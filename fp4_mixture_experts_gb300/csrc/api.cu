@@ -3,6 +3,8 @@
 // kernels of the other translation units.
 #include <string.h>
 
+#include <functional>
+
 #include "moe_fp4_internal.cuh"
 
 namespace moe_fp4 {
@@ -297,7 +299,8 @@ size_t moe_fp4_mx_workspace_bytes(const moe_fp4_dims* dims) {
 int moe_fp4_forward_mx(const moe_fp4_dims* dims, const void* x_bf16, const float* router_logits,
                        const uint8_t* w13, const uint8_t* w13_scale, const uint8_t* w2, const uint8_t* w2_scale,
                        float* out, void* h_bf16, uint8_t* h_codes, uint8_t* h_scales, uint8_t* x_codes,
-                       uint8_t* x_scales, void* workspace, size_t workspace_bytes, void* cuda_stream) {
+                       uint8_t* x_scales, void* workspace, size_t workspace_bytes, void* cuda_stream,
+                       void* const* stage_events) {
   if (!dims || !x_bf16 || !router_logits || !w13 || !w13_scale || !w2 || !w2_scale || !out || !workspace)
     return MOE_FP4_ERR_INVALID_ARG;
   const moe_fp4_dims d = *dims;
@@ -316,10 +319,18 @@ int moe_fp4_forward_mx(const moe_fp4_dims* dims, const void* x_bf16, const float
   if (x_codes) ws.xq = x_codes;
   if (x_scales) ws.xq_scales = x_scales;
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  auto mark = [&](int i) {
+    if (stage_events) cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), st);
+  };
+  mark(0);
   cudaError_t e = launch_route(d, router_logits, ws, st);
+  mark(1);
   if (e == cudaSuccess)
-    e = launch_mx_forward(d, static_cast<const uint16_t*>(x_bf16), w13, w13_scale, w2, w2_scale, ws, st);
+    e = launch_mx_forward(d, static_cast<const uint16_t*>(x_bf16), w13, w13_scale, w2, w2_scale, ws, st,
+                          stage_events ? mark : std::function<void(int)>());
+  mark(4);
   if (e == cudaSuccess) e = launch_combine(d, out, ws, st);
+  mark(5);
   return e == cudaSuccess ? MOE_FP4_OK : MOE_FP4_ERR_CUDA;
 }
 

@@ -47,7 +47,10 @@ using namespace tc;
 constexpr int kBM = 128;
 constexpr int kBKs = 128;                  // K elements per stage (4 MMAs of K = 32)
 constexpr int kBN = kTcTileN;              // <= 192 token rows per tile
-constexpr int kStages = 3;
+#ifndef MOE_MX_STAGES
+#define MOE_MX_STAGES 3
+#endif
+constexpr int kStages = MOE_MX_STAGES;
 constexpr int kWriters = 8;                // scale writers, then the epilogue
 constexpr int kMmaWarp = 0;
 constexpr int kFirstWriter = 1;
@@ -123,11 +126,15 @@ struct MxItem {
   uint32_t acc_cols;
 };
 
-__device__ __forceinline__ MxItem mx_item(const MxParams& P, int item) {
+// Every role reads the tile record of its next item one item ahead
+// (mx_tile), so that no role waits on that load at an item boundary.
+__device__ __forceinline__ int4 mx_tile(const MxParams& P, int item, int items) {
+  return item < items ? P.tiles[item / P.mblocks] : make_int4(0, 0, 0, 0);
+}
+
+__device__ __forceinline__ MxItem mx_item(const MxParams& P, int item, const int4 tl) {
   MxItem t;
-  const int tile = item / P.mblocks;
   t.mb = item % P.mblocks;
-  const int4 tl = P.tiles[tile];
   t.row0 = tl.y;
   t.n = tl.z;
   t.n_mma = (t.n + 15) & ~15;
@@ -135,6 +142,31 @@ __device__ __forceinline__ MxItem mx_item(const MxParams& P, int item) {
   t.nsfb = (t.n_mma + 31) / 32;
   t.wrow0 = tl.x * P.rows_per_expert + t.mb * P.block_rows;
   return t;
+}
+
+// One lane's scale words of one stage (four K blocks, one byte each): its
+// weight row's for accumulator `half`, and for B chunks 2c + half its token
+// row's (padding rows get 1.0, any finite scale would do).
+struct MxScales {
+  uint32_t a, b[3];
+};
+
+__device__ __forceinline__ MxScales mx_fetch(const MxParams& P, const MxItem& t, int half, int r, int lane, int kpr,
+                                             int ks) {
+  MxScales v;
+  // rows past the expert (a W2 block of 128 features at the end) read a valid row
+  const bool row_in = t.mb * P.block_rows + half * P.acc1_offset + r < P.rows_per_expert;
+  const uint8_t* sa_row = P.w_scales + (size_t)(row_in ? t.wrow0 + half * P.acc1_offset + r : t.wrow0 + r) * kpr;
+  v.a = *reinterpret_cast<const uint32_t*>(sa_row + 4 * ks);
+#pragma unroll
+  for (int c = 0; c < 3; ++c) {
+    const int cb = 2 * c + half;
+    const int n = cb * 32 + lane;
+    v.b[c] = (cb < t.nsfb && n < t.n)
+                 ? *reinterpret_cast<const uint32_t*>(P.b_scales + (size_t)(t.row0 + n) * kpr + 4 * ks)
+                 : 0x7F7F7F7Fu;
+  }
+  return v;
 }
 
 template <bool W13>
@@ -190,8 +222,10 @@ mx_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
     if (lane == 0) {
       const uint64_t pol = l2_evict_first_policy();
       bool ok = true;
+      int4 tl = mx_tile(P, blockIdx.x, items);
       for (int it = blockIdx.x; it < items && ok; it += gridDim.x) {
-        const MxItem t = mx_item(P, it);
+        const MxItem t = mx_item(P, it, tl);
+        tl = mx_tile(P, it + gridDim.x, items);
         const int boxes = (t.n_mma + kBoxRows - 1) / kBoxRows;
         for (int ks = 0; ks < nks; ++ks, ++g) {
           const int s = g % kStages;
@@ -230,8 +264,10 @@ mx_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
       const int acc = warp == kMmaWarp ? 0 : 1;
       int g = 0, li = 0;
       bool ok = true;
+      int4 tl = mx_tile(P, blockIdx.x, items);
       for (int it = blockIdx.x; it < items && ok; it += gridDim.x, ++li) {
-        const MxItem t = mx_item(P, it);
+        const MxItem t = mx_item(P, it, tl);
+        tl = mx_tile(P, it + gridDim.x, items);
         if (li > 0 && !mbar_wait(acc_empty, (li - 1) & 1, abort_flag, P.err, kErrWaitTimeout, lim)) break;
         const uint32_t d_tmem = tmem + acc * t.acc_cols;
         for (int ks = 0; ks < nks; ++ks, ++g) {
@@ -265,24 +301,21 @@ mx_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
     const int r = q * 32 + lane;              // weight row (within the block) = TMEM lane
     int g = 0, li = 0, garr = 0;
     bool ok = true, stop = false;
+    // The scale words of a stage come from global memory (L2); they are
+    // fetched two stages ahead, and the next item's first two stages before
+    // the epilogue, so that their latency stays off the pipeline.
+    MxItem t = mx_item(P, blockIdx.x, mx_tile(P, blockIdx.x, items));
+    MxScales q0 = mx_fetch(P, t, half, r, lane, kpr, 0);
+    MxScales q1 = mx_fetch(P, t, half, r, lane, kpr, nks > 1 ? 1 : 0);
     for (int it = blockIdx.x; it < items && !stop; it += gridDim.x, ++li) {
-      const MxItem t = mx_item(P, it);
-      // this lane's weight row of accumulator `half` (rows past the expert read a valid row)
-      const bool row_in = t.mb * P.block_rows + half * P.acc1_offset + r < P.rows_per_expert;
-      const uint8_t* sa_row = P.w_scales + (size_t)(row_in ? t.wrow0 + half * P.acc1_offset + r : t.wrow0 + r) * kpr;
+      const int4 tl_next = mx_tile(P, it + gridDim.x, items);
       for (int ks = 0; ks < nks; ++ks, ++g) {
         const int s = g % kStages;
-        // the four scale bytes of this stage: one word per row
-        const uint32_t wa = *reinterpret_cast<const uint32_t*>(sa_row + 4 * ks);
-        uint32_t wb[3];
-#pragma unroll
-        for (int c = 0; c < 3; ++c) {
-          const int cb = 2 * c + half;        // B chunk of 32 token rows this warp writes
-          const int n = cb * 32 + lane;
-          wb[c] = (cb < t.nsfb && n < t.n) ? *reinterpret_cast<const uint32_t*>(P.b_scales +
-                                                                                  (size_t)(t.row0 + n) * kpr + 4 * ks)
-                                           : 0x7F7F7F7Fu;  // padding rows: any finite scale
-        }
+        const MxScales cur = q0;
+        q0 = q1;
+        if (ks + 2 < nks) q1 = mx_fetch(P, t, half, r, lane, kpr, ks + 2);
+        const uint32_t wa = cur.a;
+        const uint32_t wb[3] = {cur.b[0], cur.b[1], cur.b[2]};
         if (ok) ok = mbar_wait(&empty[s], ((g / kStages) & 1) ^ 1u, abort_flag, P.err, kErrWaitTimeout, lim);
         const uint32_t sf = lane_base + sf_base + s * kSfColsPerStage;
         tmem_st1(sf + half * 4 + q, wa);     // A scales: column base + quadrant
@@ -298,34 +331,53 @@ mx_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
         }
       }
       // ---------------- epilogue ----------------
+      const MxItem tc = t;
+      if (it + (int)gridDim.x < items) {
+        t = mx_item(P, it + gridDim.x, tl_next);
+        q0 = mx_fetch(P, t, half, r, lane, kpr, 0);
+        q1 = mx_fetch(P, t, half, r, lane, kpr, nks > 1 ? 1 : 0);
+      }
       if (__all_sync(0xFFFFFFFFu, ok && mbar_wait(acc_full, li & 1, abort_flag, P.err, kErrWaitTimeout, lim))) {
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         constexpr int kChunks = (kBN + 63) / 64;
 #pragma unroll
         for (int ci = 0; ci < kChunks; ++ci) {
           const int c0 = 32 * (2 * ci + half);
-          if (c0 >= t.n_mma) break;
+          if (c0 >= tc.n_mma) break;
           float a0[32], a1[32];
-          tmem_ld32x2(lane_base + c0, lane_base + t.acc_cols + c0, a0, a1);
+          tmem_ld32x2(lane_base + c0, lane_base + tc.acc_cols + c0, a0, a1);
           if (W13) {
-            const int i = t.mb * kBM + r;   // this lane's i; the warp holds one MX block of i
+            // all 32 columns are computed (those past the tile's rows too: no
+            // side effects), so that the 32 independent chains interleave;
+            // only the stores are predicated
+            const int i = tc.mb * kBM + r;   // this lane's i; the warp holds one MX block of i
+            const int nj = min(32, tc.n - c0);
+            uint32_t hb[32], code[32], sbv[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) hb[j] = f32_to_bf16_rn(swiglu(a0[j], a1[j]));
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-              if (c0 + j >= t.n) break;  // uniform: every lane has the same token column
-              const size_t row = (size_t)(t.row0 + c0 + j);
-              const uint32_t hb = f32_to_bf16_rn(swiglu(a0[j], a1[j]));
-              P.h_out[row * P.I + i] = (uint16_t)hb;
-              const uint32_t amax = __reduce_max_sync(0xFFFFFFFFu, hb & 0x7FFFu);
-              const uint32_t sb = mx_scale_byte(amax);
-              P.hq_out[row * P.I + i] = (uint8_t)(sb == 0xFFu ? 0x7Fu : mx_e4m3_code(hb, sb));
-              if (lane == 0) P.hq_scales[row * (P.I / 32) + i / 32] = (uint8_t)sb;
+              sbv[j] = mx_scale_byte(__reduce_max_sync(0xFFFFFFFFu, hb[j] & 0x7FFFu));
+              code[j] = sbv[j] == 0xFFu ? 0x7Fu : mx_e4m3_code(hb[j], sbv[j]);
+            }
+            const size_t row0 = (size_t)(tc.row0 + c0);
+            uint16_t* hp = P.h_out + row0 * P.I + i;
+            uint8_t* qp = P.hq_out + row0 * P.I + i;
+            uint8_t* sp = P.hq_scales + row0 * (P.I / 32) + i / 32;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              if (j < nj) {
+                hp[(size_t)j * P.I] = (uint16_t)hb[j];
+                qp[(size_t)j * P.I] = (uint8_t)code[j];
+                if (lane == 0) sp[(size_t)j * (P.I / 32)] = (uint8_t)sbv[j];
+              }
             }
           } else {
-            const int nrow = t.mb * P.block_rows + r;
+            const int nrow = tc.mb * P.block_rows + r;
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-              if (c0 + j < t.n) {
-                float* yrow = P.y_out + (size_t)(t.row0 + c0 + j) * P.d;
+              if (c0 + j < tc.n) {
+                float* yrow = P.y_out + (size_t)(tc.row0 + c0 + j) * P.d;
                 yrow[nrow] = a0[j];
                 if (nrow + P.acc1_offset < P.d) yrow[nrow + P.acc1_offset] = a1[j];
               }
@@ -421,7 +473,8 @@ bool map_fp4(CUtensorMap* m, const uint8_t* w, uint64_t K, uint64_t rows) {
 }  // namespace
 
 cudaError_t launch_mx_forward(const moe_fp4_dims& d, const uint16_t* x, const uint8_t* w13, const uint8_t* w13s,
-                              const uint8_t* w2, const uint8_t* w2s, const Workspace& ws, cudaStream_t st) {
+                              const uint8_t* w2, const uint8_t* w2s, const Workspace& ws, cudaStream_t st,
+                              const std::function<void(int)>& mark) {
   const size_t S = (size_t)d.T * d.k;
   // quantising gather of x into sorted order
   {
@@ -430,6 +483,7 @@ cudaError_t launch_mx_forward(const moe_fp4_dims& d, const uint16_t* x, const ui
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
+  if (mark) mark(2);
   CUtensorMap a, b;
   // W13: weights [E*2I rows][d], tokens xq [S][d]
   if (!map_fp4(&a, w13, d.d, (uint64_t)d.E * 2 * d.I) ||
@@ -454,6 +508,7 @@ cudaError_t launch_mx_forward(const moe_fp4_dims& d, const uint16_t* x, const ui
   P.wait_ns = wait_limit_ns();
   cudaError_t e = launch_mx<true>(a, b, P, ws.max_tc_tiles, st);
   if (e != cudaSuccess) return e;
+  if (mark) mark(3);
   // W2: weights [E*d rows][I], tokens hq [S][I]
   if (!map_fp4(&a, w2, d.I, (uint64_t)d.E * d.d) ||
       !make_map_2d(&b, CU_TENSOR_MAP_DATA_TYPE_UINT8, ws.hq, d.I, S, d.I, 128, kBoxRows, CU_TENSOR_MAP_SWIZZLE_128B))

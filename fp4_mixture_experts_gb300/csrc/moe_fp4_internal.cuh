@@ -8,6 +8,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <functional>
+
 #include "../../include/moe_fp4.h"
 
 namespace moe_fp4 {
@@ -107,8 +109,10 @@ cudaError_t launch_router(const moe_fp4_dims& d, const uint16_t* x, const uint16
                           cudaStream_t st);
 // block-scaled layer after routing: quantising gather, W13 (+ SwiGLU, h and
 // its MXFP8 form) and W2 on kind::mxf8f6f4 tensor cores; y in ws.y
+// `mark` (optional) is called with 2 after the gather and 3 after W13 (stage events)
 cudaError_t launch_mx_forward(const moe_fp4_dims& d, const uint16_t* x, const uint8_t* w13, const uint8_t* w13s,
-                              const uint8_t* w2, const uint8_t* w2s, const Workspace& ws, cudaStream_t st);
+                              const uint8_t* w2, const uint8_t* w2s, const Workspace& ws, cudaStream_t st,
+                              const std::function<void(int)>& mark);
 
 // ---------------------------------------------------------------------------
 // device helpers
