@@ -25,8 +25,9 @@
 // the token tile of a stage, one expect_tx); warps 1..8 the scale writers
 // (loaded from the scale arrays, written with tcgen05.st) and then the
 // epilogue; warps 0 and 11 the MMA issuers, one per accumulator (warp 0 also
-// owns TMEM).  The W13 epilogue writes h (bf16) and its MXFP8 form for W2:
-// the 32 lanes of a warp hold 32 consecutive i of one token, one MX block.
+// owns TMEM).  The W13 epilogue writes h (bf16); the MXFP8 quantiser then
+// writes h's MXFP8 form for W2 in a separate pass (the epilogue runs while
+// the MMAs wait, so work moved out of it is work taken off the MMA's path).
 // Waits are bounded; no warp leaves a loop early; on an abort the producer
 // completes the stages the stopped scale writers left open and waits for its
 // copies, and every MMA completes before TMEM is freed.
@@ -82,8 +83,6 @@ struct MxParams {
   const int32_t* counts;
   int32_t* err;
   uint16_t* h_out;            // W13: h bf16 [S, I]
-  uint8_t* hq_out;            // W13: h as E4M3 codes [S, I]
-  uint8_t* hq_scales;         // W13: E8M0 [S, I/32]
   float* y_out;               // W2: y [S, d]
   int K;
   int rows_per_expert;        // 2I (W13) or d (W2)
@@ -350,28 +349,15 @@ mx_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
             // all 32 columns are computed (those past the tile's rows too: no
             // side effects), so that the 32 independent chains interleave;
             // only the stores are predicated
-            const int i = tc.mb * kBM + r;   // this lane's i; the warp holds one MX block of i
+            const int i = tc.mb * kBM + r;
             const int nj = min(32, tc.n - c0);
-            uint32_t hb[32], code[32], sbv[32];
+            uint32_t hb[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) hb[j] = f32_to_bf16_rn(swiglu(a0[j], a1[j]));
+            uint16_t* hp = P.h_out + (size_t)(tc.row0 + c0) * P.I + i;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              sbv[j] = mx_scale_byte(__reduce_max_sync(0xFFFFFFFFu, hb[j] & 0x7FFFu));
-              code[j] = sbv[j] == 0xFFu ? 0x7Fu : mx_e4m3_code(hb[j], sbv[j]);
-            }
-            const size_t row0 = (size_t)(tc.row0 + c0);
-            uint16_t* hp = P.h_out + row0 * P.I + i;
-            uint8_t* qp = P.hq_out + row0 * P.I + i;
-            uint8_t* sp = P.hq_scales + row0 * (P.I / 32) + i / 32;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              if (j < nj) {
-                hp[(size_t)j * P.I] = (uint16_t)hb[j];
-                qp[(size_t)j * P.I] = (uint8_t)code[j];
-                if (lane == 0) sp[(size_t)j * (P.I / 32)] = (uint8_t)sbv[j];
-              }
-            }
+            for (int j = 0; j < 32; ++j)
+              if (j < nj) hp[(size_t)j * P.I] = (uint16_t)hb[j];
           } else {
             const int nrow = tc.mb * P.block_rows + r;
 #pragma unroll
@@ -496,8 +482,6 @@ cudaError_t launch_mx_forward(const moe_fp4_dims& d, const uint16_t* x, const ui
   P.counts = ws.counts;
   P.err = ws.err;
   P.h_out = ws.h;
-  P.hq_out = ws.hq;
-  P.hq_scales = ws.hq_scales;
   P.K = d.d;
   P.rows_per_expert = 2 * d.I;
   P.mblocks = d.I / kBM;
@@ -509,6 +493,10 @@ cudaError_t launch_mx_forward(const moe_fp4_dims& d, const uint16_t* x, const ui
   cudaError_t e = launch_mx<true>(a, b, P, ws.max_tc_tiles, st);
   if (e != cudaSuccess) return e;
   if (mark) mark(3);
+  // h in MXFP8 for W2 (a separate HBM-bound pass: cheaper than quantising
+  // inside the W13 epilogue, whose time the MMAs cannot overlap)
+  e = launch_mxfp8_quantize(ws.h, (long long)S, d.I, ws.hq, ws.hq_scales, st);
+  if (e != cudaSuccess) return e;
   // W2: weights [E*d rows][I], tokens hq [S][I]
   if (!map_fp4(&a, w2, d.I, (uint64_t)d.E * d.d) ||
       !make_map_2d(&b, CU_TENSOR_MAP_DATA_TYPE_UINT8, ws.hq, d.I, S, d.I, 128, kBoxRows, CU_TENSOR_MAP_SWIZZLE_128B))

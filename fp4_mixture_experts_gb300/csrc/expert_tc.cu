@@ -110,7 +110,7 @@ constexpr int kRawTileBytes = kBM * kRawRowBytes;  // packed tile of one accumul
 constexpr int kOffB = 0;                                       // [stage]
 constexpr int kOffRaw = kOffB + kStages * kBTileBytes;         // [stage][acc]
 constexpr int kOffRowscale = kOffRaw + kStagesRaw * 2 * kRawTileBytes;
-constexpr int kOffBar = kOffRowscale + 2 * kBM * 4;
+constexpr int kOffBar = kOffRowscale + 2 * 2 * kBM * 4;  // row scales [item parity][acc][row]
 constexpr int kSmemTc = kOffBar + 512 + 1024;  // + barriers, 1 KB alignment slack
 static_assert((2 * kStagesRaw + 2 * kStages + 4) * 8 + 8 + 4 * kDqWarps <= 512, "barrier area exceeded");
 static_assert(kSmemTc <= 227 * 1024, "shared memory of the tensor-core kernel exceeds 227 KB");
@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_raw, const TcParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float* rowscale = reinterpret_cast<float*>(smem + kOffRowscale);  // [2][128]
+  float* rowscale = reinterpret_cast<float*>(smem + kOffRowscale);  // [item parity][2][128]
   uint64_t* raw_full = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint64_t* raw_empty = raw_full + kStagesRaw;
   uint64_t* full = raw_empty + kStagesRaw;    // [stage]: token tile landed and both A slots written
@@ -333,53 +333,61 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
     const int kpr = P.K / 32;                // scale bytes per row
     uint32_t ph = 0;                         // A-slot phase bits
-    uint32_t g = 0;                          // packed-weight stages consumed so far (all items)
+    uint32_t g = 0;                          // packed-weight stages of the items before the one being converted
     int li = 0;
     int gdq = 0;                             // stages this warp signalled full (lane 0's count)
     bool ok = true;                          // this lane's waits have all succeeded
     bool stop = false;                       // all dequantisers stop after this item (uniform)
-    for (int it = blockIdx.x; it < items && !stop; it += gridDim.x, ++li) {
-      const TcItem t = tc_item(P, it);
-      // a W2 tile whose second block runs past the expert's d rows (d % 256 ==
-      // 128) reads a valid row there instead (its results are not written),
-      // so that no read leaves the weight and scale tensors
+    // The first steps of the next item are converted before the epilogue of
+    // the current one (into A slots below the current accumulators), so that
+    // its MMAs can start as soon as the epilogue has read the accumulators.
+    // Only the step count and the row's reference scale stay live across the
+    // epilogue; the rest of the conversion state is rebuilt after it.
+    const uint8_t* srow = nullptr;
+    int s_ref = 0;
+    const bool vec_scales = (kpr & 15) == 0;  // scale bytes 16 at a time (8 K steps), else 2 per step
+    uint4 sg_cur = make_uint4(0, 0, 0, 0), sg_next = make_uint4(0, 0, 0, 0);
+    uint32_t sc_next = 0;
+    // this thread's scale row of item t: a W2 tile whose second block runs
+    // past the expert's d rows (d % 256 == 128) reads a valid row there
+    // instead (its results are not written), so that no read leaves the
+    // weight and scale tensors
+    auto scale_row = [&](const TcItem& t) {
       const bool row_in = t.mb * P.block_rows + acc * P.acc1_offset + r < P.rows_per_expert;
       const int wrow = row_in ? t.wrow0 + acc * P.acc1_offset + r : t.wrow0 + r;
-      const uint8_t* srow = P.scales + (size_t)wrow * kpr;
-      int s_ref = 0;
-      {
-        uint32_t smax = 0;
-        auto max4 = [](uint32_t m, uint32_t w4) {
-          return max(m, max(max(w4 & 0xFFu, (w4 >> 8) & 0xFFu), max((w4 >> 16) & 0xFFu, w4 >> 24)));
-        };
-        if ((kpr & 15) == 0) {
-          constexpr int kSv = 16;  // 16-byte loads in flight at a time
-          for (int i0 = 0; i0 < kpr; i0 += 16 * kSv) {
-            uint4 sv[kSv];
-#pragma unroll
-            for (int i = 0; i < kSv; ++i)
-              if (i0 + 16 * i < kpr) sv[i] = *reinterpret_cast<const uint4*>(srow + i0 + 16 * i);
-#pragma unroll
-            for (int i = 0; i < kSv; ++i)
-              if (i0 + 16 * i < kpr) smax = max4(max4(max4(max4(smax, sv[i].x), sv[i].y), sv[i].z), sv[i].w);
-          }
-        } else {
-          for (int i = 0; i < kpr; i += 4) smax = max4(smax, *reinterpret_cast<const uint32_t*>(srow + i));
-        }
-        s_ref = (int)smax - 13;
-        rowscale[acc * 128 + r] = pow2f(s_ref - 127);
-      }
-      // scale bytes: 16 at a time (8 K steps) when rows are 16-byte aligned, else 2 per step
-      const bool vec_scales = (kpr & 15) == 0;
-      uint4 sg_cur = make_uint4(0, 0, 0, 0), sg_next = make_uint4(0, 0, 0, 0);
-      uint32_t sc_next = 0;
+      return P.scales + (size_t)wrow * kpr;
+    };
+    // reference scale of item t (row scale of item parity `buf`) and the
+    // scale-byte registers for step 0
+    auto prepare = [&](const TcItem& t, int buf) {
+      srow = scale_row(t);
+      uint32_t smax = 0;
+      auto max4 = [](uint32_t m, uint32_t w4) {
+        return max(m, max(max(w4 & 0xFFu, (w4 >> 8) & 0xFFu), max((w4 >> 16) & 0xFFu, w4 >> 24)));
+      };
       if (vec_scales) {
+        constexpr int kSv = 4;  // 16-byte loads in flight at a time (more would spill registers)
+        for (int i0 = 0; i0 < kpr; i0 += 16 * kSv) {
+          uint4 sv[kSv];
+#pragma unroll
+          for (int i = 0; i < kSv; ++i)
+            if (i0 + 16 * i < kpr) sv[i] = *reinterpret_cast<const uint4*>(srow + i0 + 16 * i);
+#pragma unroll
+          for (int i = 0; i < kSv; ++i)
+            if (i0 + 16 * i < kpr) smax = max4(max4(max4(max4(smax, sv[i].x), sv[i].y), sv[i].z), sv[i].w);
+        }
         sg_next = *reinterpret_cast<const uint4*>(srow);
       } else {
+        for (int i = 0; i < kpr; i += 4) smax = max4(smax, *reinterpret_cast<const uint32_t*>(srow + i));
         sc_next = *reinterpret_cast<const uint16_t*>(srow);
       }
-#pragma unroll kDqUnroll
-      for (int ks = 0; ks < nk; ++ks) {
+      s_ref = (int)smax - 13;
+      rowscale[buf * 256 + acc * 128 + r] = pow2f(s_ref - 127);
+    };
+    // K step ks of item t into the A ring; with active false (a step
+    // converted ahead) only the scale-byte registers advance
+    auto convert = [&](const TcItem& t, int ks, bool active) {
+      {
         const int sa = ks % t.nS;
         const int sub = ks % kRawSteps;
         const uint32_t gs = g + ks / kRawSteps;
@@ -387,7 +395,7 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
         // once a wait has failed (or seen the abort) this lane stops waiting
         // but keeps converting, so that the warp-wide tcgen05 instructions
         // below always see all 32 lanes
-        if (sub == 0 && ok)
+        if (active && sub == 0 && ok)
           ok = mbar_wait(&raw_full[rs_slot], (gs / kStagesRaw) & 1, abort_flag, P.err, kErrWaitTimeout, lim);
         // 128-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ (r mod 8),
         // so the 8 rows of a warp's quarter hit 8 different bank groups.  The
@@ -409,9 +417,9 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
           sc = sc_next;
           if (ks + 1 < nk) sc_next = *reinterpret_cast<const uint16_t*>(srow + 2 * (ks + 1));
         }
-        if (ok) ok = mbar_wait(&empty[sa], ((ph >> sa) & 1) ^ 1u, abort_flag, P.err, kErrWaitTimeout, lim);
-        ph ^= 1u << sa;
-        {
+        if (active) {
+          if (ok) ok = mbar_wait(&empty[sa], ((ph >> sa) & 1) ^ 1u, abort_flag, P.err, kErrWaitTimeout, lim);
+          ph ^= 1u << sa;
           const uint32_t s0 = sc & 0xFFu, s1 = (sc >> 8) & 0xFFu;
           const uint32_t m0 = f16x2_pow2((int)s0 - s_ref), m1 = f16x2_pow2((int)s1 - s_ref);
           uint32_t av[32];  // column j = K elements (2j, 2j+1) of this row
@@ -437,7 +445,32 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
           }
         }
       }
+    };
+    int pre = 0;  // K steps of the current item converted ahead
+    for (int it = blockIdx.x; it < items && !stop; it += gridDim.x, ++li) {
+      const TcItem t = tc_item(P, it);
+      if (pre == 0) {
+        prepare(t, li & 1);
+      } else {
+        srow = scale_row(t);  // scale-byte registers back at step 0
+        if (vec_scales)
+          sg_next = *reinterpret_cast<const uint4*>(srow);
+        else
+          sc_next = *reinterpret_cast<const uint16_t*>(srow);
+      }
+#pragma unroll kDqUnroll
+      for (int ks = 0; ks < nk; ++ks) convert(t, ks, ks >= pre);
       g += nrs;
+      // the next item's first steps, into the slots below both items' accumulators
+      pre = 0;
+      if (it + (int)gridDim.x < items) {
+        const TcItem tn = tc_item(P, it + gridDim.x);
+        const int m = min(nk, min(t.nS, tn.nS));
+        prepare(tn, (li + 1) & 1);
+#pragma unroll 1
+        for (int ks = 0; ks < m; ++ks) convert(tn, ks, true);
+        pre = m;
+      }
       // epilogue: the two warps of a lane quadrant take alternate 32-column
       // chunks; their column scales are fetched before the accumulators are ready
       constexpr int kChunks = (kBN + 63) / 64;
@@ -454,7 +487,7 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
       asm volatile("bar.sync 1, %0;" ::"r"(kDqWarps * 32) : "memory");
       if (__all_sync(0xFFFFFFFFu, ok && mbar_wait(acc_full, li & 1, abort_flag, P.err, kErrWaitTimeout, lim))) {
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const float rs0 = rowscale[r], rs1 = rowscale[128 + r];
+        const float rs0 = rowscale[(li & 1) * 256 + r], rs1 = rowscale[(li & 1) * 256 + 128 + r];
 #pragma unroll
         for (int ci = 0; ci < kChunks; ++ci) {
           const int c0 = 32 * (2 * ci + half);

@@ -107,6 +107,9 @@ cudaError_t launch_combine(const moe_fp4_dims& d, float* out, const Workspace& w
 bool tc_fused_combine(bool pairs);
 cudaError_t launch_router(const moe_fp4_dims& d, const uint16_t* x, const uint16_t* wg, float* logits,
                           cudaStream_t st);
+// MXFP8 of bf16 rows [rows, K] (K a multiple of 32; x and codes 16-byte aligned)
+cudaError_t launch_mxfp8_quantize(const uint16_t* x, long long rows, int K, uint8_t* codes, uint8_t* scales,
+                                  cudaStream_t st);
 // block-scaled layer after routing: quantising gather, W13 (+ SwiGLU, h and
 // its MXFP8 form) and W2 on kind::mxf8f6f4 tensor cores; y in ws.y
 // `mark` (optional) is called with 2 after the gather and 3 after W13 (stage events)

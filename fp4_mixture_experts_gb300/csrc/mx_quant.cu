@@ -59,6 +59,19 @@ mxfp8_quantize_kernel(const uint4* __restrict__ x, long long n_blocks, uint4* __
 }
 
 }  // namespace
+
+cudaError_t launch_mxfp8_quantize(const uint16_t* x, long long rows, int K, uint8_t* codes, uint8_t* scales,
+                                  cudaStream_t st) {
+  const long long n_blocks = rows * (K / 32);
+  if (n_blocks <= 0) return cudaSuccess;
+  long long grid = (n_blocks + 255) / 256;
+  const long long cap = (long long)num_sms() * 16;
+  if (grid > cap) grid = cap;
+  mxfp8_quantize_kernel<<<(unsigned)grid, 256, 0, st>>>(reinterpret_cast<const uint4*>(x), n_blocks,
+                                                        reinterpret_cast<uint4*>(codes), scales);
+  return cudaGetLastError();
+}
+
 }  // namespace moe_fp4
 
 extern "C" int moe_fp4_mxfp8_quantize(const void* x_bf16, int64_t rows, int32_t K, uint8_t* codes, uint8_t* scales,
@@ -69,11 +82,8 @@ extern "C" int moe_fp4_mxfp8_quantize(const void* x_bf16, int64_t rows, int32_t 
   if (!x_bf16 || !codes || !scales) return MOE_FP4_ERR_INVALID_ARG;
   if ((reinterpret_cast<uintptr_t>(x_bf16) & 15) || (reinterpret_cast<uintptr_t>(codes) & 15))
     return MOE_FP4_ERR_INVALID_ARG;
-  const long long n_blocks = (long long)rows * (K / 32);
-  long long grid = (n_blocks + 255) / 256;
-  const long long cap = (long long)num_sms() * 16;
-  if (grid > cap) grid = cap;
-  mxfp8_quantize_kernel<<<(unsigned)grid, 256, 0, static_cast<cudaStream_t>(cuda_stream)>>>(
-      static_cast<const uint4*>(x_bf16), n_blocks, reinterpret_cast<uint4*>(codes), scales);
-  return cudaGetLastError() == cudaSuccess ? MOE_FP4_OK : MOE_FP4_ERR_CUDA;
+  return launch_mxfp8_quantize(static_cast<const uint16_t*>(x_bf16), (long long)rows, K, codes, scales,
+                               static_cast<cudaStream_t>(cuda_stream)) == cudaSuccess
+             ? MOE_FP4_OK
+             : MOE_FP4_ERR_CUDA;
 }

@@ -285,13 +285,14 @@ size_t moe_fp4_mx_workspace_bytes(const moe_fp4_dims* dims);
  *   h_scales  uint8 [S, I/32]  E8M0 scales of h_q
  *   x_codes   uint8 [S, d]     E4M3 codes of x_q of the row's token, 16-byte aligned
  *   x_scales  uint8 [S, d/32]  E8M0 scales of x_q
- * Enqueues the routing kernel, the quantising gather, the two block-scaled
- * projections and the combine; never synchronises.  A block of x or h that
+ * Enqueues the routing kernel, the quantising gather, the W13 projection,
+ * the quantiser of h, the W2 projection and the combine; never synchronises.  A block of x or h that
  * holds an infinity or a NaN gets the NaN scale 0xFF and NaN codes, and the
  * rows it feeds come out NaN.
  * stage_events: NULL, or 6 cudaEvent_t handles recorded on the stream as in
  * moe_fp4_forward_profiled (before routing, after routing, after the
- * quantising gather, after W13, after W2, after the combine). */
+ * quantising gather, after W13, after the quantiser of h and W2, after the
+ * combine). */
 int moe_fp4_forward_mx(const moe_fp4_dims* dims, const void* x_bf16, const float* router_logits,
                        const uint8_t* w13, const uint8_t* w13_scale, const uint8_t* w2, const uint8_t* w2_scale,
                        float* out, void* h_bf16, uint8_t* h_codes, uint8_t* h_scales, uint8_t* x_codes,
