@@ -5,8 +5,9 @@ W2, combine) over one batch of synthetic inputs resident in HBM.  The
 default workload is the decode-shaped layer (T=32, d=4096, I=2048, E=256,
 k=8); the prefill-shaped layer (T=4608) is measured the same way and
 reported in the "prefill" object of the same line, the skewed-routing
-(T=2048) and large (T=16384, d=7168) layers under "other_workloads", and
-the MXFP8 activation quantiser under "mxfp8_quantize".  Every expert weight
+(T=2048) and large (T=16384, d=7168) layers under "other_workloads", the
+layer with MXFP8 activations on block-scaled tensor cores (prefill shape)
+under "mx_layer", and the MXFP8 activation quantiser under "mxfp8_quantize".  Every expert weight
 set touched per step (~2.2 GB decode, 3.4 GB prefill) is far larger than
 L2 (129 MB), so no L2 flush is needed between steps.
 
@@ -315,6 +316,61 @@ def roofline_prefill(res, pk, src):
     return out
 
 
+def measure_mx_layer(name, steps, warmup, dist, local, pk, src):
+    """The layer with MXFP8 activations (moe_fp4_forward_mx: both projections
+    on block-scaled kind::mxf8f6f4 tensor cores) on one workload, stage events
+    per step.  Stages: route, quantising gather, W13 (+ SwiGLU), h quantiser +
+    W2, combine.  The dominant kernel (W13) is reported against the dense fp8
+    peak, taken as the measured bf16 peak times 2 (the nominal fp8:bf16 ratio,
+    4.5 : 2.25 PFLOP/s)."""
+    import torch
+
+    import fp4_mixture_experts_gb300 as moe
+    L = make_config(name)
+    dev = torch.device("cuda", local)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    x = t(L.x_bf16.view(np.int16)).view(torch.bfloat16)
+    args = (x, t(L.router_logits), t(L.w13), t(L.w13_scale), t(L.w2), t(L.w2_scale), L.k)
+    ws = torch.empty(moe.mx_workspace_bytes(L.T, L.d, L.I, L.E, L.k), dtype=torch.uint8, device=dev)
+    out = torch.empty(L.T, L.d, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(steps)]
+    for row in evs:
+        for ev in row:
+            ev.record(stream)
+    for _ in range(warmup):
+        moe.forward_mx(*args, out=out, workspace=ws)
+    barrier(dist)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
+    start.record(stream)
+    for k in range(steps):
+        moe.forward_mx(*args, out=out, workspace=ws, stage_events=evs[k])
+    end.record(stream)
+    barrier(dist)
+    t1 = time.time()
+    moe.check(ws)
+    ms = max_over_ranks(dist, start.elapsed_time(end)) / steps
+    names = ["route", "gather_quantise", "w13_swiglu", "quantise_h_w2", "combine"]
+    stage_ms = {n: float(np.mean([evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(steps)]))
+                for i, n in enumerate(names)}
+    S = L.T * L.k
+    flops_w13 = 4.0 * S * L.d * L.I
+    ach = flops_w13 / (stage_ms["w13_swiglu"] * 1e-3) / 1e12
+    peak = 2.0 * pk["bf16_tflops"]
+    world = 1 if dist is None else dist.get_world_size()
+    res = {"workload": f"{name} MoE layer T={L.T} d={L.d} I={L.I} E={L.E} k={L.k} (seed 0), MXFP8 activations",
+           "value": round(world * L.T / (ms * 1e-3), 1), "unit": "tokens/s", "steps": steps,
+           "ms_per_step": round(ms, 4), "dtype": "fp4(e2m1) x fp8(e4m3), e8m0 block scales -> f32",
+           "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
+           "roofline": {"bound": "tensor", "kernel": "mx_kernel<W13>", "achieved": round(ach, 1), "peak": peak,
+                        "unit": "TFLOP/s", "frac": round(ach / peak, 4), "traffic": None,
+                        "peak_source": f"{src} bf16_tflops x 2 (nominal fp8:bf16 ratio; fp8 not measured)",
+                        "flops_per_launch": flops_w13}}
+    del ws, out, args, x
+    return res, (t0, t1)
+
+
 def measure_mxfp8(local, warmup=5, iters=50):
     """The MXFP8 activation quantiser on the prefill layer's permuted-activation
     shape (36,864 x 4096 bf16, 302 MB: larger than L2), CUDA events over
@@ -413,6 +469,12 @@ def run_ours(args):
                         "roofline": rf}
         del res
         torch.cuda.empty_cache()
+    mxl = None
+    if not args.no_mx_layer:
+        mx_steps = max(3, min(args.steps, 50))
+        mxl, win = measure_mx_layer("prefill", mx_steps, max(3, min(args.warmup, 5)), dist, local, pk, src)
+        windows.append(win)
+        torch.cuda.empty_cache()
     mxq = None
     if rank == 0 and not args.no_mxfp8:
         mxq, win = measure_mxfp8(local)
@@ -463,6 +525,8 @@ def run_ours(args):
             "roofline": rf}
     if others:
         line["other_workloads"] = others
+    if mxl is not None:
+        line["mx_layer"] = mxl
     if mxq is not None:
         line["mxfp8_quantize"] = mxq
     if not args.no_cpu_baseline:
@@ -567,6 +631,8 @@ def main():
     ap.add_argument("--also", default="skewed,large", help="comma list of further workloads to time after "
                     "decode and prefill (skewed, large; '' for none); reported under other_workloads")
     ap.add_argument("--no-mxfp8", action="store_true", help="skip timing the MXFP8 activation quantiser")
+    ap.add_argument("--no-mx-layer", action="store_true",
+                    help="skip timing the layer with MXFP8 activations (block-scaled tensor cores) at prefill")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES), default=None,

@@ -48,10 +48,21 @@ using namespace tc;
 constexpr int kBM = 128;
 constexpr int kBKs = 128;                  // K elements per stage (4 MMAs of K = 32)
 constexpr int kBN = kTcTileN;              // <= 192 token rows per tile
-#ifndef MOE_MX_STAGES
-#define MOE_MX_STAGES 3
+// Ring depth: 3 stages for W13, 4 for W2 (measured).  The scale writers'
+// loads hit L1 only while the rows they touch fit beside the stages: a W13
+// scale row is 128 bytes (K = 4096), a W2 row 64; with 4 stages L1 is about
+// 24 KB and the W13 rows no longer fit.
+#ifndef MOE_MX_STAGES_W13
+#define MOE_MX_STAGES_W13 3
 #endif
-constexpr int kStages = MOE_MX_STAGES;
+#ifndef MOE_MX_STAGES_W2
+#define MOE_MX_STAGES_W2 4
+#endif
+template <bool W13>
+__host__ __device__ constexpr int mx_stages() {
+  return W13 ? MOE_MX_STAGES_W13 : MOE_MX_STAGES_W2;
+}
+constexpr int kMaxStages = MOE_MX_STAGES_W13 > MOE_MX_STAGES_W2 ? MOE_MX_STAGES_W13 : MOE_MX_STAGES_W2;
 constexpr int kWriters = 8;                // scale writers, then the epilogue
 constexpr int kMmaWarp = 0;
 constexpr int kFirstWriter = 1;
@@ -69,11 +80,17 @@ constexpr int kStageBytes = 2 * kATileBytes + kBTileBytes;
 constexpr int kSfColsPerStage = 16;                 // SFA acc0 [0,4), acc1 [4,8), SFB [8, 8 + N/32)
 constexpr uint32_t kTmemCols = 512;
 constexpr int kOffStages = 0;
-constexpr int kOffBar = kOffStages + kStages * kStageBytes;
-constexpr int kSmemMx = kOffBar + 256 + 1024;
+template <bool W13>
+__host__ __device__ constexpr int mx_off_bar() {
+  return kOffStages + mx_stages<W13>() * kStageBytes;
+}
+template <bool W13>
+__host__ __device__ constexpr int mx_smem() {
+  return mx_off_bar<W13>() + 256 + 1024;
+}
 static_assert(kStageBytes % 1024 == 0, "stages must stay 1 KB aligned for the 128-byte swizzle");
-static_assert(kSmemMx <= 227 * 1024, "shared memory exceeds 227 KB");
-static_assert(2 * ((kBN + 31) / 32 * 32) + kStages * kSfColsPerStage <= (int)kTmemCols, "TMEM columns exceeded");
+static_assert(mx_smem<true>() <= 227 * 1024 && mx_smem<false>() <= 227 * 1024, "shared memory exceeds 227 KB");
+static_assert(2 * ((kBN + 31) / 32 * 32) + kMaxStages * kSfColsPerStage <= (int)kTmemCols, "TMEM columns exceeded");
 static_assert((kBN + 31) / 32 <= kSfColsPerStage - 8, "B scale columns exceed the stage's share");
 
 struct MxParams {
@@ -173,7 +190,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 mx_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b, const MxParams P) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kOffBar);  // [stage]: bytes landed, scales written
+  constexpr int kStages = mx_stages<W13>();
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + mx_off_bar<W13>());  // [stage]: bytes landed, scales written
   uint64_t* empty = full + kStages;                               // [stage]: its MMAs completed
   uint64_t* acc_full = empty + kStages;
   uint64_t* acc_empty = acc_full + 1;
@@ -399,6 +417,7 @@ mx_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
 
 template <bool W13>
 cudaError_t launch_mx(const CUtensorMap& a, const CUtensorMap& b, const MxParams& P, int max_tiles, cudaStream_t st) {
+  constexpr int kSmemMx = mx_smem<W13>();
   const cudaError_t oe = ensure_smem_optin(reinterpret_cast<const void*>(mx_kernel<W13>), kSmemMx);
   if (oe != cudaSuccess) return oe;
   const long long most = (long long)max_tiles * P.mblocks;
