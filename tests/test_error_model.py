@@ -87,3 +87,71 @@ def test_out_slack_covers_a_flip_and_nothing_more():
     import pytest
     with pytest.raises(AssertionError):
         assert_out_within(wrong, ref["out"], L)
+
+
+# ---- the MXFP8 layer: h's interval passed through the block quantiser ----
+def _bf16_neighbours(v):
+    """the bf16 values one ulp below and above v (bf16 values, fp64)"""
+    b = (np.asarray(v, dtype=np.float32).view(np.uint32) >> 16).astype(np.int64)
+    up = np.where(v >= 0, b + 1, b - 1)
+    dn = np.where(v > 0, b - 1, np.where(v == 0, 0x8001, b + 1))
+    f = lambda bits: ((bits.astype(np.uint32) & 0xFFFF) << 16).view(np.float32).astype(np.float64)
+    return np.minimum(f(dn), f(up)), np.maximum(f(dn), f(up))
+
+
+def test_mx_hq_bound_covers_every_choice_inside_the_interval():
+    """brute force: for blocks with up to three elements whose h may be either
+    bf16 neighbour (one of them the block's largest, next to a power of two,
+    so that the scale can move), every choice quantises within the bound"""
+    import itertools
+
+    from oracle import mx_activations as mxa
+
+    from _layer_util import mx_hq_bound
+    rng = np.random.default_rng(91)
+    for case in range(40):
+        h = oracle.bf16_round(rng.standard_normal((1, 32)) * np.exp2(rng.integers(-8, 8)))
+        if case % 2 == 0:   # the largest element right at a power of two: the scale exponent may step
+            j = int(np.argmax(np.abs(h)))
+            h[0, j] = np.copysign(np.exp2(np.floor(np.log2(np.abs(h[0, j]))) + 1), h[0, j])
+        idx = rng.choice(32, size=3, replace=False)
+        if case % 2 == 0:
+            idx[0] = int(np.argmax(np.abs(h)))
+        lo, hi = h.copy(), h.copy()
+        a, b = _bf16_neighbours(h[0, idx])
+        lo[0, idx], hi[0, idx] = a, b
+        hq = mxa.mx_round_trip(h)
+        bound = mx_hq_bound(lo, hi, hq)
+        for choice in itertools.product(range(3), repeat=3):
+            hp = h.copy()
+            for c, i in zip(choice, idx):
+                hp[0, i] = (lo[0, i], h[0, i], hi[0, i])[c]
+            d = np.abs(mxa.mx_round_trip(hp) - hq)
+            assert np.all(d <= bound), (case, choice)
+        # not vacuous: nothing moves by more than a few top-binade E4M3 ulps
+        top = np.exp2(np.floor(np.log2(np.abs(hi).max())) - 3)
+        assert bound.max() <= 4 * top
+
+
+def test_mx_hq_bound_is_zero_for_single_point_intervals():
+    from oracle import mx_activations as mxa
+
+    from _layer_util import mx_hq_bound
+    rng = np.random.default_rng(92)
+    h = oracle.bf16_round(rng.standard_normal((5, 64)))
+    assert not mx_hq_bound(h, h, mxa.mx_round_trip(h)).any()
+
+
+def test_mx_out_slack_rejects_a_real_error():
+    import pytest
+
+    from oracle import mx_activations as mxa
+
+    from _layer_util import MAX_ABS, assert_out_within_mx
+    L = make_layer(T=6, d=128, I=64, E=2, k=1, seed=93)
+    ref = mxa.forward_mx(L.x_bf16, L.router_logits, L.w13, L.w13_scale, L.w2, L.w2_scale, L.k)
+    assert_out_within_mx(ref["out"], ref["out"], L)
+    wrong = ref["out"].copy()
+    wrong[3, 7] += 50 * MAX_ABS
+    with pytest.raises(AssertionError):
+        assert_out_within_mx(wrong, ref["out"], L)
