@@ -364,7 +364,8 @@ def measure_mx_layer(name, steps, warmup, dist, local, pk, src):
            "ms_per_step": round(ms, 4), "dtype": "fp4(e2m1) x fp8(e4m3), e8m0 block scales -> f32",
            "stage_ms": {k: round(v, 4) for k, v in stage_ms.items()},
            "roofline": {"bound": "tensor", "kernel": "mx_kernel<W13>", "achieved": round(ach, 1), "peak": peak,
-                        "unit": "TFLOP/s", "frac": round(ach / peak, 4), "traffic": None,
+                        "unit": "TFLOP/s", "frac": round(ach / peak, 4),
+                        "traffic": ncu_traffic("mx_kernel<W13>@prefill"),
                         "peak_source": f"{src} bf16_tflops x 2 (nominal fp8:bf16 ratio; fp8 not measured)",
                         "flops_per_launch": flops_w13}}
     del ws, out, args, x
