@@ -108,6 +108,7 @@ struct MxParams {
   int acc1_offset;            // I (W13: up rows) or 128 (W2)
   int I, d;
   uint64_t wait_ns;
+  int fault;                  // nonzero: the first CTA withholds its first stage (fault-injection test)
 };
 
 // Block-scaled MMA: D (+)= A[smem] * B[smem] with the E8M0 scales of the
@@ -235,7 +236,8 @@ mx_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
   if (warp == kProdWarp) {
     // ---------------- TMA producer: both weight blocks and the token tile ----------------
     uint32_t ph = 0;
-    int g = 0;
+    int g = 0;  // stages passed (issued, or withheld by the fault injection)
+    const bool fault_cta = P.fault != 0 && blockIdx.x == 0;
     if (lane == 0) {
       const uint64_t pol = l2_evict_first_policy();
       bool ok = true;
@@ -251,6 +253,9 @@ mx_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
             break;
           }
           ph ^= 1u << s;
+          // fault injection: the first stage of the first CTA never arrives,
+          // so the MMA issuers' wait on it runs out
+          if (fault_cta && g == 0) continue;
           uint8_t* st = smem + kOffStages + s * kStageBytes;
           mbar_expect_tx(&full[s], 2 * kATileTxBytes + boxes * kBoxRows * 128);
           tma_load_2d_hint(st, &map_a, ks * kBKs, t.wrow0, &full[s], pol);
@@ -266,6 +271,7 @@ mx_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
     asm volatile("bar.sync 3, %0;" ::"r"((kWriters + 1) * 32) : "memory");
     if (lane == 0 && *abort_flag) {
       for (int q = g > kStages ? g - kStages : 0; q < g; ++q) {
+        if (fault_cta && q == 0) continue;  // withheld: no copy to wait for
         const int s = q % kStages;
         int arrived = 0;
         for (int w = 0; w < kWriters; ++w) arrived += wr_arrived[w] > q ? 1 : 0;
@@ -509,6 +515,7 @@ cudaError_t launch_mx_forward(const moe_fp4_dims& d, const uint16_t* x, const ui
   P.I = d.I;
   P.d = d.d;
   P.wait_ns = wait_limit_ns();
+  P.fault = fault_site() == MOE_FP4_FAULT_TC_TOKEN_TILE;
   cudaError_t e = launch_mx<true>(a, b, P, ws.max_tc_tiles, st);
   if (e != cudaSuccess) return e;
   if (mark) mark(3);

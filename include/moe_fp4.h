@@ -308,7 +308,10 @@ int moe_fp4_forward_mx(const moe_fp4_dims* dims, const void* x_bf16, const float
  * fault on the host's instruction, and every pipeline wait gives up after
  * wait_limit_us microseconds instead of 2 s:
  *   MOE_FP4_FAULT_TC_TOKEN_TILE   the tensor-core W13 kernel's first CTA never
- *                                 loads its first token tile;
+ *                                 loads its first token tile (in
+ *                                 moe_fp4_forward_mx: the block-scaled W13
+ *                                 kernel's first CTA never loads its first
+ *                                 stage);
  *   MOE_FP4_FAULT_STREAM_STAGE    the streaming W13 kernel's first CTA never
  *                                 loads its first weight stage.
  * Nothing faults, traps or hangs: the waiting threads give up, the outputs of

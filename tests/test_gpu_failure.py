@@ -56,6 +56,33 @@ def test_timed_out_wait_is_reported_and_the_next_call_is_correct(moe, site, flag
     assert_out_close(out.cpu().numpy(), ref["out"], f"after fault site {site}")
 
 
+def test_timed_out_wait_in_the_block_scaled_kernel(moe):
+    """the MXFP8-activation layer: its W13 kernel's first stage withheld"""
+    from oracle import mx_activations as mxa
+
+    from _layer_util import assert_out_within_mx
+    L = make_layer(T=48, d=1024, I=1024, E=8, k=2, seed=62)
+    D = to_device(L)
+    args = (D["x"], D["logits"], D["w13"], D["w13_scale"], D["w2"], D["w2_scale"], L.k)
+    ws = torch.empty(moe.mx_workspace_bytes(L.T, L.d, L.I, L.E, L.k), dtype=torch.uint8, device="cuda")
+    moe.set_fault_injection(moe.FAULT_TC_TOKEN_TILE, 20000)
+    try:
+        t0 = time.perf_counter()
+        moe.forward_mx(*args, workspace=ws)
+        with pytest.raises(moe.MoeFp4Error) as ei:
+            moe.check(ws)
+        elapsed = time.perf_counter() - t0
+    finally:
+        moe.set_fault_injection(moe.FAULT_NONE)
+    assert ei.value.status == -5
+    assert elapsed < 30.0
+    moe.check(ws)
+    out = moe.forward_mx(*args, workspace=ws)
+    moe.check(ws)
+    ref = mxa.forward_mx(L.x_bf16, L.router_logits, L.w13, L.w13_scale, L.w2, L.w2_scale, L.k)
+    assert_out_within_mx(out.cpu().numpy(), ref["out"], L, what="after the block-scaled fault")
+
+
 def test_fault_injection_arguments(moe):
     with pytest.raises(moe.MoeFp4Error):
         moe.set_fault_injection(7, 1000)
