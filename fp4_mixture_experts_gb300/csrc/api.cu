@@ -36,7 +36,8 @@ bool layout_workspace(const moe_fp4_dims& d, void* base, bool with_staging, Work
   const size_t S = (size_t)d.T * d.k;
   ws->nb_route = (d.T + kRouteTokensPerBlock - 1) / kRouteTokensPerBlock;
   ws->max_gemv_chunks = d.E + (int)((S + kGemvTokens - 1) / kGemvTokens);
-  ws->max_tc_tiles = d.E + (int)((S + kTcTileN - 1) / kTcTileN);
+  // at most one partial tile per expert beyond S / (smallest tile cap)
+  ws->max_tc_tiles = d.E + (int)((S + kTcTileMultiN - 1) / kTcTileMultiN);
   char* p = static_cast<char*>(base);
   size_t off = 0;
   auto take = [&](size_t bytes) -> void* {
@@ -323,7 +324,7 @@ int moe_fp4_forward_mx(const moe_fp4_dims* dims, const void* x_bf16, const float
     if (stage_events) cudaEventRecord(static_cast<cudaEvent_t>(stage_events[i]), st);
   };
   mark(0);
-  cudaError_t e = launch_route(d, router_logits, ws, st);
+  cudaError_t e = launch_route(d, router_logits, ws, st, kTcTileN);
   mark(1);
   if (e == cudaSuccess)
     e = launch_mx_forward(d, static_cast<const uint16_t*>(x_bf16), w13, w13_scale, w2, w2_scale, ws, st,

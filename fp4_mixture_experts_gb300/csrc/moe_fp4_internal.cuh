@@ -21,6 +21,20 @@ constexpr int kGemvTokens = 8;             // token rows per streaming-GEMV chun
 #define MOE_TC_TILE_N 192
 #endif
 constexpr int kTcTileN = MOE_TC_TILE_N;    // max token rows per tensor-core tile (UMMA N, a multiple of 64)
+// An expert whose rows need several tiles takes tiles of at most
+// kTcTileMultiN rows on the exact tensor-core path: a tile above 160 rows
+// leaves TMEM room for a 2-deep A ring only, and more tiles of <= 160 rows
+// (3- or 4-deep) measured faster there (large layer W13 6.40 -> 5.88 ms,
+// skewed 0.614 -> 0.543 ms), while one tile per expert stays best up to 192
+// rows (prefill).  The block-scaled path keeps its A operand in shared memory
+// and uses kTcTileN throughout.
+constexpr int kTcTileMultiN = 160;
+
+// Tensor-core tiles of an expert with cnt rows: one tile up to kTcTileN rows,
+// else ceil(cnt / multi) tiles (multi <= kTcTileN).
+__host__ __device__ inline int tc_tile_count(int cnt, int multi) {
+  return cnt <= 0 ? 0 : cnt <= kTcTileN ? 1 : (cnt + multi - 1) / multi;
+}
 
 // Device error word values (moe_fp4_check).
 constexpr int kErrBadExpertId = 1;
@@ -83,7 +97,10 @@ int fault_site();
 uint64_t wait_limit_ns();
 
 // ---- launchers (one per kernel family; each returns cudaGetLastError()) ----
-cudaError_t launch_route(const moe_fp4_dims& d, const float* logits, const Workspace& ws, cudaStream_t st);
+// tile_multi: the tile cap of experts with several tiles (kTcTileMultiN for
+// the exact tensor-core path, kTcTileN for the block-scaled one)
+cudaError_t launch_route(const moe_fp4_dims& d, const float* logits, const Workspace& ws, cudaStream_t st,
+                         int tile_multi = kTcTileMultiN);
 cudaError_t launch_gather(const moe_fp4_dims& d, const uint16_t* x, const Workspace& ws, cudaStream_t st);
 cudaError_t launch_h_f16(const moe_fp4_dims& d, const Workspace& ws, cudaStream_t st);
 cudaError_t launch_gemv_w13(const moe_fp4_dims& d, const uint16_t* x, const uint8_t* w13,

@@ -192,7 +192,7 @@ __device__ __forceinline__ unsigned long long pack2(int lo, int hi) {
 __global__ void __launch_bounds__(1024, 1)
 sort_scan_kernel(int32_t* __restrict__ block_hist, int nb, int E, int G, int32_t* __restrict__ offsets,
                  int32_t* __restrict__ active, int32_t* __restrict__ counts,
-                 int4* __restrict__ gemv_chunks, int4* __restrict__ tc_tiles) {
+                 int4* __restrict__ gemv_chunks, int4* __restrict__ tc_tiles, int tile_multi) {
   __shared__ unsigned long long scratch[33];
   const int e = threadIdx.x / G, p = threadIdx.x & (G - 1);
   const bool ok = e < E;
@@ -214,7 +214,7 @@ sort_scan_kernel(int32_t* __restrict__ block_hist, int nb, int E, int G, int32_t
   // offsets and the non-empty-expert positions in one scan, the GEMV chunk
   // and tensor-core tile positions in another
   const int nch = ok ? (cnt + kGemvTokens - 1) / kGemvTokens : 0;
-  const int ntl = ok ? (cnt + kTcTileN - 1) / kTcTileN : 0;
+  const int ntl = ok ? tc_tile_count(cnt, tile_multi) : 0;
   unsigned long long tot1, tot2;
   const unsigned long long x1 =
       block_exclusive_scan(lead ? pack2(cnt, cnt > 0 ? 1 : 0) : 0ull, scratch, &tot1);
@@ -238,7 +238,7 @@ sort_scan_kernel(int32_t* __restrict__ block_hist, int nb, int E, int G, int32_t
     // GEMV chunks of up to kGemvTokens rows
     for (int c = p; c < nch; c += G)
       gemv_chunks[cpos + c] = make_int4(e, off + c * kGemvTokens, min(kGemvTokens, cnt - c * kGemvTokens), 0);
-    // tensor-core tiles: ceil(cnt / kTcTileN) tiles of equal size (rounded up to 16)
+    // tensor-core tiles: tc_tile_count tiles of equal size (rounded up to 16)
     const int per_tile = ntl ? (((cnt + ntl - 1) / ntl + 15) & ~15) : 0;
     for (int c = p; c < ntl; c += G)
       tc_tiles[tpos + c] = make_int4(e, off + c * per_tile, min(per_tile, cnt - c * per_tile), 0);
@@ -311,9 +311,9 @@ static_assert(kSmallCtas * kSmallWarps == 32, "a token mask is one 32-bit word")
 // Per-expert counters packed in 16-bit fields: rows, non-empty, GEMV chunks,
 // tensor-core tiles.  Each total is at most T*k <= 1024 (or E <= 1024), so
 // fields never carry into one another.
-__device__ __forceinline__ unsigned long long pack4(int cnt) {
+__device__ __forceinline__ unsigned long long pack4(int cnt, int tile_multi) {
   const unsigned long long nch = (cnt + kGemvTokens - 1) / kGemvTokens;
-  const unsigned long long ntl = (cnt + kTcTileN - 1) / kTcTileN;
+  const unsigned long long ntl = tc_tile_count(cnt, tile_multi);
   return (unsigned long long)cnt | ((unsigned long long)(cnt > 0) << 16) | (nch << 32) | (ntl << 48);
 }
 
@@ -321,7 +321,8 @@ __global__ void __cluster_dims__(kSmallCtas, 1, 1) __launch_bounds__(kSmallThrea
 route_small_kernel(const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ topk_ids,
                    float* __restrict__ topk_w, int32_t* __restrict__ offsets, int32_t* __restrict__ active,
                    int32_t* __restrict__ counts, int4* __restrict__ gemv_chunks, int4* __restrict__ tc_tiles,
-                   int32_t* __restrict__ sorted_slot, int32_t* __restrict__ slot_pos, int32_t* __restrict__ err) {
+                   int32_t* __restrict__ sorted_slot, int32_t* __restrict__ slot_pos, int32_t* __restrict__ err,
+                   int tile_multi) {
   __shared__ int ids_s[kRouteTokensPerBlock * 32];  // [T*k] expert of each slot (CTA 0's copy)
   __shared__ uint32_t mask_s[kMaxExperts];          // bit t: token t picked the expert
   __shared__ int off_s[kMaxExperts];
@@ -354,7 +355,7 @@ route_small_kernel(const float* __restrict__ logits, int T, int E, int k, int32_
   const int ept = (E + kSmallThreads - 1) / kSmallThreads;
   const int e0 = min(E, (int)threadIdx.x * ept), e1 = min(E, e0 + ept);
   unsigned long long mine = 0;
-  for (int e = e0; e < e1; ++e) mine += pack4(__popc(mask_s[e]));
+  for (int e = e0; e < e1; ++e) mine += pack4(__popc(mask_s[e]), tile_multi);
   unsigned long long incl = mine;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -379,11 +380,11 @@ route_small_kernel(const float* __restrict__ logits, int T, int E, int k, int32_
     const int nch = (cnt + kGemvTokens - 1) / kGemvTokens;
     for (int c = 0; c < nch; ++c)
       gemv_chunks[cpos + c] = make_int4(e, off + c * kGemvTokens, min(kGemvTokens, cnt - c * kGemvTokens), 0);
-    // tensor-core tiles: ceil(cnt / kTcTileN) tiles of equal size (rounded up to 16)
-    const int ntl = (cnt + kTcTileN - 1) / kTcTileN;
+    // tensor-core tiles: tc_tile_count tiles of equal size (rounded up to 16)
+    const int ntl = tc_tile_count(cnt, tile_multi);
     const int per = ntl ? (((cnt + ntl - 1) / ntl + 15) & ~15) : 0;
     for (int c = 0; c < ntl; ++c) tc_tiles[tpos + c] = make_int4(e, off + c * per, min(per, cnt - c * per), 0);
-    base += pack4(cnt);
+    base += pack4(cnt, tile_multi);
   }
   if (threadIdx.x == 0) {
     offsets[E] = (int)(total & 0xFFFF);
@@ -403,12 +404,15 @@ route_small_kernel(const float* __restrict__ logits, int T, int E, int k, int32_
 
 }  // namespace
 
-cudaError_t launch_route(const moe_fp4_dims& d, const float* logits, const Workspace& ws, cudaStream_t st) {
+cudaError_t launch_route(const moe_fp4_dims& d, const float* logits, const Workspace& ws, cudaStream_t st,
+                         int tile_multi) {
   const int nb = ws.nb_route;
+  if (tile_multi < 16 || tile_multi > kTcTileN) return cudaErrorInvalidValue;
   if (nb == 1) {
     route_small_kernel<<<kSmallCtas, kSmallThreads, 0, st>>>(logits, d.T, d.E, d.k, ws.topk_ids, ws.topk_w,
                                                            ws.offsets, ws.active, ws.counts, ws.gemv_chunks,
-                                                           ws.tc_tiles, ws.sorted_slot, ws.slot_pos, ws.err);
+                                                           ws.tc_tiles, ws.sorted_slot, ws.slot_pos, ws.err,
+                                                           tile_multi);
     return cudaGetLastError();
   }
   size_t smem1 = (size_t)(kWarps * d.E) * sizeof(float) + (size_t)d.E * sizeof(int);
@@ -417,7 +421,7 @@ cudaError_t launch_route(const moe_fp4_dims& d, const float* logits, const Works
   int G = 1;  // threads per expert in sort_scan
   while (G < 32 && 2 * G * d.E <= 1024) G *= 2;
   sort_scan_kernel<<<1, 1024, 0, st>>>(ws.block_hist, nb, d.E, G, ws.offsets, ws.active, ws.counts,
-                                       ws.gemv_chunks, ws.tc_tiles);
+                                       ws.gemv_chunks, ws.tc_tiles, tile_multi);
   size_t smem3 = (size_t)(kWarps + 1) * d.E * sizeof(int);
   scatter_kernel<<<nb, kRouteThreads, smem3, st>>>(ws.topk_ids, ws.block_hist, d.T, d.E, d.k,
                                                    ws.sorted_slot, ws.slot_pos, ws.err);
