@@ -144,6 +144,25 @@ w2_rows_kernel(const uint16_t* __restrict__ h, const uint8_t* __restrict__ w2,
 // x_perm[r] = x[sorted_slot[r] / k] as f16 scaled by 2^shift_r, with
 // x_scale[r] = 2^-shift_r; the row's largest magnitude lands in [2^14, 2^15),
 // so every bf16 value within 2^31 of it converts exactly.  One warp per row.
+// NV > 0: the row is held in registers (NV 16-byte vectors per lane, all
+// loads issued before the first use, so a warp keeps NV loads in flight and
+// the row is read once); NV = 0: rows too long for that are read twice.
+__device__ __forceinline__ uint32_t bf16x2_max_exp(uint32_t e, uint32_t w) {
+  return max(e, max((w >> 7) & 0xFFu, (w >> 23) & 0xFFu));
+}
+
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(const uint4 q, float f1, float f2) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half2 h = __floats2half2_rn(bf16_to_f32(w[i] & 0xFFFFu) * f1 * f2, bf16_to_f32(w[i] >> 16) * f1 * f2);
+    o[i] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+template <int NV>
 __global__ void __launch_bounds__(256)
 gather_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ sorted_slot, int S, int k, int d,
               uint16_t* __restrict__ x_perm, float* __restrict__ x_scale, int32_t* __restrict__ zero, int n_zero) {
@@ -157,29 +176,56 @@ gather_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ sorted
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)(sorted_slot ? sorted_slot[r] / k : r) * d);
     uint4* dst = reinterpret_cast<uint4*>(x_perm + (size_t)r * d);
     uint32_t emax = 1;
-    for (int v = lane; v < vec; v += 32) {
-      const uint4 q = src[v];
-      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    uint4 q[NV > 0 ? NV : 1];
+    if (NV > 0) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) emax = max(emax, max((w[i] >> 7) & 0xFFu, (w[i] >> 23) & 0xFFu));
+      for (int i = 0; i < NV; ++i)
+        if (lane + 32 * i < vec) q[i] = src[lane + 32 * i];
+#pragma unroll
+      for (int i = 0; i < NV; ++i)
+        if (lane + 32 * i < vec)
+          emax = bf16x2_max_exp(bf16x2_max_exp(bf16x2_max_exp(bf16x2_max_exp(emax, q[i].x), q[i].y), q[i].z), q[i].w);
+    } else {
+#pragma unroll 4
+      for (int v = lane; v < vec; v += 32) {
+        const uint4 t = src[v];
+        emax = bf16x2_max_exp(bf16x2_max_exp(bf16x2_max_exp(bf16x2_max_exp(emax, t.x), t.y), t.z), t.w);
+      }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) emax = max(emax, __shfl_xor_sync(0xFFFFFFFFu, emax, o));
     const int shift = 141 - (int)emax;
     const float f1 = ldexpf(1.0f, shift / 2), f2 = ldexpf(1.0f, shift - shift / 2);
-    for (int v = lane; v < vec; v += 32) {
-      const uint4 q = src[v];
-      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-      uint32_t o[4];
+    if (NV > 0) {
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const __half2 h = __floats2half2_rn(bf16_to_f32(w[i] & 0xFFFFu) * f1 * f2, bf16_to_f32(w[i] >> 16) * f1 * f2);
-        o[i] = *reinterpret_cast<const uint32_t*>(&h);
-      }
-      dst[v] = make_uint4(o[0], o[1], o[2], o[3]);
+      for (int i = 0; i < NV; ++i)
+        if (lane + 32 * i < vec) dst[lane + 32 * i] = bf16x8_to_f16x8(q[i], f1, f2);
+    } else {
+#pragma unroll 4
+      for (int v = lane; v < vec; v += 32) dst[v] = bf16x8_to_f16x8(src[v], f1, f2);
     }
     if (lane == 0) x_scale[r] = ldexpf(1.0f, -shift);
   }
+}
+
+// the row of d elements in registers when it fits 32 vectors a lane (d <= 8192)
+cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* sorted_slot, int S, int k, int d, uint16_t* out,
+                               float* scale, int32_t* zero, int n_zero, cudaStream_t st) {
+  const int nv = (d / 8 + 31) / 32;
+  const int per_block = 8;  // rows (warps) per block
+  int blocks = (S + per_block - 1) / per_block;
+  const int cap = num_sms() * (nv > 16 ? 4 : 8);
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  if (nv <= 8)
+    gather_kernel<8><<<blocks, 256, 0, st>>>(x, sorted_slot, S, k, d, out, scale, zero, n_zero);
+  else if (nv <= 16)
+    gather_kernel<16><<<blocks, 256, 0, st>>>(x, sorted_slot, S, k, d, out, scale, zero, n_zero);
+  else if (nv <= 32)
+    gather_kernel<32><<<blocks, 256, 0, st>>>(x, sorted_slot, S, k, d, out, scale, zero, n_zero);
+  else
+    gather_kernel<0><<<blocks, 256, 0, st>>>(x, sorted_slot, S, k, d, out, scale, zero, n_zero);
+  return cudaGetLastError();
 }
 
 // out[t] = sum_j w_tj * y[slot_pos(t, j)]; block (t, c) covers columns
@@ -226,19 +272,12 @@ cudaError_t launch_gemv_w2(const moe_fp4_dims& d, const uint8_t* w2, const uint8
 }
 
 cudaError_t launch_gather(const moe_fp4_dims& d, const uint16_t* x, const Workspace& ws, cudaStream_t st) {
-  const int S = d.T * d.k;
-  int blocks = (S + 7) / 8;
-  if (blocks > num_sms() * 16) blocks = num_sms() * 16;
-  gather_kernel<<<blocks, 256, 0, st>>>(x, ws.sorted_slot, S, d.k, d.d, ws.x_perm, ws.x_scale, ws.combine_cnt,
-                                       d.T * ((d.d + 255) / 256));
-  return cudaGetLastError();
+  return launch_gather_rows(x, ws.sorted_slot, d.T * d.k, d.k, d.d, ws.x_perm, ws.x_scale, ws.combine_cnt,
+                            d.T * ((d.d + 255) / 256), st);
 }
 
 cudaError_t launch_h_f16(const moe_fp4_dims& d, const Workspace& ws, cudaStream_t st) {
-  const int S = d.T * d.k;
-  const int blocks = (S + 7) / 8 < num_sms() * 16 ? (S + 7) / 8 : num_sms() * 16;
-  gather_kernel<<<blocks, 256, 0, st>>>(ws.h, nullptr, S, 1, d.I, ws.h16, ws.h_scale, nullptr, 0);
-  return cudaGetLastError();
+  return launch_gather_rows(ws.h, nullptr, d.T * d.k, 1, d.I, ws.h16, ws.h_scale, nullptr, 0, st);
 }
 
 cudaError_t launch_combine(const moe_fp4_dims& d, float* out, const Workspace& ws, cudaStream_t st) {
