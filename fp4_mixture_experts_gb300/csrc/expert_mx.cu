@@ -375,13 +375,14 @@ mx_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
             // only the stores are predicated
             const int i = tc.mb * kBM + r;
             const int nj = min(32, tc.n - c0);
-            uint32_t hb[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) hb[j] = f32_to_bf16_rn(swiglu(a0[j], a1[j]));
             uint16_t* hp = P.h_out + (size_t)(tc.row0 + c0) * P.I + i;
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (j < nj) hp[(size_t)j * P.I] = (uint16_t)hb[j];
+            for (int j = 0; j < 32; j += 2) {
+              // two columns per conversion (cvt.rn.bf16x2.f32)
+              const __nv_bfloat162 hb = __floats2bfloat162_rn(swiglu(a0[j], a1[j]), swiglu(a0[j + 1], a1[j + 1]));
+              if (j < nj) hp[(size_t)j * P.I] = __bfloat16_as_ushort(__low2bfloat16(hb));
+              if (j + 1 < nj) hp[(size_t)(j + 1) * P.I] = __bfloat16_as_ushort(__high2bfloat16(hb));
+            }
           } else {
             const int nrow = tc.mb * P.block_rows + r;
 #pragma unroll

@@ -497,12 +497,16 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
           const float xs_l = xs_pre[ci];
           if (W13) {
             const int i = t.mb * kBM + r;
+            // two columns per conversion (cvt.rn.bf16x2.f32: one instruction
+            // for both roundings, nearest even like the single conversion)
+            uint16_t* hp = P.h_out + (size_t)(t.row0 + c0) * P.I + i;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float xs = __shfl_sync(0xFFFFFFFFu, xs_l, j);
-              if (c0 + j < t.n)
-                P.h_out[(size_t)(t.row0 + c0 + j) * P.I + i] =
-                    f32_to_bf16_rn(swiglu(a0[j] * rs0 * xs, a1[j] * rs1 * xs));
+            for (int j = 0; j < 32; j += 2) {
+              const float xs0 = __shfl_sync(0xFFFFFFFFu, xs_l, j), xs1 = __shfl_sync(0xFFFFFFFFu, xs_l, j + 1);
+              const __nv_bfloat162 hb = __floats2bfloat162_rn(swiglu(a0[j] * rs0 * xs0, a1[j] * rs1 * xs0),
+                                                              swiglu(a0[j + 1] * rs0 * xs1, a1[j + 1] * rs1 * xs1));
+              if (c0 + j < t.n) hp[(size_t)j * P.I] = __bfloat16_as_ushort(__low2bfloat16(hb));
+              if (c0 + j + 1 < t.n) hp[(size_t)(j + 1) * P.I] = __bfloat16_as_ushort(__high2bfloat16(hb));
             }
           } else {
             const int nrow = t.mb * P.block_rows + r;
