@@ -127,3 +127,28 @@ def test_fault_injection_setting_is_checked_on_the_host(lib):
     assert lib.moe_fp4_set_fault_injection(-1, 1000) == -1
     assert lib.moe_fp4_set_fault_injection(1, 0) == -1
     assert lib.moe_fp4_set_fault_injection(0, 0) == 0
+
+
+def test_forward_mx_rejects_bad_arguments_on_the_host(lib):
+    P = ctypes.c_void_p
+    fake = 0x100000  # never dereferenced: every call below fails its host-side checks
+    d = moe.Dims(16, 256, 128, 8, 2)
+    f = lib.moe_fp4_forward_mx
+    ws = moe.mx_workspace_bytes(16, 256, 128, 8, 2)
+    assert ws > moe.workspace_bytes(16, 256, 128, 8, 2)  # the MXFP8 operand regions
+    assert moe.mx_workspace_bytes(16, 100, 128, 8, 2) == 0
+    w = [P(fake)] * 7                                     # x, logits, w13, w13 scales, w2, w2 scales, out
+    opt = [None] * 5                                      # h, h codes, h scales, x codes, x scales
+    # null out
+    assert f(ctypes.byref(d), *w[:6], None, *opt, P(fake), ws, None, None) == -1
+    # w13 / w2 must be 32-byte aligned (4-bit tensor maps)
+    assert f(ctypes.byref(d), P(fake), P(fake), P(fake + 16), *w[3:], *opt, P(fake), ws, None, None) == -1
+    assert f(ctypes.byref(d), *w[:4], P(fake + 16), *w[5:], *opt, P(fake), ws, None, None) == -1
+    # misaligned optional code outputs
+    assert f(ctypes.byref(d), *w, None, P(fake + 8), None, None, None, P(fake), ws, None, None) == -1
+    assert f(ctypes.byref(d), *w, None, None, None, P(fake + 8), None, P(fake), ws, None, None) == -1
+    # unsupported sizes, workspace too small, misaligned workspace
+    bad = moe.Dims(16, 100, 128, 8, 2)
+    assert f(ctypes.byref(bad), *w, *opt, P(fake), ws, None, None) == -2
+    assert f(ctypes.byref(d), *w, *opt, P(fake), ws - 256, None, None) == -3
+    assert f(ctypes.byref(d), *w, *opt, P(fake + 16), ws, None, None) == -1

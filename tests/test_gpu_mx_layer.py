@@ -184,3 +184,10 @@ def test_mx_prefill_full_size(moe):
     sub = mxa.forward_mx(L.x_bf16[toks], L.router_logits[toks], L.w13, L.w13_scale, L.w2, L.w2_scale, L.k)
     m, excess = assert_out_within_mx(r["out"].numpy()[toks], sub["out"], L, toks, "prefill")
     print("prefill mx", m, "largest excess over max abs:", excess)
+
+
+def test_mx_decode_shape(moe):
+    """the decode workload's sizes (T=32, d=4096, I=2048, E=256, k=8): about one
+    row per expert, so every token tile is the smallest (N = 16) and the
+    ragged-tile paths of the block-scaled kernel run on every item"""
+    check_layer(moe, make_config("decode"), what="decode shape")
