@@ -509,14 +509,26 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
               if (c0 + j + 1 < t.n) hp[(size_t)(j + 1) * P.I] = __bfloat16_as_ushort(__high2bfloat16(hb));
             }
           } else {
-            const int nrow = t.mb * P.block_rows + r;
+            // 8-byte stores of two adjacent features: for the token pair (j,
+            // j + 1) the even lane of each lane pair takes token j and the odd
+            // lane token j + 1, swapping one value with its neighbour (half
+            // the store instructions, which bound this epilogue)
+            const bool odd = lane & 1;
+            const int nrow = t.mb * P.block_rows + (r & ~1);  // the pair's first feature
+            const bool second_in = nrow + P.acc1_offset < P.d;  // last block may hold 128 rows
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float xs = __shfl_sync(0xFFFFFFFFu, xs_l, j);
-              if (c0 + j < t.n) {
-                float* yrow = P.y_out + (size_t)(t.row0 + c0 + j) * P.d;
-                yrow[nrow] = a0[j] * rs0 * xs;
-                if (nrow + P.acc1_offset < P.d) yrow[nrow + P.acc1_offset] = a1[j] * rs1 * xs;  // last block may hold 128 rows
+            for (int j = 0; j < 32; j += 2) {
+              const float xs0 = __shfl_sync(0xFFFFFFFFu, xs_l, j), xs1 = __shfl_sync(0xFFFFFFFFu, xs_l, j + 1);
+              const float p0 = a0[j] * rs0 * xs0, q0 = a0[j + 1] * rs0 * xs1;
+              const float p1 = a1[j] * rs1 * xs0, q1 = a1[j + 1] * rs1 * xs1;
+              const float o0 = __shfl_xor_sync(0xFFFFFFFFu, odd ? p0 : q0, 1);
+              const float o1 = __shfl_xor_sync(0xFFFFFFFFu, odd ? p1 : q1, 1);
+              const int jj = j + (odd ? 1 : 0);
+              if (c0 + jj < t.n) {
+                float* yrow = P.y_out + (size_t)(t.row0 + c0 + jj) * P.d + nrow;
+                *reinterpret_cast<float2*>(yrow) = odd ? make_float2(o0, q0) : make_float2(p0, o0);
+                if (second_in)
+                  *reinterpret_cast<float2*>(yrow + P.acc1_offset) = odd ? make_float2(o1, q1) : make_float2(p1, o1);
               }
             }
           }
