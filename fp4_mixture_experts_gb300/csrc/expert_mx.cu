@@ -384,13 +384,23 @@ mx_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUt
               if (j + 1 < nj) hp[(size_t)(j + 1) * P.I] = __bfloat16_as_ushort(__high2bfloat16(hb));
             }
           } else {
-            const int nrow = tc.mb * P.block_rows + r;
+            // 8-byte stores of two adjacent features: for the token pair (j,
+            // j + 1) the even lane of each lane pair takes token j and the odd
+            // lane token j + 1, swapping one value with its neighbour
+            const bool odd = lane & 1;
+            const int nrow = tc.mb * P.block_rows + (r & ~1);  // the pair's first feature
+            const bool second_in = nrow + P.acc1_offset < P.d;  // last block may hold 128 rows
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              if (c0 + j < tc.n) {
-                float* yrow = P.y_out + (size_t)(tc.row0 + c0 + j) * P.d;
-                yrow[nrow] = a0[j];
-                if (nrow + P.acc1_offset < P.d) yrow[nrow + P.acc1_offset] = a1[j];
+            for (int j = 0; j < 32; j += 2) {
+              const float o0 = __shfl_xor_sync(0xFFFFFFFFu, odd ? a0[j] : a0[j + 1], 1);
+              const float o1 = __shfl_xor_sync(0xFFFFFFFFu, odd ? a1[j] : a1[j + 1], 1);
+              const int jj = j + (odd ? 1 : 0);
+              if (c0 + jj < tc.n) {
+                float* yrow = P.y_out + (size_t)(tc.row0 + c0 + jj) * P.d + nrow;
+                *reinterpret_cast<float2*>(yrow) = odd ? make_float2(o0, a0[j + 1]) : make_float2(a0[j], o0);
+                if (second_in)
+                  *reinterpret_cast<float2*>(yrow + P.acc1_offset) =
+                      odd ? make_float2(o1, a1[j + 1]) : make_float2(a1[j], o1);
               }
             }
           }
