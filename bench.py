@@ -66,6 +66,20 @@ def ncu_traffic(key):
         return None
 
 
+def decode_config(world):
+    """The `config` object of both arms' JSON lines: the decode workload, the
+    same keys and values for the CUDA path and the oracle's reference arm
+    (the touched experts counted from the workload's router logits: the top-8
+    of each token, ties to the lower index, as the layer routes)."""
+    L = make_config("decode")
+    order = np.lexsort((np.broadcast_to(np.arange(L.E), L.router_logits.shape), -L.router_logits), axis=1)
+    touched = int(np.unique(order[:, :L.k]).size)
+    return {"workload": "decode-shaped MoE layer T=32 d=4096 I=2048 E=256 k=8 (seed 0)",
+            "global_batch": world * L.T, "parallelism": f"replicas x{world}",
+            "l2": "inputs larger than L2 (touched weights %.2f GB)" % (touched * sum(expert_bytes(L.d, L.I)) / 1e9),
+            "touched_experts": touched}
+
+
 def expert_bytes(d, I):
     """packed codes + E8M0 scales of one expert: W13 [2I, d] and W2 [d, I]"""
     w13 = 2 * I * d // 2 + 2 * I * d // 32
@@ -500,12 +514,8 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
         "ms_per_step_stream_launch": round(dec["ms_stream"] / args.steps, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "fp4(e2m1)xbf16->f32", "data": "synthetic",
-        "config": {"workload": "decode-shaped MoE layer T=32 d=4096 I=2048 E=256 k=8 (seed 0)",
-                   "global_batch": world * L.T, "parallelism": f"replicas x{world}",
-                   "launch": "one layer call captured in a CUDA graph, replayed per step",
-                   "l2": "inputs larger than L2 (touched weights %.2f GB)" % (
-                       dec["touched"] * sum(expert_bytes(L.d, L.I)) / 1e9),
-                   "touched_experts": dec["touched"]},
+        "config": decode_config(world),
+        "launch": "one layer call captured in a CUDA graph, replayed per step",
         "stage_ms": {k: round(v, 5) for k, v in dec["stage_ms"].items()},
         "roofline": roofline_decode(dec, pk, src),
         "gpu_launches": launches_per_step * args.steps,
@@ -577,7 +587,7 @@ def run_reference(args):
             "value": round(value, 4), "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "decode-shaped MoE layer T=32 d=4096 I=2048 E=256 k=8 (seed 0)"},
+            "config": decode_config(args.gpus),
             "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
                              "sample": f"{units:.3f} tokens (one token, or part of its {L.k} experts, per step)"},
             "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
