@@ -191,3 +191,29 @@ def test_mx_decode_shape(moe):
     row per expert, so every token tile is the smallest (N = 16) and the
     ragged-tile paths of the block-scaled kernel run on every item"""
     check_layer(moe, make_config("decode"), what="decode shape")
+
+
+def test_mx_graph_capture_replays_bit_identical(moe):
+    """the MXFP8-activation layer allocates nothing and never waits on the
+    host, so one call can be captured in a CUDA graph; replays give the eager
+    call's output bit for bit"""
+    L = make_layer(T=300, d=1024, I=512, E=16, k=4, seed=21)
+    D = to_device(L)
+    args = (D["x"], D["logits"], D["w13"], D["w13_scale"], D["w2"], D["w2_scale"], L.k)
+    ws = torch.empty(moe.mx_workspace_bytes(L.T, L.d, L.I, L.E, L.k), dtype=torch.uint8, device="cuda")
+    out = torch.empty(L.T, L.d, dtype=torch.float32, device="cuda")
+    eager = moe.forward_mx(*args, workspace=ws).clone()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        moe.forward_mx(*args, out=out, workspace=ws)
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        moe.forward_mx(*args, out=out, workspace=ws)
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, eager)
+    moe.check(ws)
