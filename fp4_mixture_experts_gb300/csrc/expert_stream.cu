@@ -16,14 +16,14 @@
 //     power of two per token (every bf16 value within 2^31 of the row maximum
 //     is exact, smaller ones round at 2^-39 of it);
 //   - per 32-element MX block a thread loads 4 packed bytes of each of its
-//     two rows, one byte per register (a 4 x u8 vector load, so no shifts are
-//     spent on the ALU pipe); every cvt.rn.f16x2.e2m1x2 result is directly an
+//     two rows as one 32-bit word (32-bit shared-window addresses, offsets
+//     precomputed per thread: the loop spends its ALU issue on little but the
+//     conversions); every cvt.rn.f16x2.e2m1x2 result is directly an
 //     A-fragment register of mma.sync.m16n8k16 (the K order inside the block
 //     is permuted so that each thread's bytes and activations are contiguous,
-//     identically for A and B); two MMAs give the block's exact sums (f16 x
-//     f16 products are exact, accumulation fp32), which are scaled by
-//     2^(s-127) in fp32 and accumulated, so every E8M0 value is handled
-//     exactly;
+//     identically for A and B); two MMAs give the block's sums (f16 x f16
+//     products are exact, accumulation fp32), which are scaled by 2^(s-127)
+//     in fp32 and accumulated, so every E8M0 value is handled exactly;
 //   - the W13 epilogue applies SwiGLU and rounds h to bf16, the W2 epilogue
 //     writes fp32 y.
 // Waits are bounded; a timeout raises the CTA abort flag, after which every
@@ -72,17 +72,39 @@ struct StreamParams {
   int act_l2;              // nonzero: read the activations through L2 only (written by other SMs in this launch)
 };
 
-__device__ __forceinline__ uint32_t e2m1x2_h2(uint32_t byte) { return e2m1x2_to_f16x2(byte); }
-
-// 4 consecutive bytes of shared memory, one per register (zero-extended):
-// one load instead of a word load and three shifts on the busy ALU pipe.  Not
-// volatile, so loads of later blocks may be scheduled early; the memory clobber
-// keeps it after the wait on the stage's full barrier.
-__device__ __forceinline__ void lds_bytes4(const uint8_t* p, uint32_t (&b)[4]) {
+// Shared-memory loads by 32-bit shared-window address.  Not volatile, so loads
+// of later blocks may be scheduled early; the memory clobber keeps them after
+// the wait on the stage's full barrier.
+//
+// 4 consecutive bytes, one per register (zero-extended): the E8M0 scales.
+__device__ __forceinline__ void lds_bytes4(uint32_t a, uint32_t (&b)[4]) {
   asm("ld.shared.v4.u8 {%0,%1,%2,%3}, [%4];"
       : "=r"(b[0]), "=r"(b[1]), "=r"(b[2]), "=r"(b[3])
-      : "r"(smem_u32(p))
+      : "r"(a)
       : "memory");
+}
+
+__device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
+  uint32_t v;
+  asm("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint4 lds_u128(uint32_t a) {
+  uint4 v;
+  asm("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a) : "memory");
+  return v;
+}
+
+// The 8 E2M1 codes of a 32-bit word as 4 f16x2 registers (byte j -> r[j],
+// low nibble -> low half).  The vector move names the word's bytes for the
+// conversions, so no shifts or masks are spent on the ALU pipe.
+__device__ __forceinline__ void e2m1x8_f16(uint32_t w, uint32_t (&r)[4]) {
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+      : "r"(w));
 }
 
 __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1,
@@ -242,14 +264,26 @@ __device__ __forceinline__ void stream_consume(const StreamParams& P, const Stre
   const int g = lane >> 2, t = lane & 3;
   const int tile = warp % kTiles, kpart = warp / kTiles;  // 16-row tile, share of the stage's blocks
   // rows of this thread inside the stage's 128 rows (A-fragment rows g and g+8)
-  const int rowA = W13 ? tile * 8 + g : tile * 16 + g;         // gate row / first W2 row
-  const int rowB = W13 ? 64 + tile * 8 + g : tile * 16 + g + 8; // up row / second W2 row
-  // swizzled byte offsets of this thread's 4 packed bytes, per 16-byte chunk
+  const int rowA = W13 ? tile * 8 + g : tile * 16 + g;  // gate row / first W2 row; row B: the
+  // matching up row 64 rows on (W13) or the row 8 rows on (W2).  Both rows have the
+  // same 128-byte swizzle phase (g), so row B's bytes sit a fixed distance after
+  // row A's: the up half of the stage (W13) or 8 rows of 128 bytes (W2).
+  constexpr uint32_t kDeltaB = W13 ? 16384 : 8 * 128;
+  constexpr uint32_t kDeltaS = W13 ? 64 * 16 : 8 * 16;  // the same for the scale rows
+  // packed boxes: K 0..255 and 256..511, each 128 rows (W2) or 2 x 64 rows (W13)
   const int box_stride = W13 ? 8192 : 16384;
-  const int ra = W13 ? rowA & 63 : rowA, rbw = W13 ? rowB & 63 : rowB;
-  const int baseA = (W13 ? (rowA >> 6) * 16384 : 0) + ra * 128 + 4 * t;
-  const int baseB = (W13 ? (rowB >> 6) * 16384 : 0) + rbw * 128 + 4 * t;
-  const int swA_ = ra & 7, swB_ = rbw & 7;
+  const int ra = W13 ? rowA & 63 : rowA;
+  const int baseA = ra * 128 + 4 * t;
+  // 32-bit shared addresses; per block of this warp's share, the swizzled offset
+  // of this thread's 4 packed bytes of row A inside a stage
+  const uint32_t ring_s = smem_u32(ring), xs_s = smem_u32(xs_buf);
+  const uint32_t sofA = kStageA + rowA * 16 + kpart * kBlkPerWarp;
+  uint32_t offA[kBlkPerWarp];
+#pragma unroll
+  for (int bi = 0; bi < kBlkPerWarp; ++bi) {
+    const int blk = kpart * kBlkPerWarp + bi;
+    offA[bi] = baseA + (blk >> 3) * box_stride + (((blk & 7) ^ (ra & 7)) << 4);
+  }
   int cur = -1, row0 = 0, mt = 0;
   int& slot = R.slot;
   int& rbuf = R.rbuf;
@@ -303,45 +337,40 @@ __device__ __forceinline__ void stream_consume(const StreamParams& P, const Stre
     // mma.sync below always sees all 32 lanes
     const bool run = !*abort_flag;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    const uint8_t* xg = xs_buf + (size_t)g * P.x_pitch + 16 * t;  // token g, this thread's 8 elements
+    const uint32_t xk0 = xs_s + g * P.x_pitch + 16 * t + kpart * kBlkPerWarp * 64;
     for (int ks = 0; ks < nst; ++ks) {
       if (run) mbar_wait(&full[slot], phase, abort_flag, P.err, kErrWaitTimeout, P.wait_ns);
       {
-        const uint8_t* st = ring + (size_t)slot * kStageBytes;
-        // packed rows: two 128-byte-swizzled boxes (K 0..255, 256..511) of 128 (or 2 x 64) rows
-        const uint8_t* pa = st + baseA;
-        const uint8_t* pb = st + baseB;
-        // this warp's blocks [kpart * kBlkPerWarp, +kBlkPerWarp) of the stage's 16
-        // the E8M0 bytes of this warp's blocks, one per register
+        const uint32_t st = ring_s + slot * kStageBytes;
+        // the E8M0 bytes of this warp's blocks [kpart * kBlkPerWarp, +kBlkPerWarp), one per register
         uint32_t sbA[kBlkPerWarp], sbB[kBlkPerWarp];
 #pragma unroll
         for (int i = 0; i < kBlkPerWarp / 4; ++i) {
           uint32_t ta[4], tb[4];
-          lds_bytes4(st + kStageA + rowA * 16 + kpart * kBlkPerWarp + 4 * i, ta);
-          lds_bytes4(st + kStageA + rowB * 16 + kpart * kBlkPerWarp + 4 * i, tb);
+          lds_bytes4(st + sofA + 4 * i, ta);
+          lds_bytes4(st + sofA + kDeltaS + 4 * i, tb);
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             sbA[4 * i + j] = ta[j];
             sbB[4 * i + j] = tb[j];
           }
         }
-        const uint8_t* xk = xg + (size_t)ks * kKStage * 2 + kpart * kBlkPerWarp * 64;
+        const uint32_t xk = xk0 + ks * kKStage * 2;
 #pragma unroll
         for (int bi = 0; bi < kBlkPerWarp; ++bi) {
-          const int blk = kpart * kBlkPerWarp + bi;  // uniform over the warp
-          const int half = blk >> 3, chunk = blk & 7;
-          uint32_t ba[4], bb[4];  // this thread's 4 packed bytes of rows A and B (8 codes each)
-          lds_bytes4(pa + half * box_stride + ((chunk ^ swA_) << 4), ba);
-          lds_bytes4(pb + half * box_stride + ((chunk ^ swB_) << 4), bb);
-          const uint4 xf = *reinterpret_cast<const uint4*>(xk + bi * 64);
+          uint32_t ha[4], hb[4];  // this thread's 8 codes of rows A and B as f16 pairs
+          const uint32_t pa = st + offA[bi];
+          e2m1x8_f16(lds_u32(pa), ha);
+          e2m1x8_f16(lds_u32(pa + kDeltaB), hb);
+          const uint4 xf = lds_u128(xk + bi * 64);
           const float zero[4] = {0.f, 0.f, 0.f, 0.f};
           float cb[4];
-          uint32_t a[4] = {e2m1x2_h2(ba[0]), e2m1x2_h2(bb[0]), e2m1x2_h2(ba[1]), e2m1x2_h2(bb[1])};
+          uint32_t a[4] = {ha[0], hb[0], ha[1], hb[1]};
           mma_16816(cb, a, xf.x, xf.y, zero);
-          a[0] = e2m1x2_h2(ba[2]);
-          a[1] = e2m1x2_h2(bb[2]);
-          a[2] = e2m1x2_h2(ba[3]);
-          a[3] = e2m1x2_h2(bb[3]);
+          a[0] = ha[2];
+          a[1] = hb[2];
+          a[2] = ha[3];
+          a[3] = hb[3];
           mma_16816(cb, a, xf.z, xf.w, cb);
           const float fa = scale2_of(sbA[bi]), fb = scale2_of(sbB[bi]);
           acc[0] = fmaf(cb[0], fa, acc[0]);
