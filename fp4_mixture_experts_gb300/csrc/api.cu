@@ -28,6 +28,18 @@ bool dims_supported(const moe_fp4_dims& d) {
 
 bool aligned(const void* p, size_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
 
+// The address of host memory p on the current device, if the device can
+// address it (page-locked memory from the CUDA allocator or registered with
+// it), else null.
+void* device_view(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();  // unregistered memory may report an error on older drivers: not sticky
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
 }  // namespace
 
 bool layout_workspace(const moe_fp4_dims& d, void* base, bool with_staging, Workspace* ws, bool mx) {
@@ -279,15 +291,26 @@ int moe_fp4_forward_host(const moe_fp4_dims* dims, const void* x_bf16_host, cons
   if ((flags & MOE_FP4_FLAG_FORCE_GEMV) && (d.d % 1024 != 0 || d.I % 1024 != 0)) return MOE_FP4_ERR_UNSUPPORTED;
   if (workspace_bytes < ws.total) return MOE_FP4_ERR_WORKSPACE;
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  // Host buffers the device can address (pinned or registered memory) are
+  // used in place: the routing kernel reads the logits, the combine writes
+  // out, with no copy and no copy-engine round trip.  x, which many CTAs read
+  // again, is copied to device staging; so is anything else.
+  const float* logits_dev = static_cast<const float*>(device_view(router_logits_host));
+  float* out_dev = static_cast<float*>(device_view(out_host));
+  if (logits_dev && !aligned(logits_dev, 4)) logits_dev = nullptr;
+  if (out_dev && !aligned(out_dev, 16)) out_dev = nullptr;
   const size_t xb = (size_t)d.T * d.d * sizeof(uint16_t), lb = (size_t)d.T * d.E * sizeof(float),
                ob = (size_t)d.T * d.d * sizeof(float);
-  if (cudaMemcpyAsync(ws.stage_x, x_bf16_host, xb, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+  if (cudaMemcpyAsync(ws.stage_x, x_bf16_host, xb, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return MOE_FP4_ERR_CUDA;
+  if (!logits_dev &&
       cudaMemcpyAsync(ws.stage_logits, router_logits_host, lb, cudaMemcpyHostToDevice, st) != cudaSuccess)
     return MOE_FP4_ERR_CUDA;
-  int rc = run_forward(d, ws.stage_x, ws.stage_logits, w13, w13_scale, w2, w2_scale, ws.stage_out, nullptr,
-                       nullptr, nullptr, nullptr, nullptr, flags, ws, st);
+  int rc = run_forward(d, ws.stage_x, logits_dev ? logits_dev : ws.stage_logits, w13, w13_scale, w2, w2_scale,
+                       out_dev ? out_dev : ws.stage_out, nullptr, nullptr, nullptr, nullptr, nullptr, flags, ws, st);
   if (rc != MOE_FP4_OK) return rc;
-  if (cudaMemcpyAsync(out_host, ws.stage_out, ob, cudaMemcpyDeviceToHost, st) != cudaSuccess) return MOE_FP4_ERR_CUDA;
+  if (!out_dev && cudaMemcpyAsync(out_host, ws.stage_out, ob, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MOE_FP4_ERR_CUDA;
   return cudaStreamSynchronize(st) == cudaSuccess ? MOE_FP4_OK : MOE_FP4_ERR_CUDA;
 }
 

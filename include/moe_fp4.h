@@ -189,9 +189,13 @@ int moe_fp4_forward_profiled(const moe_fp4_dims* dims, const void* x_bf16, const
 size_t moe_fp4_host_workspace_bytes(const moe_fp4_dims* dims);
 
 /* The whole layer with HOST x, router_logits and out (weights stay on the
- * device).  Copies x and the logits to device staging inside the workspace,
- * runs moe_fp4_forward, copies out back and synchronises the stream before
- * returning.  Host buffers may be pageable or pinned (pinned is faster). */
+ * device).  Copies x to device staging inside the workspace, runs
+ * moe_fp4_forward and synchronises the stream before returning.  Host buffers
+ * may be pageable or pinned (pinned is faster).  router_logits and out in
+ * memory the device can address (page-locked by the CUDA allocator or
+ * registered with it; out 16-byte aligned) are used in place: the routing
+ * kernel reads the logits and the combine writes out over the host link, with
+ * no copy.  Otherwise they go through device staging too. */
 int moe_fp4_forward_host(const moe_fp4_dims* dims, const void* x_bf16_host,
                          const float* router_logits_host,
                          const uint8_t* w13, const uint8_t* w13_scale,

@@ -211,6 +211,16 @@ def test_forward_host_matches_forward(moe):
     host_out = moe.forward_host(xh, lh, D["w13"], D["w13_scale"], D["w2"], D["w2_scale"], L.k)
     torch.cuda.synchronize()
     assert np.array_equal(host_out.numpy(), dev_out.cpu().numpy())
+    # pinned logits and out are used in place, pageable ones go through device staging: the
+    # same result either way, and for each mix of the two
+    xp = torch.from_numpy(L.x_bf16.view(np.int16).copy()).view(torch.bfloat16)
+    lp = torch.from_numpy(L.router_logits.copy())
+    for x_, l_, pinned_out in ((xp, lp, False), (xh, lp, True), (xp, lh, False), (xh, lh, True)):
+        o_ = torch.full((L.T, L.d), float("nan"), dtype=torch.float32)
+        if pinned_out:
+            o_ = o_.pin_memory()
+        moe.forward_host(x_, l_, D["w13"], D["w13_scale"], D["w2"], D["w2_scale"], L.k, out_host=o_)
+        assert np.array_equal(o_.numpy(), dev_out.cpu().numpy())
 
 
 def test_check_reports_clean_workspace(moe):
