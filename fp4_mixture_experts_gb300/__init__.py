@@ -8,11 +8,11 @@ Importing the package does not need a GPU; calling a compute function
 without the built library raises.
 """
 from ._binding import (EXPORTED_SYMBOLS, FAULT_NONE, FAULT_STREAM_STAGE, FAULT_TC_TOKEN_TILE, FLAG_FORCE_GEMV,
-                       FLAG_CTA_PAIRS, FLAG_FORCE_TC, FLAG_PERSISTENT, Dims, MoeFp4Error, check, forward, forward_gated, forward_host, forward_mx,
+                       FLAG_CTA_PAIRS, FLAG_DETERMINISTIC, FLAG_FORCE_TC, FLAG_PERSISTENT, Dims, MoeFp4Error, check, forward, forward_gated, forward_host, forward_mx,
                        forward_noalloc, host_workspace_bytes, mx_workspace_bytes, lib_path, load_library, mxfp8_quantize, noalloc_check, route, router,
                        set_fault_injection, status_string, workspace_bytes)
 
 __all__ = ["EXPORTED_SYMBOLS", "FAULT_NONE", "FAULT_STREAM_STAGE", "FAULT_TC_TOKEN_TILE", "FLAG_FORCE_GEMV",
-           "FLAG_CTA_PAIRS", "FLAG_FORCE_TC", "FLAG_PERSISTENT", "Dims", "MoeFp4Error", "check", "forward", "forward_gated", "forward_host", "forward_mx",
+           "FLAG_CTA_PAIRS", "FLAG_DETERMINISTIC", "FLAG_FORCE_TC", "FLAG_PERSISTENT", "Dims", "MoeFp4Error", "check", "forward", "forward_gated", "forward_host", "forward_mx",
            "forward_noalloc", "host_workspace_bytes", "mx_workspace_bytes", "lib_path", "load_library", "mxfp8_quantize", "noalloc_check", "route", "router",
            "set_fault_injection", "status_string", "workspace_bytes"]

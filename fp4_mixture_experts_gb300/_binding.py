@@ -16,6 +16,7 @@ FLAG_FORCE_GEMV = 0x1
 FLAG_FORCE_TC = 0x2
 FLAG_PERSISTENT = 0x4
 FLAG_CTA_PAIRS = 0x8
+FLAG_DETERMINISTIC = 0x10
 
 FAULT_NONE = 0
 FAULT_TC_TOKEN_TILE = 1

@@ -115,20 +115,28 @@ int run_forward(const moe_fp4_dims& d, const void* x, const float* logits, const
   if (sorted_slot) ws.sorted_slot = sorted_slot;
   if (h) ws.h = static_cast<uint16_t*>(h);
   const uint16_t* xb = static_cast<const uint16_t*>(x);
+  const bool det = (flags & MOE_FP4_FLAG_DETERMINISTIC) != 0;
+  const size_t out_bytes = (size_t)d.T * d.d * sizeof(float);
+  const bool gemv = use_gemv_path(d, flags);
+  // the combine in the W2 epilogue (atomic adds into out): the streaming
+  // kernels and the one-SM tensor-core kernel, unless reproducibility is asked
+  const bool stream_combine = !det && gemv && stream_path_supported(d);
   mark(0);
+  // on the streaming path the W13 kernel zeroes out while it waits for the routing
   cudaError_t e = launch_route(d, logits, ws, st);
   if (e != cudaSuccess) return MOE_FP4_ERR_CUDA;
   mark(1);
   bool fused_combine = false;
-  if (use_gemv_path(d, flags)) {
+  if (gemv) {
     mark(2);
     if (stream_path_supported(d) && (flags & MOE_FP4_FLAG_PERSISTENT)) {
-      e = launch_stream_fused(d, xb, w13, w13s, w2, w2s, ws, st);  // both projections: the W2 stage reads 0
+      // both projections: the W2 stage reads 0
+      e = launch_stream_fused(d, xb, w13, w13s, w2, w2s, ws, stream_combine ? out : nullptr, st);
       mark(3);
     } else if (stream_path_supported(d)) {
-      e = launch_stream_w13(d, xb, w13, w13s, ws, st);
+      e = launch_stream_w13(d, xb, w13, w13s, ws, stream_combine ? out : nullptr, st);
       mark(3);
-      if (e == cudaSuccess) e = launch_stream_w2(d, w2, w2s, ws, st);
+      if (e == cudaSuccess) e = launch_stream_w2(d, w2, w2s, ws, stream_combine ? out : nullptr, st);
     } else {
       e = launch_gemv_w13(d, xb, w13, w13s, ws, st);
       mark(3);
@@ -140,19 +148,21 @@ int run_forward(const moe_fp4_dims& d, const void* x, const float* logits, const
     const bool pairs = (flags & MOE_FP4_FLAG_CTA_PAIRS) != 0;
     if (e == cudaSuccess) e = launch_tc_w13(d, w13, w13s, ws, pairs, st);
     mark(3);
+    const bool tc_combine = !det && !pairs;
     if (e == cudaSuccess) e = launch_h_f16(d, ws, st);  // counted in the W2 stage
-    if (e == cudaSuccess) e = launch_tc_w2(d, w2, w2s, ws, out, pairs, st);
-    fused_combine = tc_fused_combine(pairs);
+    if (e == cudaSuccess && tc_combine) e = cudaMemsetAsync(out, 0, out_bytes, st);
+    if (e == cudaSuccess) e = launch_tc_w2(d, w2, w2s, ws, out, pairs, tc_combine, st);
+    fused_combine = tc_combine || tc_fused_combine(pairs);
   }
   mark(4);
-  if (e == cudaSuccess && !fused_combine) e = launch_combine(d, out, ws, st);
+  if (e == cudaSuccess && !fused_combine && !stream_combine) e = launch_combine(d, out, ws, st);
   mark(5);
   return e == cudaSuccess ? MOE_FP4_OK : MOE_FP4_ERR_CUDA;
 }
 
 int check_flags(unsigned flags) {
-  const unsigned known =
-      MOE_FP4_FLAG_FORCE_GEMV | MOE_FP4_FLAG_FORCE_TC | MOE_FP4_FLAG_PERSISTENT | MOE_FP4_FLAG_CTA_PAIRS;
+  const unsigned known = MOE_FP4_FLAG_FORCE_GEMV | MOE_FP4_FLAG_FORCE_TC | MOE_FP4_FLAG_PERSISTENT |
+                         MOE_FP4_FLAG_CTA_PAIRS | MOE_FP4_FLAG_DETERMINISTIC;
   if (flags & ~known) return MOE_FP4_ERR_INVALID_ARG;
   if ((flags & MOE_FP4_FLAG_FORCE_GEMV) && (flags & MOE_FP4_FLAG_FORCE_TC)) return MOE_FP4_ERR_INVALID_ARG;
   return MOE_FP4_OK;
@@ -299,6 +309,9 @@ int moe_fp4_forward_host(const moe_fp4_dims* dims, const void* x_bf16_host, cons
   float* out_dev = static_cast<float*>(device_view(out_host));
   if (logits_dev && !aligned(logits_dev, 4)) logits_dev = nullptr;
   if (out_dev && !aligned(out_dev, 16)) out_dev = nullptr;
+  // out in host memory is written by the combine pass with plain stores (no
+  // atomic adds across the host link)
+  if (out_dev) flags |= MOE_FP4_FLAG_DETERMINISTIC;
   const size_t xb = (size_t)d.T * d.d * sizeof(uint16_t), lb = (size_t)d.T * d.E * sizeof(float),
                ob = (size_t)d.T * d.d * sizeof(float);
   if (cudaMemcpyAsync(ws.stage_x, x_bf16_host, xb, cudaMemcpyHostToDevice, st) != cudaSuccess)

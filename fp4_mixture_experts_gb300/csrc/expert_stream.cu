@@ -62,6 +62,10 @@ struct StreamParams {
   int32_t* err;
   uint16_t* h_out;         // W13: h [S, I]
   float* y_out;            // W2: y [S, d]
+  float* out;              // W2, non-null: out [T, d] += w * y row by row (fp32 atomic adds), no y
+  float4* zero;            // W13, non-null: out, zeroed by this kernel before the W2 kernel adds into it
+  long long zero_n4;       // its length in float4
+  const float* topk_w;     // routing weights by slot (with out)
   int k, d, I;
   int K;                   // reduction length: d (W13) or I (W2)
   int n_rb;                // row blocks per expert
@@ -150,6 +154,8 @@ struct StreamSmem {
   uint8_t* xs_buf;         // [8 tokens][x_pitch] f16 activations of the current chunk
   float4* red;             // [2][kKSplit-1][8 tiles][32] partial sums of the K split
   float* tok_scale;        // [8]
+  int* tok_row;            // [8] W2 with out: token of each chunk row
+  float* tok_w;            // [8] W2 with out: routing weight of each chunk row
   uint64_t* full;          // [stages]
   uint64_t* empty;         // [stages]
   volatile int* abort_flag;
@@ -162,7 +168,9 @@ __device__ __forceinline__ StreamSmem stream_smem(uint8_t* smem_raw, int stages,
   S.xs_buf = S.ring + (size_t)stages * kStageBytes;
   S.red = reinterpret_cast<float4*>(S.xs_buf + (size_t)kMaxTok * x_pitch);
   S.tok_scale = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(S.red) + kRedBytes);
-  S.full = reinterpret_cast<uint64_t*>(S.tok_scale + kMaxTok);
+  S.tok_row = reinterpret_cast<int*>(S.tok_scale + kMaxTok);
+  S.tok_w = reinterpret_cast<float*>(S.tok_row + kMaxTok);
+  S.full = reinterpret_cast<uint64_t*>(S.tok_w + kMaxTok);
   S.empty = S.full + stages;
   S.abort_flag = reinterpret_cast<volatile int*>(S.empty + stages);
   return S;
@@ -324,7 +332,14 @@ __device__ __forceinline__ void stream_consume(const StreamParams& P, const Stre
           }
           reinterpret_cast<uint4*>(xrow)[v] = make_uint4(o[0], o[1], o[2], o[3]);
         }
-        if (lane == 0) tok_scale[warp] = pow2f(-shift - 1);  // 2^-shift / 2 (scale2_of carries a factor 2)
+        if (lane == 0) {
+          tok_scale[warp] = pow2f(-shift - 1);  // 2^-shift / 2 (scale2_of carries a factor 2)
+          if (!W13 && P.out) {
+            const int slot = P.sorted_slot[row0 + warp];
+            S.tok_row[warp] = slot / P.k;
+            S.tok_w[warp] = P.topk_w[slot];
+          }
+        }
       } else {
         for (int v = lane; v < P.K / 8; v += 32) reinterpret_cast<uint4*>(xrow)[v] = make_uint4(0, 0, 0, 0);
         if (lane == 0) tok_scale[warp] = 0.f;
@@ -419,6 +434,21 @@ __device__ __forceinline__ void stream_consume(const StreamParams& P, const Stre
       const int i = rb * 64 + tile * 8 + g;
       if (t0 < mt) P.h_out[(size_t)(row0 + t0) * P.I + i] = f32_to_bf16_rn(swiglu(acc[0] * s0, acc[2] * s0));
       if (t1 < mt) P.h_out[(size_t)(row0 + t1) * P.I + i] = f32_to_bf16_rn(swiglu(acc[1] * s1, acc[3] * s1));
+    } else if (P.out) {
+      // the weighted combine: each slot's row added into its token's out row
+      const int n = rb * 128 + tile * 16 + g;
+      if (t0 < mt) {
+        float* o = P.out + (size_t)S.tok_row[t0] * P.d + n;
+        const float w = S.tok_w[t0];
+        red_add_f32(o, w * (acc[0] * s0));
+        red_add_f32(o + 8, w * (acc[2] * s0));
+      }
+      if (t1 < mt) {
+        float* o = P.out + (size_t)S.tok_row[t1] * P.d + n;
+        const float w = S.tok_w[t1];
+        red_add_f32(o, w * (acc[1] * s1));
+        red_add_f32(o + 8, w * (acc[3] * s1));
+      }
     } else {
       const int n = rb * 128 + tile * 16 + g;
       if (t0 < mt) {
@@ -445,6 +475,11 @@ stream_kernel(const __grid_constant__ CUtensorMap map_w, const __grid_constant__
   // that wait, so the work list is complete, and it reads it through L2
   // (ld.global.cg) so that its producer can stream weights while W13 ends;
   // its consumers wait for W13 (h) below.
+  // out is zeroed while the routing kernel still runs (nothing of this call
+  // reads or writes it before the W2 kernel, which waits for this one)
+  if (W13 && P.zero)
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < P.zero_n4; i += (long long)gridDim.x * blockDim.x)
+      P.zero[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   if (W13) griddep_wait();
   griddep_launch_dependents();
   if ((threadIdx.x >> 5) == kConsWarps) {
@@ -473,6 +508,11 @@ stream_fused_kernel(const __grid_constant__ CUtensorMap map_w13, const __grid_co
                     const StreamParams P13, const StreamParams P2, int32_t* arrivals) {
   extern __shared__ uint8_t smem_raw[];
   const StreamSmem S = stream_smem(smem_raw, P13.stages, P13.x_pitch);
+  // out is zeroed before the W2 phase adds into it (the grid-wide barrier
+  // between the phases orders the two)
+  if (P13.zero)
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < P13.zero_n4; i += (long long)gridDim.x * blockDim.x)
+      P13.zero[i] = make_float4(0.f, 0.f, 0.f, 0.f);
   stream_init(S, P13.stages);
   griddep_launch_dependents();
   if ((threadIdx.x >> 5) == kConsWarps) {
@@ -511,7 +551,7 @@ stream_fused_kernel(const __grid_constant__ CUtensorMap map_w13, const __grid_co
 
 size_t smem_needed(int stages, int x_pitch) {
   return 1024 /* alignment slack */ + (size_t)stages * kStageBytes + (size_t)kMaxTok * x_pitch + kRedBytes +
-         kMaxTok * sizeof(float) + 2 * stages * sizeof(uint64_t) + 16;
+         3 * kMaxTok * sizeof(float) + 2 * stages * sizeof(uint64_t) + 16;
 }
 
 template <bool W13>
@@ -560,8 +600,10 @@ StreamParams params_w13(const moe_fp4_dims& d, const uint16_t* x, const Workspac
   return P;
 }
 
-StreamParams params_w2(const moe_fp4_dims& d, const Workspace& ws) {
+StreamParams params_w2(const moe_fp4_dims& d, const Workspace& ws, float* out) {
   StreamParams P{};
+  P.out = out;
+  P.topk_w = ws.topk_w;
   P.chunks = ws.gemv_chunks;
   P.counts = ws.counts;
   P.sorted_slot = ws.sorted_slot;
@@ -587,24 +629,30 @@ bool stream_path_supported(const moe_fp4_dims& d) {
 }
 
 cudaError_t launch_stream_w13(const moe_fp4_dims& d, const uint16_t* x, const uint8_t* w13, const uint8_t* w13s,
-                              const Workspace& ws, cudaStream_t st) {
+                              const Workspace& ws, float* zero_out, cudaStream_t st) {
   CUtensorMap mw, ms;
   if (!maps_w13(d, w13, w13s, &mw, &ms)) return cudaErrorInvalidValue;
-  return launch_stream<true>(mw, ms, params_w13(d, x, ws), st);
+  StreamParams P = params_w13(d, x, ws);
+  P.zero = reinterpret_cast<float4*>(zero_out);
+  P.zero_n4 = (long long)d.T * d.d / 4;
+  return launch_stream<true>(mw, ms, P, st);
 }
 
 cudaError_t launch_stream_w2(const moe_fp4_dims& d, const uint8_t* w2, const uint8_t* w2s, const Workspace& ws,
-                             cudaStream_t st) {
+                             float* out, cudaStream_t st) {
   CUtensorMap mw, ms;
   if (!maps_w2(d, w2, w2s, &mw, &ms)) return cudaErrorInvalidValue;
-  return launch_stream<false>(mw, ms, params_w2(d, ws), st);
+  return launch_stream<false>(mw, ms, params_w2(d, ws, out), st);
 }
 
 cudaError_t launch_stream_fused(const moe_fp4_dims& d, const uint16_t* x, const uint8_t* w13, const uint8_t* w13s,
-                                const uint8_t* w2, const uint8_t* w2s, const Workspace& ws, cudaStream_t st) {
+                                const uint8_t* w2, const uint8_t* w2s, const Workspace& ws, float* out,
+                                cudaStream_t st) {
   CUtensorMap mw13, ms13, mw2, ms2;
   if (!maps_w13(d, w13, w13s, &mw13, &ms13) || !maps_w2(d, w2, w2s, &mw2, &ms2)) return cudaErrorInvalidValue;
-  StreamParams P13 = params_w13(d, x, ws), P2 = params_w2(d, ws);
+  StreamParams P13 = params_w13(d, x, ws), P2 = params_w2(d, ws, out);
+  P13.zero = reinterpret_cast<float4*>(out);
+  P13.zero_n4 = (long long)d.T * d.d / 4;
   // one shared-memory layout for both phases: the wider activation rows
   const int x_pitch = (d.d > d.I ? d.d : d.I) * 2 + 64;
   int stages = 4;

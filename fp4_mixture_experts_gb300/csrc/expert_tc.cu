@@ -476,11 +476,20 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
       constexpr int kChunks = (kBN + 63) / 64;
       const int half = dq >> 2;
       float xs_pre[kChunks] = {};
+      float wt_pre[kChunks] = {};  // W2 with the combine: routing weight and token of each column
+      int tk_pre[kChunks] = {};
       {
 #pragma unroll
         for (int i = 0; i < kChunks; ++i) {
           const int col = 32 * (2 * i + half) + lane;
-          if (col < t.n) xs_pre[i] = P.x_scale[t.row0 + col];
+          if (col < t.n) {
+            xs_pre[i] = P.x_scale[t.row0 + col];
+            if (!W13 && P.out) {
+              const int slot = P.sorted_slot[t.row0 + col];
+              wt_pre[i] = P.topk_w[slot];
+              tk_pre[i] = slot / P.k;
+            }
+          }
         }
       }
       // the row scales written above must be visible to every epilogue warp
@@ -524,7 +533,21 @@ tc_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUt
               const float o0 = __shfl_xor_sync(0xFFFFFFFFu, odd ? p0 : q0, 1);
               const float o1 = __shfl_xor_sync(0xFFFFFFFFu, odd ? p1 : q1, 1);
               const int jj = j + (odd ? 1 : 0);
-              if (c0 + jj < t.n) {
+              if (P.out) {
+                // the weighted combine: the pair of features of token column jj
+                // added into that token's out row
+                const float wj = __shfl_sync(0xFFFFFFFFu, wt_pre[ci], jj);
+                const int tj = __shfl_sync(0xFFFFFFFFu, tk_pre[ci], jj);
+                if (c0 + jj < t.n) {
+                  float* orow = P.out + (size_t)tj * P.d + nrow;
+                  const float2 v0 = odd ? make_float2(o0, q0) : make_float2(p0, o0);
+                  red_add_v2_f32(orow, wj * v0.x, wj * v0.y);
+                  if (second_in) {
+                    const float2 v1 = odd ? make_float2(o1, q1) : make_float2(p1, o1);
+                    red_add_v2_f32(orow + P.acc1_offset, wj * v1.x, wj * v1.y);
+                  }
+                }
+              } else if (c0 + jj < t.n) {
                 float* yrow = P.y_out + (size_t)(t.row0 + c0 + jj) * P.d + nrow;
                 *reinterpret_cast<float2*>(yrow) = odd ? make_float2(o0, q0) : make_float2(p0, o0);
                 if (second_in)
@@ -627,7 +650,7 @@ cudaError_t launch_tc_w13(const moe_fp4_dims& d, const uint8_t* w13, const uint8
 bool tc_fused_combine(bool pairs) { return pairs && kFusedCombine; }
 
 cudaError_t launch_tc_w2(const moe_fp4_dims& d, const uint8_t* w2, const uint8_t* w2s, const Workspace& ws,
-                         float* out, bool pairs, cudaStream_t st) {
+                         float* out, bool pairs, bool atomic_combine, cudaStream_t st) {
   const size_t S = (size_t)d.T * d.k;
   CUtensorMap b, raw;
   if (!make_map_2d(&raw, CU_TENSOR_MAP_DATA_TYPE_UINT8, w2, d.I / 2, (uint64_t)d.E * d.d, d.I / 2, kRawRowBytes, kBM,
@@ -670,6 +693,12 @@ cudaError_t launch_tc_w2(const moe_fp4_dims& d, const uint8_t* w2, const uint8_t
   P.mblocks = (d.d + 2 * kBM - 1) / (2 * kBM);  // d % 256 == 128 leaves a 128-row last block
   P.block_rows = 2 * kBM;
   P.acc1_offset = kBM;
+  if (atomic_combine) {
+    P.out = out;
+    P.topk_w = ws.topk_w;
+    P.sorted_slot = ws.sorted_slot;
+    P.k = d.k;
+  }
   return launch_tc<false>(b, raw, P, ws.max_tc_tiles, st);
 }
 

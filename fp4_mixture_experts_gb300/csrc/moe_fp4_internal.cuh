@@ -108,16 +108,21 @@ cudaError_t launch_gemv_w13(const moe_fp4_dims& d, const uint16_t* x, const uint
 cudaError_t launch_gemv_w2(const moe_fp4_dims& d, const uint8_t* w2, const uint8_t* w2s,
                            const Workspace& ws, cudaStream_t st);
 bool stream_path_supported(const moe_fp4_dims& d);
+// zero_out non-null: the kernel zeroes out (T x d fp32) for the W2 kernel's combine
 cudaError_t launch_stream_w13(const moe_fp4_dims& d, const uint16_t* x, const uint8_t* w13, const uint8_t* w13s,
-                              const Workspace& ws, cudaStream_t st);
+                              const Workspace& ws, float* zero_out, cudaStream_t st);
+// out non-null: the W2 epilogue adds each slot's weighted row into out (zeroed
+// beforehand) instead of writing y for the combine kernel
 cudaError_t launch_stream_w2(const moe_fp4_dims& d, const uint8_t* w2, const uint8_t* w2s, const Workspace& ws,
-                             cudaStream_t st);
+                             float* out, cudaStream_t st);
 cudaError_t launch_stream_fused(const moe_fp4_dims& d, const uint16_t* x, const uint8_t* w13, const uint8_t* w13s,
-                                const uint8_t* w2, const uint8_t* w2s, const Workspace& ws, cudaStream_t st);
+                                const uint8_t* w2, const uint8_t* w2s, const Workspace& ws, float* out,
+                                cudaStream_t st);
 cudaError_t launch_tc_w13(const moe_fp4_dims& d, const uint8_t* w13, const uint8_t* w13s, const Workspace& ws,
                           bool pairs, cudaStream_t st);
+// one-SM kernel: out non-null as for launch_stream_w2; CTA pairs: see tc_fused_combine
 cudaError_t launch_tc_w2(const moe_fp4_dims& d, const uint8_t* w2, const uint8_t* w2s, const Workspace& ws,
-                         float* out, bool pairs, cudaStream_t st);
+                         float* out, bool pairs, bool atomic_combine, cudaStream_t st);
 cudaError_t launch_combine(const moe_fp4_dims& d, float* out, const Workspace& ws, cudaStream_t st);
 // true: the tensor-core W2 kernel writes out itself (the weighted combine in
 // its epilogue; the CTA-pair kernel does)
@@ -154,6 +159,17 @@ __device__ __forceinline__ float e8m0_to_f32(uint32_t s) {
 
 // bf16 bits -> fp32
 __device__ __forceinline__ float bf16_to_f32(uint32_t b16) { return __uint_as_float(b16 << 16); }
+
+// out[i] += v in global memory, no return value (fp32 reduction at L2); the
+// order of concurrent additions is not fixed.
+__device__ __forceinline__ void red_add_f32(float* p, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+
+// The same for two adjacent floats (p 8-byte aligned).
+__device__ __forceinline__ void red_add_v2_f32(float* p, float a, float b) {
+  asm volatile("red.global.add.v2.f32 [%0], {%1, %2};" ::"l"(p), "f"(a), "f"(b) : "memory");
+}
 
 // fp32 -> bf16 bits, round to nearest even (the CUDA intrinsic).
 __device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {

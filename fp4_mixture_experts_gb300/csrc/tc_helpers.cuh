@@ -35,9 +35,11 @@ struct TcParams {
   // expert * rows_per_expert + a * acc_row_off + index; indices at or beyond
   // limit are not written
   int cta_rows, acc_idx_step, acc_row_off, limit;
-  // CTA pairs, W2 with the combine in the epilogue (out != nullptr): out[t] =
+  // W2 with the combine in the epilogue (out != nullptr).  CTA pairs: out[t] =
   // sum_j topk_w[t, j] * y[slot_pos[t k + j]] for each 256-feature block,
-  // written by the CTA whose item brings the block's last slot (counters)
+  // written by the CTA whose item brings the block's last slot (counters).
+  // One-SM kernel: each slot's weighted row added into out (zeroed
+  // beforehand) with fp32 atomic adds, no y.
   float* out;
   const float* topk_w;
   const int32_t* sorted_slot;

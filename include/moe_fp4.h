@@ -112,6 +112,16 @@ typedef enum moe_fp4_status {
  * the pair's MMAs read both SMs' tensor memory).  Ignored on the streaming
  * path. */
 #define MOE_FP4_FLAG_CTA_PAIRS 0x8u
+/* The weighted combine.  By default the W2 kernel adds each slot's weighted
+ * output row into out in its epilogue (fp32 atomic adds, out zeroed first):
+ * no y buffer round trip and no separate pass, but the k terms of an output
+ * element are summed in whatever order the slots finish, so results may
+ * differ in the last bits between calls.  With this flag the W2 kernel writes
+ * y and a separate pass sums the k rows of each token in slot order:
+ * bitwise reproducible.  CTA pairs always use their own in-epilogue combine in
+ * slot order (reproducible); the fallback paths for sizes outside the
+ * streaming kernel's use the separate pass. */
+#define MOE_FP4_FLAG_DETERMINISTIC 0x10u
 
 /* Bytes of device workspace a call with these sizes needs (256-byte aligned
  * base required).  Returns 0 when the sizes are invalid or unsupported:

@@ -20,7 +20,7 @@ from _layer_util import to_device
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
-GEMV, TC = 0x1, 0x2
+GEMV, TC, DET = 0x1, 0x2, 0x10
 SCRATCH = 16 * 1024 * 1024
 
 
@@ -57,7 +57,7 @@ def _compare(moe, L, flags, what):
     assert torch.equal(out, ref), f"{what}: noalloc differs from forward"
 
 
-@pytest.mark.parametrize("flags", [GEMV, TC])
+@pytest.mark.parametrize("flags", [GEMV | DET, TC | DET])
 def test_noalloc_matches_forward_twice(moe, flags):
     for seed in (21, 22):
         _compare(moe, make_layer(T=32, d=1024, I=1024, E=32, k=4, seed=seed), flags, f"flags {flags} seed {seed}")
@@ -66,8 +66,8 @@ def test_noalloc_matches_forward_twice(moe, flags):
 def test_noalloc_tensor_core_call_after_streaming_call(moe):
     # the tensor-core path reads regions of the shared scratch (64-row token
     # boxes, the f16 copy of h) that a streaming call before it left dirty
-    _compare(moe, make_layer(T=40, d=1024, I=1024, E=16, k=4, seed=23), GEMV, "streaming")
-    _compare(moe, make_layer(T=96, d=1024, I=1024, E=4, k=2, seed=24), TC, "tensor-core after streaming")
+    _compare(moe, make_layer(T=40, d=1024, I=1024, E=16, k=4, seed=23), GEMV | DET, "streaming")
+    _compare(moe, make_layer(T=96, d=1024, I=1024, E=4, k=2, seed=24), TC | DET, "tensor-core after streaming")
 
 
 def _largest_T(moe, d, I, E, k):
@@ -80,7 +80,7 @@ def _largest_T(moe, d, I, E, k):
 def test_noalloc_largest_problem_and_one_token_more(moe):
     d, I, E, k = 1024, 1024, 16, 4
     T = _largest_T(moe, d, I, E, k)
-    _compare(moe, make_layer(T=T, d=d, I=I, E=E, k=k, seed=25), 0, f"largest T={T}")
+    _compare(moe, make_layer(T=T, d=d, I=I, E=E, k=k, seed=25), DET, f"largest T={T}")
     L = make_layer(T=T + 1, d=d, I=I, E=E, k=k, seed=26)
     D = to_device(L)
     out = torch.empty(L.T, L.d, dtype=torch.float32, device="cuda")
@@ -113,4 +113,4 @@ def test_noalloc_check_reports_a_timed_out_wait(moe):
     finally:
         moe.set_fault_injection(moe.FAULT_NONE)
     assert _check_raw(moe) == 0
-    _compare(moe, L, TC, "after the fault")
+    _compare(moe, L, TC | DET, "after the fault")
