@@ -402,9 +402,12 @@ __device__ __forceinline__ void stream_consume(const StreamParams& P, const Stre
       }
     }
     // the warps sharing a tile add their partial sums; the exit decision on an
-    // abort is taken jointly (barrier with an OR vote) so no barrier is left waiting
+    // abort is taken jointly (barrier with an OR vote) so no barrier is left
+    // waiting.  With the combine in the W2 epilogue each warp adds its own
+    // partial sums into out (the order of the additions is free), no exchange.
+    const bool pair_sum = W13 || !P.out;
     bool aborted = *abort_flag;
-    if (kKSplit > 1) {
+    if (kKSplit > 1 && pair_sum) {
       if (kpart > 0)
         red[((rbuf * (kKSplit - 1) + kpart - 1) * kTiles + tile) * 32 + lane] = make_float4(acc[0], acc[1], acc[2], acc[3]);
       uint32_t any;
@@ -426,7 +429,7 @@ __device__ __forceinline__ void stream_consume(const StreamParams& P, const Stre
       }
       rbuf ^= 1;
     }
-    if (aborted || kpart > 0) continue;  // keep meeting the chunk barriers, no output
+    if (aborted || (pair_sum && kpart > 0)) continue;  // keep meeting the chunk barriers, no output
     // epilogue: acc[0..1] = row A x tokens 2t, 2t+1; acc[2..3] = row B
     const int t0 = 2 * t, t1 = 2 * t + 1;
     const float s0 = tok_scale[t0], s1 = tok_scale[t1];

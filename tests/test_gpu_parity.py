@@ -183,11 +183,13 @@ def test_epilogue_combine_matches_slot_order_combine(moe, shape):
         b = run_gpu(moe, L, flags | DET)
         assert torch.equal(a["h"], b["h"]) and torch.equal(a["sorted_slot"], b["sorted_slot"])
         x, y = a["out"].cpu().numpy().astype(np.float64), b["out"].cpu().numpy().astype(np.float64)
-        # each term w * y is within 2^-24 of its fp32 value and k partial sums
-        # round at 2^-24 each: bound the difference by 2 k 2^-24 sum_j |term|,
-        # taken generously as 2 k 2^-24 k max|out| per token
+        # the epilogue adds up to 2k fp32 terms per element (the streaming
+        # kernel's two K halves of each slot separately), each rounded at 2^-24
+        # like every partial sum: bound the difference by 4 k 2^-24 times the
+        # terms' magnitude, taken as k max|out| of the token
         scale = np.abs(y).max(axis=1, keepdims=True) + 1e-30
-        assert (np.abs(x - y) <= 2 * L.k * L.k * 2.0 ** -24 * scale + 1e-30).all(), f"flags {flags}"
+        assert (np.abs(x - y) <= 4 * L.k * L.k * 2.0 ** -24 * scale).all(), f"flags {flags}"
+        assert np.linalg.norm(x - y) <= 1e-6 * np.linalg.norm(y), f"flags {flags}"
 
 
 def test_route_entry_point(moe):
@@ -422,4 +424,4 @@ def test_cuda_graph_capture_replays_bit_identical(moe, flags):
         # in no fixed order: each replay gives the layer once, up to fp32 rounding
         x, y = out.cpu().numpy().astype(np.float64), eager.cpu().numpy().astype(np.float64)
         scale = np.abs(y).max(axis=1, keepdims=True)
-        assert (np.abs(x - y) <= 2 * L.k * L.k * 2.0 ** -24 * scale).all()
+        assert (np.abs(x - y) <= 4 * L.k * L.k * 2.0 ** -24 * scale).all()
