@@ -61,6 +61,11 @@ def test_bad_arguments_are_rejected_on_the_host(lib):
     # unknown flags
     rc = lib.moe_fp4_forward(ctypes.byref(d), *args, *none, 0x80, P(fake), 1 << 30, None)
     assert rc == -1
+    rc = lib.moe_fp4_forward(ctypes.byref(d), *args, *none, 0x20, P(fake), 1 << 30, None)
+    assert rc == -1
+    # the slot-order combine flag is a known flag: the call gets as far as the workspace check
+    rc = lib.moe_fp4_forward(ctypes.byref(d), *args, *none, moe.FLAG_DETERMINISTIC, P(fake), 64, None)
+    assert rc == -3
     # both path flags
     rc = lib.moe_fp4_forward(ctypes.byref(d), *args, *none, 0x3, P(fake), 1 << 30, None)
     assert rc == -1
