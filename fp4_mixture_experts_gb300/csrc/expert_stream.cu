@@ -10,9 +10,9 @@
 //     scales) into a shared-memory ring guarded by full/empty mbarriers;
 //   - 16 consumer warps: each 16-row tile (W13: 8 gate rows and the 8
 //     matching up rows, so SwiGLU stays in-thread; W2: 16 output rows) is
-//     shared by two warps, each taking half of the stage's MX blocks; the
-//     pair adds its partial sums once per item through shared memory.  A
-//     chunk's token rows (up to 8) sit in shared memory as f16 scaled by a
+//     shared by two warps, each taking half of the stage's MX blocks; for
+//     W13 (and W2 writing y) the pair adds its partial sums once per item
+//     through shared memory.  A chunk's token rows (up to 8) sit in shared memory as f16 scaled by a
 //     power of two per token (every bf16 value within 2^31 of the row maximum
 //     is exact, smaller ones round at 2^-39 of it);
 //   - per 32-element MX block a thread loads 4 packed bytes of each of its
@@ -24,8 +24,11 @@
 //     identically for A and B); two MMAs give the block's sums (f16 x f16
 //     products are exact, accumulation fp32), which are scaled by 2^(s-127)
 //     in fp32 and accumulated, so every E8M0 value is handled exactly;
-//   - the W13 epilogue applies SwiGLU and rounds h to bf16, the W2 epilogue
-//     writes fp32 y.
+//   - the W13 epilogue applies SwiGLU and rounds h to bf16 (the W13 kernel
+//     also zeroes out while it waits for the routing); the W2 epilogue adds
+//     each warp's half-K sums, times the slot's routing weight, into the
+//     token's fp32 out row (atomic adds), or writes fp32 y for the slot-order
+//     combine pass.
 // Waits are bounded; a timeout raises the CTA abort flag, after which every
 // warp runs the same loop without waiting (its arithmetic discarded), so all
 // barriers are still met and the kernel exits; the producer waits (also
