@@ -96,6 +96,19 @@ def test_single_token(moe, flags):
     full_check(moe, make_layer(T=1, d=1024, I=1024, E=8, k=2, seed=5), flags)
 
 
+@pytest.mark.parametrize("flags", [GEMV, TC, GEMV | DET, TC | DET])
+def test_against_the_cpp_oracle(moe, flags):
+    """The same checks against the second CPU oracle (plain C++ loops)"""
+    from oracle import cpp_ref
+    L = make_layer(T=24, d=1024, I=1024, E=12, k=3, seed=36)
+    ref = cpp_ref.forward(L.x_bf16, L.router_logits, L.w13, L.w13_scale, L.w2, L.w2_scale, L.k)
+    ref["slot_pos"] = np.argsort(ref["sorted_slot"]).astype(np.int32)
+    r = run_gpu(moe, L, flags)
+    check_routing(r, ref)
+    check_h(r, ref, L)
+    assert_out_within(r["out"].cpu().numpy(), ref["out"], L, what=f"C++ oracle, flags={flags}")
+
+
 @pytest.mark.parametrize("flags", [GEMV, TC])
 def test_top1_and_single_expert(moe, flags):
     full_check(moe, make_layer(T=20, d=1024, I=1024, E=6, k=1, seed=6), flags)
