@@ -40,6 +40,8 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 STAGES = ["route", "gather", "w13_swiglu", "w2", "combine"]
+# flags of every exact-layer call (bench --deterministic: the slot-order combine pass)
+LAYER_FLAGS = 0
 
 
 def peaks():
@@ -216,18 +218,20 @@ def measure_workload(name, steps, warmup, dist, local, sampler=None):
     for row in evs:
         for ev in row:
             ev.record(stream)
-    r = moe.forward(x, logits, w13, w13s, w2, w2s, L.k, out=out, workspace=ws, return_routing=True)
+    r = moe.forward(x, logits, w13, w13s, w2, w2s, L.k, out=out, workspace=ws, return_routing=True,
+                    flags=LAYER_FLAGS)
     torch.cuda.synchronize()
     ids = r["topk_ids"].cpu().numpy()
     touched = int(np.unique(ids).size)
     for _ in range(warmup):
-        moe.forward(x, logits, w13, w13s, w2, w2s, L.k, out=out, workspace=ws)
+        moe.forward(x, logits, w13, w13s, w2, w2s, L.k, out=out, workspace=ws, flags=LAYER_FLAGS)
     barrier(dist)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     t_wall0 = time.time()
     start.record(stream)
     for s in range(steps):
-        moe.forward(x, logits, w13, w13s, w2, w2s, L.k, out=out, workspace=ws, stage_events=evs[s])
+        moe.forward(x, logits, w13, w13s, w2, w2s, L.k, out=out, workspace=ws, stage_events=evs[s],
+                    flags=LAYER_FLAGS)
     end.record(stream)
     barrier(dist)
     t_wall1 = time.time()
@@ -241,10 +245,10 @@ def measure_workload(name, steps, warmup, dist, local, sampler=None):
     side = torch.cuda.Stream(dev)
     side.wait_stream(stream)
     with torch.cuda.stream(side):
-        moe.forward(x, logits, w13, w13s, w2, w2s, L.k, out=out, workspace=ws)
+        moe.forward(x, logits, w13, w13s, w2, w2s, L.k, out=out, workspace=ws, flags=LAYER_FLAGS)
     stream.wait_stream(side)
     with torch.cuda.graph(graph):
-        moe.forward(x, logits, w13, w13s, w2, w2s, L.k, out=out, workspace=ws)
+        moe.forward(x, logits, w13, w13s, w2, w2s, L.k, out=out, workspace=ws, flags=LAYER_FLAGS)
     for _ in range(warmup):
         graph.replay()
     barrier(dist)
@@ -277,11 +281,11 @@ def measure_e2e(res, steps, warmup, dist, local):
     dev = torch.device("cuda", local)
     wsh = torch.empty(moe.host_workspace_bytes(L.T, L.d, L.I, L.E, L.k), dtype=torch.uint8, device=dev)
     for _ in range(warmup):
-        moe.forward_host(xh, lh, w13, w13s, w2, w2s, L.k, out_host=oh, workspace=wsh)
+        moe.forward_host(xh, lh, w13, w13s, w2, w2s, L.k, out_host=oh, workspace=wsh, flags=LAYER_FLAGS)
     barrier(dist)
     t0 = time.perf_counter()
     for _ in range(steps):
-        moe.forward_host(xh, lh, w13, w13s, w2, w2s, L.k, out_host=oh, workspace=wsh)
+        moe.forward_host(xh, lh, w13, w13s, w2, w2s, L.k, out_host=oh, workspace=wsh, flags=LAYER_FLAGS)
     barrier(dist)
     dt = max_over_ranks(dist, time.perf_counter() - t0)
     h2d = L.x_bf16.nbytes + L.router_logits.nbytes
@@ -507,8 +511,9 @@ def run_ours(args):
     ms_step = dec["ms_total"] / args.steps
     value = world * L.T * args.steps / (dec["ms_total"] * 1e-3)
     # decode path: route_small (routing + sort in one cluster launch), W13 + SwiGLU (which also
-    # zeroes out), W2 with the weighted combine in its epilogue
-    launches_per_step = 3
+    # zeroes out), W2 with the weighted combine in its epilogue; --deterministic: W2 writes y
+    # and the combine pass is a fourth launch
+    launches_per_step = 4 if LAYER_FLAGS else 3
     line = {
         "metric": "routed-MoE tokens/s (decode T=32, prefill T=4608); % of HBM/tensor roofline",
         "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -517,6 +522,8 @@ def run_ours(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "fp4(e2m1)xbf16->f32", "data": "synthetic",
         "config": decode_config(world),
         "launch": "one layer call captured in a CUDA graph, replayed per step",
+        "combine": ("slot-order pass (deterministic)" if LAYER_FLAGS
+                    else "in the W2 epilogue (fp32 atomic adds, summation order not fixed)"),
         "stage_ms": {k: round(v, 5) for k, v in dec["stage_ms"].items()},
         "roofline": roofline_decode(dec, pk, src),
         "gpu_launches": launches_per_step * args.steps,
@@ -545,7 +552,7 @@ def run_ours(args):
         # one more layer call on the measured decode tensors, checked against the oracle's sample
         x, logits, w13, w13s, w2, w2s, _ = dec["tensors"]
         import fp4_mixture_experts_gb300 as moe
-        r = moe.forward(x, logits, w13, w13s, w2, w2s, L.k, return_routing=True)
+        r = moe.forward(x, logits, w13, w13s, w2, w2s, L.k, return_routing=True, flags=LAYER_FLAGS)
         torch.cuda.synchronize()
         gpu = {"out": r["out"].cpu().numpy(), "topk_ids": r["topk_ids"].cpu().numpy()}
         line["cpu_baseline"] = cpu_baseline_sample("decode", args.cpu_seconds, gpu)
@@ -626,7 +633,10 @@ def run_profile_case(args):
     ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
     out = torch.empty(L.T, L.d, dtype=torch.float32, device="cuda")
     for _ in range(args.warmup + args.steps):
-        (moe.forward_mx if mx else moe.forward)(*args_, out=out, workspace=ws)
+        if mx:
+            moe.forward_mx(*args_, out=out, workspace=ws)
+        else:
+            moe.forward(*args_, out=out, workspace=ws, flags=LAYER_FLAGS)
     torch.cuda.synchronize()
     moe.check(ws)
     print(f"profile case {args.profile_case}: T={L.T} d={L.d} I={L.I} E={L.E} k={L.k}, "
@@ -646,10 +656,15 @@ def main():
     ap.add_argument("--no-mx-layer", action="store_true",
                     help="skip timing the layer with MXFP8 activations (block-scaled tensor cores) at prefill")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--deterministic", action="store_true",
+                    help="run the exact layer with the slot-order combine pass (bitwise reproducible) instead "
+                         "of the combine in the W2 epilogue")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--profile-case", choices=sorted(PROFILE_CASES), default=None,
                     help="only run forward passes of one case (for ncu), no measurement")
     args = ap.parse_args()
+    global LAYER_FLAGS
+    LAYER_FLAGS = 0x10 if args.deterministic else 0  # MOE_FP4_FLAG_DETERMINISTIC
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     for n in [n for n in args.also.split(",") if n]:
