@@ -15,7 +15,9 @@
  *   3. for every expert, multiplies its tokens by the packed-FP4 W13 (gate and
  *      up) and applies SwiGLU, h = bf16(silu(g) * u);
  *   4. multiplies h by the packed-FP4 W2 (down) and combines the k expert
- *      outputs of each token with its routing weights, in slot order.
+ *      outputs of each token with its routing weights (by default added into
+ *      out in the W2 kernel's epilogue in no fixed order; in slot order with
+ *      MOE_FP4_FLAG_DETERMINISTIC).
  *
  * Formats (MXFP4, OCP Microscaling v1.0):
  *   - weights: two E2M1 codes per byte along K, the LOW nibble holds the even
@@ -182,8 +184,9 @@ int moe_fp4_forward_gated(const moe_fp4_dims* dims, const void* x_bf16, const vo
  *   events[1] before the token gather (tensor-core path only; else empty)
  *   events[2] before W13 + SwiGLU
  *   events[3] before W2
- *   events[4] before the combine
- *   events[5] after the combine
+ *   events[4] before the combine pass
+ *   events[5] after the combine pass (empty when the W2 kernel does the
+ *   combine in its epilogue, the default)
  * Same arguments, checks and results as moe_fp4_forward. */
 #define MOE_FP4_NUM_STAGE_EVENTS 6
 int moe_fp4_forward_profiled(const moe_fp4_dims* dims, const void* x_bf16, const float* router_logits,
