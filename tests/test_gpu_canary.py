@@ -89,8 +89,13 @@ def test_forward_writes_only_inside_its_buffers(moe, shape, flags):
     torch.cuda.synchronize()
     if flags & DET:
         assert torch.equal(g["out"].view(torch.float32, (T, d)), ref["out"])
-    else:  # the epilogue combine adds the k terms in no fixed order
-        torch.testing.assert_close(g["out"].view(torch.float32, (T, d)), ref["out"], rtol=1e-5, atol=1e-5)
+    else:
+        # the epilogue combine adds the k terms (the streaming kernel: 2k half-K
+        # terms) in no fixed order: equal up to fp32 rounding of the partial sums
+        x = g["out"].view(torch.float32, (T, d)).cpu().double().numpy()
+        y = ref["out"].cpu().double().numpy()
+        scale = np.abs(y).max(axis=1, keepdims=True)
+        assert (np.abs(x - y) <= 4 * k * k * 2.0 ** -24 * scale).all()
     assert torch.equal(g["ids"].view(torch.int32, (T, k)), ref["topk_ids"])
     assert torch.equal(g["w"].view(torch.float32, (T, k)), ref["topk_weights"])
     assert torch.equal(g["off"].view(torch.int32, (E + 1,)), ref["expert_offsets"])
